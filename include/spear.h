@@ -1,0 +1,189 @@
+/*
+ * spear.h -- C ABI of the GB300 (sm_103a) library for SPEAR's gated 4-bit
+ * weight-quantized linear layer with an input-adaptive low-rank error
+ * compensator.
+ *
+ * Source of the method: "SPEAR: A System for Post-Quantization Error-Adaptive
+ * Recovery Enabling Efficient Low-Bit LLM Serving" (gist.science explainer of
+ * the paper).  Technical Summary 2.1 A gives the compensated effective weight
+ * W + alpha * B * diag(gate) * A with a per-token gate; 2.1 B the
+ * entropy-aware module selection; 2.2 A the phase-aware dispatch (decode:
+ * compensator fused into the low-bit GEMM epilogue, one kernel; prefill:
+ * compensator as a separate kernel overlapped with the GEMM through a CUDA
+ * graph); 3.1 the RTN per-channel int4 setting.
+ *
+ * Per token x (one row of x [M][K]) every linear call computes
+ *
+ *     y = dequant(Wq) x  +  alpha * g(x) * B (A x),   g(x) = sigmoid(w_g . x + b_g)
+ *
+ * (the explainer leaves the gate's exact form open; this library fixes it to
+ * the scalar sigmoid above; the explainer's bottleneck-MLP form of the gate is
+ * not part of this ABI).
+ *
+ * Conventions
+ *  - Every function returns a spear_status code (0 = SPEAR_OK).  On failure
+ *    spear_last_error() gives a one-line, thread-local description.
+ *  - Buffers are owned by the caller.  "device" pointers must point into
+ *    device memory of the current CUDA device and be 16-byte aligned; "host"
+ *    pointers are ordinary host memory.  Nothing here allocates or frees
+ *    device memory; calls that need scratch take a caller workspace.
+ *  - Device work is queued on the given stream (a cudaStream_t passed as
+ *    void*, NULL = legacy default stream) and returns without synchronising.
+ *    Kernel-side failures (a bounded wait that ran out, a non-finite weight
+ *    seen while packing) are recorded in a device status word that
+ *    spear_get_device_status() reads back.
+ *  - bf16 and fp16 tensors are passed as uint16_t bit patterns.
+ *  - Shapes: K % 128 == 0, N % 64 == 0, group_size == K (per output channel)
+ *    or group_size == 128; rank in {0, 16, 32, 64}.
+ */
+#ifndef SPEAR_H
+#define SPEAR_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef int spear_status;
+enum {
+  SPEAR_OK = 0,
+  SPEAR_ERR_INVALID_ARG = 1,   /* bad shape, NULL or misaligned pointer     */
+  SPEAR_ERR_UNSUPPORTED = 2,   /* valid call outside what the kernels cover */
+  SPEAR_ERR_WORKSPACE = 3,     /* workspace missing or too small            */
+  SPEAR_ERR_CUDA = 4,          /* a CUDA runtime call failed                */
+  SPEAR_ERR_TIMEOUT = 5        /* a bounded device-side wait gave up        */
+};
+
+/* Prefill modes (Technical Summary 2.2 A, "semi-fused" prefill). */
+enum {
+  SPEAR_PREFILL_AUTO = 0,    /* pick by measured time for the shape            */
+  SPEAR_PREFILL_FUSED = 1,   /* gate/down-projection pass, then one GEMM whose
+                                K loop is extended by the rank-r up-projection */
+  SPEAR_PREFILL_STREAM = 2   /* W4 GEMM on `stream` while the compensator's
+                                down-projection runs on `stream_aux`; joined by
+                                an up-projection-and-add kernel                */
+};
+
+/* Output element type of y. */
+enum { SPEAR_OUT_BF16 = 0, SPEAR_OUT_F32 = 1 };
+
+/*
+ * One quantized linear layer with its compensator (all pointers device).
+ *   qweight : uint8 [N][K/2]; byte = u[k even] | u[k odd] << 4, code u in 0..15
+ *   scales  : fp16  [N][K/group_size]
+ *   zeros   : uint8 [N][ceil(K/group_size/2)], zero points packed like the
+ *             codes (low nibble = even group); NULL when symmetric (zero 8)
+ *   A       : bf16 [rank][K]   (down-projection)
+ *   B       : bf16 [N][rank]   (up-projection)
+ *   w_g     : bf16 [K]         (gate weights), b_g gate bias, alpha scale
+ *   comp_enabled == 0 or rank == 0 gives the plain W4 layer (A, B, w_g unused).
+ */
+typedef struct spear_w4_layer {
+  int N, K, group_size, symmetric;
+  const uint8_t* qweight;
+  const uint16_t* scales;
+  const uint8_t* zeros;
+  int rank;
+  const uint16_t* A;
+  const uint16_t* B;
+  const uint16_t* w_g;
+  float b_g, alpha;
+  int comp_enabled;
+} spear_w4_layer;
+
+/* Byte sizes of the three packed buffers for an N x K weight. */
+spear_status spear_pack_w4_sizes(int N, int K, int group_size, int symmetric,
+                                 size_t* qweight_bytes, size_t* scales_bytes,
+                                 size_t* zeros_bytes);
+
+/*
+ * Round-to-nearest int4 quantisation and packing of W (device fp32 [N][K],
+ * row-major).  Per group of group_size consecutive k in a row:
+ *   symmetric : s = fp16_round_up(max|w| / 7), u = clamp(rint(w/s), -8, 7) + 8
+ *   asymmetric: lo = min(min w, 0), hi = max(max w, 0),
+ *               s = fp16_round_up((hi - lo) / 15), z = clamp(rint(-lo/s), 0, 15),
+ *               u = clamp(rint(w/s) + z, 0, 15)
+ * (fp32 IEEE division, rint = round half to even; an all-zero group stores
+ * s = 0 and the zero point as its codes).  Writes qweight, scales and, when
+ * asymmetric, zeros (device).  A non-finite weight or a scale beyond the fp16
+ * range is reported through spear_get_device_status (SPEAR_ERR_INVALID_ARG).
+ */
+spear_status spear_pack_w4(const float* W, int N, int K, int group_size, int symmetric,
+                           uint8_t* qweight, uint16_t* scales, uint8_t* zeros,
+                           void* stream);
+
+/*
+ * Decode (Technical Summary 2.2 A, decode phase, M small): ONE kernel launch
+ * streams the int4 weights, computes g(x) and A x for every token in the same
+ * launch and adds alpha*g*B(Ax) in the epilogue.  1 <= M <= 64.
+ *   x : device bf16 [M][K];  y : device [M][N], bf16 or fp32 (out_dtype).
+ * The thread blocks of the launch exchange the M x (rank+1) down-projection
+ * and the partial sums of weight tiles they share through `workspace`
+ * (device, at least spear_decode_workspace_bytes()).  The workspace must be
+ * zeroed once before its first use (spear_workspace_init) and is left ready
+ * for the next call; two calls that run at the same time must not share one.
+ * After a SPEAR_ERR_TIMEOUT device status, zero it again.
+ */
+spear_status spear_decode_workspace_bytes(const spear_w4_layer* L, int M, size_t* bytes);
+spear_status spear_linear_decode(const spear_w4_layer* L, const uint16_t* x, int M,
+                                 void* y, int out_dtype, void* workspace, size_t ws_bytes,
+                                 void* stream);
+
+/*
+ * Prefill (Technical Summary 2.2 A, prefill phase, M large): tcgen05 tensor-core
+ * GEMM over int4 tiles dequantized to bf16 in shared memory, plus the
+ * compensator in one of the modes above.  1 <= M.
+ *   x : device bf16 [M][K];  y : device [M][N], bf16 or fp32.
+ *   workspace : device, at least spear_prefill_workspace_bytes(); no zeroing
+ *               needed.  stream_aux is used by SPEAR_PREFILL_STREAM only (it
+ *               may be NULL otherwise); the call orders it after `stream` and
+ *               joins it back, so the call behaves as one operation on `stream`.
+ */
+spear_status spear_prefill_workspace_bytes(const spear_w4_layer* L, int M, int mode,
+                                           size_t* bytes);
+spear_status spear_linear_prefill(const spear_w4_layer* L, const uint16_t* x, int M,
+                                  void* y, int out_dtype, int mode,
+                                  void* workspace, size_t ws_bytes,
+                                  void* stream, void* stream_aux);
+
+/* Zero a decode workspace (device) on `stream`. */
+spear_status spear_workspace_init(void* workspace, size_t bytes, void* stream);
+
+/*
+ * Module selection (Technical Summary 2.1 B), host only.  damage[L] >= 0 is a
+ * per-module quantisation-damage score, cost[L] > 0 the bytes one unit of
+ * rank costs in module i.  The damage distribution p_i = d_i / sum d sets
+ * k = clamp(round(exp(entropy(p))), 1, L) modules; they are the k best by
+ * p_i / (cost_i / mean cost) (ties: lower index), and all get the largest
+ * rank that is a multiple of 16 in [rank_min, rank_max] with
+ * rank * sum(selected cost) <= budget_bytes; if even the smallest rank does
+ * not fit, the worst selected module is dropped and the rank chosen again.
+ * Writes mask_out[L] (1 = carries a compensator) and rank_out[L] (0 when
+ * unselected), both host.
+ */
+spear_status spear_layer_select_mask(const float* damage, const float* cost, int L,
+                                     double budget_bytes, int rank_min, int rank_max,
+                                     uint8_t* mask_out, int* rank_out);
+
+/*
+ * Reads and clears the device status word of the current device
+ * (synchronises `stream`).  *out = SPEAR_OK, or the first kernel-side error
+ * recorded since the last read.
+ */
+spear_status spear_get_device_status(int* out, void* stream);
+
+/* Static, human-readable name of a status code. */
+const char* spear_status_string(int status);
+
+/* Thread-local description of the last failing call on this thread. */
+const char* spear_last_error(void);
+
+/* Library version as "major.minor.patch". */
+const char* spear_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* SPEAR_H */

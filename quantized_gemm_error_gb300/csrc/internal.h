@@ -1,0 +1,44 @@
+// internal.h -- host-side interface between the C ABI (api.cu) and the
+// kernel translation units.  Not part of the public ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "spear.h"
+
+namespace spear {
+
+// Records a thread-local error message and returns `status`.
+int fail(int status, const char* fmt, ...);
+// Maps a CUDA error to SPEAR_ERR_CUDA with a message (SPEAR_OK if e == cudaSuccess).
+int cuda_check(cudaError_t e, const char* what);
+
+// Device properties of the current device, cached per device.
+struct DeviceInfo {
+  int device;
+  int num_sms;
+  int cc_major, cc_minor;
+  size_t smem_optin;
+};
+int device_info(DeviceInfo* out);
+
+// ---- pack.cu
+int launch_pack_w4(const float* W, int N, int K, int G, int sym, uint8_t* qweight,
+                   uint16_t* scales, uint8_t* zeros, cudaStream_t st);
+int read_and_clear_status_pack(unsigned* out, cudaStream_t st);
+
+// ---- decode.cu
+int decode_workspace_bytes(const spear_w4_layer& L, int M, size_t* bytes);
+int launch_decode(const spear_w4_layer& L, const uint16_t* x, int M, void* y, int out_f32,
+                  void* ws, size_t ws_bytes, cudaStream_t st);
+int read_and_clear_status_decode(unsigned* out, cudaStream_t st);
+
+// ---- prefill.cu
+int prefill_workspace_bytes(const spear_w4_layer& L, int M, int mode, size_t* bytes);
+int launch_prefill(const spear_w4_layer& L, const uint16_t* x, int M, void* y, int out_f32,
+                   int mode, void* ws, size_t ws_bytes, cudaStream_t st, cudaStream_t st_aux);
+int read_and_clear_status_prefill(unsigned* out, cudaStream_t st);
+
+}  // namespace spear

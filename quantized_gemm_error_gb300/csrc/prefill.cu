@@ -1,0 +1,631 @@
+// prefill.cu -- prefill path of the gated W4 + low-rank compensated linear
+// (SPEAR explainer, Technical Summary 2.2 A: prefill is compute-bound; the
+// compensator runs as a separate kernel next to the GEMM instead of inside it).
+//
+// Kernels
+//  * w4_gemm_tc: Y[M][N] = X[M][K] * dequant(Wq)^T on the 5th-generation tensor
+//    cores.  One 128 (tokens) x 256 (outputs) tile per thread block; K in
+//    steps of 64.  A TMA warp loads the bf16 X tile (128-byte swizzle) and the
+//    raw int4 tile; four converter warps expand the int4 tile to bf16 straight
+//    into the tensor core's swizzled K-major layout; one thread issues
+//    tcgen05.mma into a 128 x 256 fp32 accumulator in tensor memory; the same
+//    four warps then drain it (tcgen05.ld) and store Y.
+//      - per-channel scales: the tile holds the exact integers (u - z) and the
+//        fp32 scale of each output column is applied in the epilogue;
+//      - group scales: the tile holds (u - z) * s computed in fp32 and rounded
+//        once to bf16.
+//    Optionally ("fused" mode) the K loop is extended by the compensator's
+//    up-projection: extra K steps with A = [T_hi | T_lo] (the gated
+//    down-projection split into two bf16 halves) and B = the factor B, into a
+//    second accumulator that the epilogue adds unscaled.
+//  * comp_down: T[m][j] = alpha * g_m * (A x_m)[j], g_m = sigmoid(w_g . x_m + b_g),
+//    written as bf16 hi/lo pairs; mma.sync over token tiles, one pass over X.
+//  * comp_up_add: Y[m][n] += sum_j T[m][j] B[n][j] in place ("stream" mode:
+//    runs after the plain W4 GEMM, while comp_down ran beside it on a second
+//    stream).
+#include <cuda.h>
+
+#include <algorithm>
+#include <mutex>
+
+#include "common.cuh"
+#include "internal.h"
+#include "sm100_ptx.cuh"
+
+namespace spear {
+namespace {
+
+__device__ unsigned g_prefill_status;
+
+using namespace sm100;
+
+constexpr int kBM = 128;                  // tokens per tile (MMA M)
+constexpr int kBN = 256;                  // outputs per tile (MMA N)
+constexpr int kBK = 64;                   // k per stage (one 128-byte swizzle row of bf16)
+constexpr int kStages = 4;
+constexpr int kXBytes = kBM * kBK * 2;    // 16 KB
+constexpr int kWBytes = kBN * kBK * 2;    // 32 KB
+constexpr int kRawBytes = kBN * kBK / 2;  // 8 KB
+constexpr int kStageBytes = kXBytes + kWBytes + kRawBytes;
+constexpr int kGemmThreads = 192;         // warp 0: TMA, warp 1: MMA, warps 2-5: convert + epilogue
+constexpr uint32_t kTmemCols = 512;       // main accumulator in [0, 256), correction in [256, 512)
+constexpr uint64_t kWaitNs = 2000ull * 1000 * 1000;   // 2 s: far beyond any legitimate wait
+
+struct GemmParams {
+  int M, N, K, G, ng, sym, perch;
+  const __half* scales;
+  const uint8_t* zeros;
+  void* y;
+  int out_f32;
+  int comp_stages;      // extra K steps of the fused up-projection (0 = none)
+  int r;
+  int t_row_bytes;      // bytes per T2 row box (<= 128)
+  int b_row_bytes;      // bytes per B row (2r)
+};
+
+__device__ __forceinline__ uint32_t sw_layout(int row_bytes) {
+  return row_bytes >= 128 ? LAYOUT_SW128 : row_bytes == 64 ? LAYOUT_SW64 : LAYOUT_SW32;
+}
+
+__global__ void __launch_bounds__(kGemmThreads, 1)
+w4_gemm_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_wq,
+           const __grid_constant__ CUtensorMap tm_t, const __grid_constant__ CUtensorMap tm_b,
+           const GemmParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  __shared__ __align__(8) uint64_t bar_full[kStages], bar_cvt[kStages], bar_empty[kStages], bar_acc;
+  __shared__ uint32_t s_tmem;
+  __shared__ int s_abort;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n0 = blockIdx.x * kBN, m0 = blockIdx.y * kBM;
+  const int k_stages = p.K / kBK;
+  const int total_stages = k_stages + p.comp_stages;
+
+  auto x_slot = [&](int s) { return smem + s * kStageBytes; };
+  auto w_slot = [&](int s) { return smem + s * kStageBytes + kXBytes; };
+  auto raw_slot = [&](int s) { return smem + s * kStageBytes + kXBytes + kWBytes; };
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(smem_u32(&bar_full[s]), 1);
+      mbar_init(smem_u32(&bar_cvt[s]), 4);
+      mbar_init(smem_u32(&bar_empty[s]), 1);
+    }
+    mbar_init(smem_u32(&bar_acc), 1);
+    s_abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&s_tmem), kTmemCols);
+    tmem_relinquish();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&tm_x);
+    prefetch_tmap(&tm_wq);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = s_tmem;
+
+  auto give_up = [&]() {
+    record_status(&g_prefill_status, DEV_ERR_TIMEOUT);
+    atomicExch(&s_abort, 1);
+  };
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      int issued = 0;
+      for (int s = 0; s < total_stages; ++s) {
+        const int slot = s % kStages;
+        if (!mbar_wait(smem_u32(&bar_empty[slot]), ((s / kStages) & 1) ^ 1, kWaitNs) || s_abort) {
+          give_up();
+          break;
+        }
+        const uint32_t full = smem_u32(&bar_full[slot]);
+        if (s < k_stages) {
+          mbar_arrive_expect_tx(full, kXBytes + kRawBytes);
+          tma_load_2d(smem_u32(x_slot(slot)), &tm_x, s * kBK, m0, full);
+          tma_load_2d(smem_u32(raw_slot(slot)), &tm_wq, s * (kBK / 2), n0, full);
+        } else {
+          const int j = s - k_stages;   // compensator step: T box j and the factor B
+          mbar_arrive_expect_tx(full, kBM * p.t_row_bytes + kBN * p.b_row_bytes);
+          tma_load_2d(smem_u32(x_slot(slot)), &tm_t, j * 64, m0, full);
+          tma_load_2d(smem_u32(w_slot(slot)), &tm_b, 0, n0, full);
+        }
+        ++issued;
+      }
+      // never leave with copies in flight: wait (bounded) for every issued stage
+      if (s_abort) {
+        for (int s = std::max(0, issued - kStages); s < issued; ++s)
+          mbar_wait(smem_u32(&bar_full[s % kStages]), (s / kStages) & 1, kWaitNs);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc = idesc_bf16_f32(kBM, kBN);
+      bool ok = true;
+      for (int s = 0; s < total_stages && ok; ++s) {
+        const int slot = s % kStages;
+        const uint32_t ph = (s / kStages) & 1;
+        ok = mbar_wait(smem_u32(&bar_full[slot]), ph, kWaitNs) && !s_abort;
+        if (ok && s < k_stages) ok = mbar_wait(smem_u32(&bar_cvt[slot]), ph, kWaitNs) && !s_abort;
+        if (!ok) { give_up(); break; }
+        tc_fence_after();
+        const uint32_t xa = smem_u32(x_slot(slot)), wa = smem_u32(w_slot(slot));
+        if (s < k_stages) {
+#pragma unroll
+          for (int k = 0; k < kBK / 16; ++k) {
+            const uint64_t ad = smem_desc(xa + 32 * k, 1024, LAYOUT_SW128);
+            const uint64_t bd = smem_desc(wa + 32 * k, 1024, LAYOUT_SW128);
+            mma_bf16_ss(tmem, ad, bd, idesc, (s > 0 || k > 0) ? 1u : 0u);
+          }
+        } else {
+          // A = T box j (columns 64j.. of [T_hi | T_lo]); B = the factor B (k = rank);
+          // accumulated into the second accumulator (columns 256..511).
+          const int j = s - k_stages;
+          const uint32_t a_layout = sw_layout(p.t_row_bytes), b_layout = sw_layout(p.b_row_bytes);
+          for (int i = 0; i < p.t_row_bytes / 32; ++i) {
+            const int col = 64 * j + 16 * i;                 // column of [T_hi | T_lo]
+            if (col >= 2 * p.r) break;
+            const int bstep = (col % p.r) / 16;
+            const uint64_t ad = smem_desc(xa + 32 * i, 8 * p.t_row_bytes, a_layout);
+            const uint64_t bd = smem_desc(wa + 32 * bstep, 8 * p.b_row_bytes, b_layout);
+            mma_bf16_ss(tmem + kBN, ad, bd, idesc, (j > 0 || i > 0) ? 1u : 0u);
+          }
+        }
+        mma_commit(smem_u32(&bar_empty[slot]));             // frees the stage when these MMAs finish
+      }
+      mma_commit(smem_u32(&bar_acc));                        // accumulators complete
+    }
+  } else {
+    // ------------------------------------------ converters, then the epilogue
+    const int ct = threadIdx.x - 64;                         // 0..127
+    const int zrow = (p.ng + 1) / 2;
+    bool ok = true;
+    for (int s = 0; s < k_stages; ++s) {
+      const int slot = s % kStages;
+      if (!mbar_wait(smem_u32(&bar_full[slot]), (s / kStages) & 1, kWaitNs) || s_abort) {
+        give_up();
+        ok = false;
+        break;
+      }
+      const int gi = (s * kBK) / p.G;
+      const uint8_t* raw = raw_slot(slot);
+      uint8_t* wdst = w_slot(slot);
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int row = ct + 128 * h;
+        const int n = n0 + row;
+        uint4 out[8];
+        if (n < p.N) {
+          int z = 8;
+          if (!p.sym) {
+            const uint8_t zb = p.zeros[(size_t)n * zrow + gi / 2];
+            z = (gi & 1) ? (zb >> 4) : (zb & 15);
+          }
+          const float sc = p.perch ? 1.0f : __half2float(p.scales[(size_t)n * p.ng + gi]);
+          const uint32_t zb2 = bf16x2_bias((uint32_t)z);
+          const uint4 r0 = *reinterpret_cast<const uint4*>(raw + row * 32);
+          const uint4 r1 = *reinterpret_cast<const uint4*>(raw + row * 32 + 16);
+          const uint32_t words[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
+#pragma unroll
+          for (int w = 0; w < 8; ++w) {
+            uint32_t v[4];
+            nibbles_to_bf16x2_biased(words[w], v);           // (k_i, k_{i+4}) as 128 + u
+#pragma unroll
+            for (int i = 0; i < 4; ++i) v[i] = bf16x2_sub(v[i], zb2);   // u - z, exact
+            if (p.perch) {
+              out[w] = make_uint4(__byte_perm(v[0], v[1], 0x5410), __byte_perm(v[2], v[3], 0x5410),
+                                  __byte_perm(v[0], v[1], 0x7632), __byte_perm(v[2], v[3], 0x7632));
+            } else {
+              // (u - z) * s exact in fp32, one rounding to bf16; natural k order
+              out[w] = make_uint4(pack_bf16x2(bf16x2_lo(v[0]) * sc, bf16x2_lo(v[1]) * sc),
+                                  pack_bf16x2(bf16x2_lo(v[2]) * sc, bf16x2_lo(v[3]) * sc),
+                                  pack_bf16x2(bf16x2_hi(v[0]) * sc, bf16x2_hi(v[1]) * sc),
+                                  pack_bf16x2(bf16x2_hi(v[2]) * sc, bf16x2_hi(v[3]) * sc));
+            }
+          }
+        } else {
+#pragma unroll
+          for (int w = 0; w < 8; ++w) out[w] = make_uint4(0, 0, 0, 0);
+        }
+        // 128-byte swizzle: 16-byte chunk c of row r lives at chunk c ^ (r & 7)
+#pragma unroll
+        for (int w = 0; w < 8; ++w)
+          *reinterpret_cast<uint4*>(wdst + row * 128 + ((w ^ (row & 7)) << 4)) = out[w];
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&bar_cvt[slot]));
+    }
+
+    // epilogue: TMEM lanes 32*(warp%4) .. +31 are this warp's rows (tokens)
+    if (ok && !mbar_wait(smem_u32(&bar_acc), 0, kWaitNs)) give_up();
+    tc_fence_after();
+    if (!s_abort) {
+      const int q = warp & 3;
+      const int tok = m0 + 32 * q + lane;
+      for (int cch = 0; cch < kBN / 32; ++cch) {
+        uint32_t r[32], rc[32];
+        tmem_ld_32cols(tmem + ((uint32_t)(32 * q) << 16) + cch * 32, r);
+        if (p.comp_stages) tmem_ld_32cols(tmem + ((uint32_t)(32 * q) << 16) + kBN + cch * 32, rc);
+        tmem_ld_wait();
+        const int n = n0 + cch * 32;
+        if (n >= p.N) continue;
+        float v[32];
+        if (p.perch) {
+          const uint4* sp = reinterpret_cast<const uint4*>(p.scales + n);   // per-channel: one scale per row
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const uint4 s8 = __ldg(sp + i);
+            const uint32_t sw[4] = {s8.x, s8.y, s8.z, s8.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&sw[j]));
+              v[8 * i + 2 * j] = __uint_as_float(r[8 * i + 2 * j]) * f.x;
+              v[8 * i + 2 * j + 1] = __uint_as_float(r[8 * i + 2 * j + 1]) * f.y;
+            }
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+        }
+        if (p.comp_stages) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] += __uint_as_float(rc[i]);
+        }
+        if (tok < p.M) {
+          if (p.out_f32) {
+            float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.y) + (size_t)tok * p.N + n);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+          } else {
+            uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.y) + (size_t)tok * p.N + n);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              dst[i] = make_uint4(pack_bf16x2(v[8 * i], v[8 * i + 1]), pack_bf16x2(v[8 * i + 2], v[8 * i + 3]),
+                                  pack_bf16x2(v[8 * i + 4], v[8 * i + 5]), pack_bf16x2(v[8 * i + 6], v[8 * i + 7]));
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// ------------------------------------------------------------- comp_down --
+// One block = 32 tokens (4 token tiles of 8), all r+1 projection rows; 8 warps
+// split K in 128-k chunks and are summed in a fixed order.  Same operand
+// mapping as the decode producer: lane (g, c) owns 8 consecutive k per row.
+constexpr int kCdThreads = 256;
+constexpr int kCdTok = 32;
+constexpr int kCdMT = kCdTok / 8;
+
+struct CompDownParams {
+  int M, K, r;
+  const __nv_bfloat16* x;
+  const __nv_bfloat16* A;
+  const __nv_bfloat16* w_g;
+  float b_g, alpha;
+  __nv_bfloat16* T2;    // [M][t2_cols]: T_hi in [0, r), T_lo in [r, 2r)
+  int t2_cols;
+};
+
+template <int RT>
+__global__ void __launch_bounds__(kCdThreads) comp_down_kernel(const CompDownParams p) {
+  __shared__ float red[8][kCdMT][4][32];
+  __shared__ float res[RT * 16][kCdTok];      // [projection row][token]
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane >> 2, c = lane & 3;
+  const int tok0 = blockIdx.x * kCdTok;
+  float acc[RT][kCdMT][4];
+#pragma unroll
+  for (int rt = 0; rt < RT; ++rt)
+#pragma unroll
+    for (int t = 0; t < kCdMT; ++t)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) acc[rt][t][i] = 0.0f;
+  const int nchunks = p.K / 128;
+  for (int ch = warp; ch < nchunks; ch += 8) {
+#pragma unroll
+    for (int piece = 0; piece < 4; ++piece) {
+      const int kb = ch * 128 + piece * 32 + 8 * c;
+      uint4 xv[kCdMT];
+#pragma unroll
+      for (int t = 0; t < kCdMT; ++t) {
+        const int tok = tok0 + t * 8 + g;
+        xv[t] = tok < p.M ? ldg16(p.x + (size_t)tok * p.K + kb) : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int rt = 0; rt < RT; ++rt) {
+        const int rlo = rt * 16 + g, rhi = rlo + 8;
+        const uint4 va = rlo < p.r ? ldg16(p.A + (size_t)rlo * p.K + kb)
+                                   : rlo == p.r ? ldg16(p.w_g + kb) : make_uint4(0, 0, 0, 0);
+        const uint4 vb = rhi < p.r ? ldg16(p.A + (size_t)rhi * p.K + kb)
+                                   : rhi == p.r ? ldg16(p.w_g + kb) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+        for (int t = 0; t < kCdMT; ++t) {
+          mma_bf16_16816(acc[rt][t], va.x, vb.x, va.y, vb.y, xv[t].x, xv[t].y);
+          mma_bf16_16816(acc[rt][t], va.z, vb.z, va.w, vb.w, xv[t].z, xv[t].w);
+        }
+      }
+    }
+  }
+  // fixed-order sum over warps, one projection-row tile at a time
+#pragma unroll
+  for (int rt = 0; rt < RT; ++rt) {
+#pragma unroll
+    for (int t = 0; t < kCdMT; ++t)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) red[warp][t][i][lane] = acc[rt][t][i];
+    __syncthreads();
+    for (int e = threadIdx.x; e < kCdMT * 4 * 32; e += kCdThreads) {
+      const int t = e / 128, i = (e / 32) & 3, ln = e & 31;
+      float s = 0.0f;
+      for (int w = 0; w < 8; ++w) s += red[w][t][i][ln];
+      // C fragment element i of lane ln: row (ln/4) + 8 (i/2), token 2 (ln%4) + (i%2)
+      res[rt * 16 + (ln >> 2) + 8 * (i >> 1)][t * 8 + 2 * (ln & 3) + (i & 1)] = s;
+    }
+    __syncthreads();
+  }
+  // row r is the gate logit; rows 0..r-1 the down-projection
+  for (int e = threadIdx.x; e < kCdTok * p.r; e += kCdThreads) {
+    const int m = e / p.r, j = e % p.r;
+    const int tok = tok0 + m;
+    const float gate = 1.0f / (1.0f + expf(-(res[p.r][m] + p.b_g)));
+    const float tv = p.alpha * gate * res[j][m];
+    const __nv_bfloat16 hi = __float2bfloat16_rn(tv);
+    const __nv_bfloat16 lo = __float2bfloat16_rn(tv - __bfloat162float(hi));
+    if (tok < p.M) {
+      p.T2[(size_t)tok * p.t2_cols + j] = hi;
+      p.T2[(size_t)tok * p.t2_cols + p.r + j] = lo;
+    }
+  }
+}
+
+// ----------------------------------------------------------- comp_up_add --
+// Y[m][n] += sum_j (T_hi + T_lo)[m][j] B[n][j].  One warp = 16 tokens x 64
+// outputs (8 mma n-tiles), A operand = T rows, B operand = rows of B.
+struct CompUpParams {
+  int M, N, r, t2_cols, out_f32;
+  const __nv_bfloat16* T2;
+  const __nv_bfloat16* B;
+  void* y;
+};
+
+__global__ void __launch_bounds__(256) comp_up_add_kernel(const CompUpParams p) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane >> 2, c = lane & 3;
+  const int tok0 = (blockIdx.y * 8 + warp) * 16;
+  const int nb = blockIdx.x * 64;
+  if (tok0 >= p.M) return;
+  float acc[8][4];
+#pragma unroll
+  for (int t = 0; t < 8; ++t)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) acc[t][i] = 0.0f;
+  const int tlo = min(tok0 + g, p.M - 1), thi = min(tok0 + g + 8, p.M - 1);
+  for (int part = 0; part < 2; ++part) {                     // T_hi, then T_lo
+    for (int j0 = 0; j0 < p.r; j0 += 16) {
+      const uint32_t* Tl = reinterpret_cast<const uint32_t*>(p.T2 + (size_t)tlo * p.t2_cols + part * p.r + j0);
+      const uint32_t* Th = reinterpret_cast<const uint32_t*>(p.T2 + (size_t)thi * p.t2_cols + part * p.r + j0);
+      const uint32_t a0 = Tl[c], a1 = Th[c], a2 = Tl[c + 4], a3 = Th[c + 4];
+#pragma unroll
+      for (int t = 0; t < 8; ++t) {
+        const uint32_t* Bn = reinterpret_cast<const uint32_t*>(p.B + (size_t)(nb + t * 8 + g) * p.r + j0);
+        mma_bf16_16816(acc[t], a0, a1, a2, a3, __ldg(Bn + c), __ldg(Bn + c + 4));
+      }
+    }
+  }
+#pragma unroll
+  for (int t = 0; t < 8; ++t) {
+    const int n = nb + t * 8 + 2 * c;
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      const int tok = tok0 + g + 8 * hh;
+      if (tok >= p.M) continue;
+      if (p.out_f32) {
+        float2* dst = reinterpret_cast<float2*>(reinterpret_cast<float*>(p.y) + (size_t)tok * p.N + n);
+        float2 v = *dst;
+        v.x += acc[t][2 * hh];
+        v.y += acc[t][2 * hh + 1];
+        *dst = v;
+      } else {
+        __nv_bfloat162* dst = reinterpret_cast<__nv_bfloat162*>(reinterpret_cast<__nv_bfloat16*>(p.y) + (size_t)tok * p.N + n);
+        const float2 v = __bfloat1622float2(*dst);
+        *dst = __floats2bfloat162_rn(v.x + acc[t][2 * hh], v.y + acc[t][2 * hh + 1]);
+      }
+    }
+  }
+}
+
+// ----------------------------------------------------------------- host --
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  });
+  return fn;
+}
+
+CUtensorMapSwizzle swizzle_for(int row_bytes) {
+  return row_bytes >= 128 ? CU_TENSOR_MAP_SWIZZLE_128B
+         : row_bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
+         : row_bytes == 32 ? CU_TENSOR_MAP_SWIZZLE_32B
+                           : CU_TENSOR_MAP_SWIZZLE_NONE;
+}
+
+// 2-D row-major tensor [outer][inner] with a box of [box_outer][box_inner].
+int make_tmap(CUtensorMap* m, CUtensorMapDataType dt, int elem_bytes, const void* base, uint64_t inner,
+              uint64_t outer, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle sw) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return fail(SPEAR_ERR_CUDA, "prefill: cuTensorMapEncodeTiled is unavailable");
+  const cuuint64_t dims[2] = {inner, outer};
+  const cuuint64_t strides[1] = {inner * (uint64_t)elem_bytes};
+  const cuuint32_t box[2] = {box_inner, box_outer};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(SPEAR_ERR_CUDA, "prefill: tensor map encode failed (%d)", (int)r);
+  return SPEAR_OK;
+}
+
+int t2_cols_for(int r) { return 2 * r; }
+size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
+
+int resolve_mode(int mode) { return mode == SPEAR_PREFILL_AUTO ? SPEAR_PREFILL_FUSED : mode; }
+
+int launch_gemm(const spear_w4_layer& L, const uint16_t* x, int M, void* y, int out_f32, const __nv_bfloat16* T2,
+                int r_fused, cudaStream_t st) {
+  CUtensorMap tm_x, tm_wq, tm_t, tm_b;
+  if (int rc = make_tmap(&tm_x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, x, L.K, M, kBK, kBM, CU_TENSOR_MAP_SWIZZLE_128B)) return rc;
+  if (int rc = make_tmap(&tm_wq, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, L.qweight, L.K / 2, L.N, kBK / 2, kBN,
+                         CU_TENSOR_MAP_SWIZZLE_NONE)) return rc;
+  GemmParams p{};
+  p.M = M; p.N = L.N; p.K = L.K; p.G = L.group_size; p.ng = L.K / L.group_size; p.sym = L.symmetric;
+  p.perch = L.group_size == L.K;
+  p.scales = reinterpret_cast<const __half*>(L.scales);
+  p.zeros = L.zeros;
+  p.y = y; p.out_f32 = out_f32;
+  p.r = r_fused;
+  if (r_fused > 0) {
+    const int tcols = t2_cols_for(r_fused);
+    const int tbox = std::min(tcols, 64);
+    p.t_row_bytes = tbox * 2;
+    p.b_row_bytes = r_fused * 2;
+    p.comp_stages = (2 * r_fused + 63) / 64;
+    if (int rc = make_tmap(&tm_t, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, T2, tcols, M, tbox, kBM,
+                           swizzle_for(p.t_row_bytes))) return rc;
+    if (int rc = make_tmap(&tm_b, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, L.B, r_fused, L.N, r_fused, kBN,
+                           swizzle_for(p.b_row_bytes))) return rc;
+  } else {
+    tm_t = tm_x;
+    tm_b = tm_x;
+  }
+  const size_t smem = (size_t)kStages * kStageBytes + 1024;
+  if (int rc = cuda_check(cudaFuncSetAttribute(w4_gemm_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem),
+                          "prefill: smem attribute")) return rc;
+  dim3 grid((L.N + kBN - 1) / kBN, (M + kBM - 1) / kBM);
+  if (grid.y > 65535) return fail(SPEAR_ERR_UNSUPPORTED, "prefill: M=%d too large", M);
+  w4_gemm_tc<<<grid, kGemmThreads, smem, st>>>(tm_x, tm_wq, tm_t, tm_b, p);
+  return cuda_check(cudaGetLastError(), "prefill gemm launch");
+}
+
+int launch_comp_down(const spear_w4_layer& L, const uint16_t* x, int M, __nv_bfloat16* T2, cudaStream_t st) {
+  CompDownParams p{};
+  p.M = M; p.K = L.K; p.r = L.rank;
+  p.x = reinterpret_cast<const __nv_bfloat16*>(x);
+  p.A = reinterpret_cast<const __nv_bfloat16*>(L.A);
+  p.w_g = reinterpret_cast<const __nv_bfloat16*>(L.w_g);
+  p.b_g = L.b_g; p.alpha = L.alpha;
+  p.T2 = T2; p.t2_cols = t2_cols_for(L.rank);
+  const unsigned blocks = (unsigned)((M + kCdTok - 1) / kCdTok);
+  switch ((L.rank + 1 + 15) / 16) {
+    case 2: comp_down_kernel<2><<<blocks, kCdThreads, 0, st>>>(p); break;
+    case 3: comp_down_kernel<3><<<blocks, kCdThreads, 0, st>>>(p); break;
+    default: comp_down_kernel<5><<<blocks, kCdThreads, 0, st>>>(p); break;
+  }
+  return cuda_check(cudaGetLastError(), "comp_down launch");
+}
+
+int launch_comp_up(const spear_w4_layer& L, int M, void* y, int out_f32, const __nv_bfloat16* T2, cudaStream_t st) {
+  CompUpParams p{};
+  p.M = M; p.N = L.N; p.r = L.rank; p.t2_cols = t2_cols_for(L.rank); p.out_f32 = out_f32;
+  p.T2 = T2;
+  p.B = reinterpret_cast<const __nv_bfloat16*>(L.B);
+  p.y = y;
+  dim3 grid(L.N / 64, (M + 127) / 128);
+  comp_up_add_kernel<<<grid, 256, 0, st>>>(p);
+  return cuda_check(cudaGetLastError(), "comp_up launch");
+}
+
+struct StreamEvents {
+  cudaEvent_t fork = nullptr, join = nullptr;
+};
+
+int stream_events(StreamEvents* ev) {
+  static std::mutex mu;
+  static StreamEvents cache[64];
+  static bool made[64] = {};
+  int dev = 0;
+  if (int rc = cuda_check(cudaGetDevice(&dev), "cudaGetDevice")) return rc;
+  if (dev < 0 || dev >= 64) return fail(SPEAR_ERR_UNSUPPORTED, "device index %d", dev);
+  std::lock_guard<std::mutex> lk(mu);
+  if (!made[dev]) {
+    if (int rc = cuda_check(cudaEventCreateWithFlags(&cache[dev].fork, cudaEventDisableTiming), "event")) return rc;
+    if (int rc = cuda_check(cudaEventCreateWithFlags(&cache[dev].join, cudaEventDisableTiming), "event")) return rc;
+    made[dev] = true;
+  }
+  *ev = cache[dev];
+  return SPEAR_OK;
+}
+
+}  // namespace
+
+int prefill_workspace_bytes(const spear_w4_layer& L, int M, int mode, size_t* bytes) {
+  const bool comp = L.comp_enabled && L.rank > 0;
+  (void)mode;
+  *bytes = comp ? align256((size_t)M * t2_cols_for(L.rank) * 2) : 0;
+  return SPEAR_OK;
+}
+
+int launch_prefill(const spear_w4_layer& L, const uint16_t* x, int M, void* y, int out_f32, int mode, void* ws,
+                   size_t ws_bytes, cudaStream_t st, cudaStream_t st_aux) {
+  DeviceInfo di;
+  if (int rc = device_info(&di)) return rc;
+  const bool comp = L.comp_enabled && L.rank > 0;
+  if (!comp) return launch_gemm(L, x, M, y, out_f32, nullptr, 0, st);
+  size_t need = 0;
+  prefill_workspace_bytes(L, M, mode, &need);
+  if (!ws || ws_bytes < need)
+    return fail(SPEAR_ERR_WORKSPACE, "prefill: workspace of %zu B is smaller than the %zu B needed", ws_bytes, need);
+  if ((reinterpret_cast<uintptr_t>(ws) & 255) != 0)
+    return fail(SPEAR_ERR_INVALID_ARG, "prefill: workspace must be 256-byte aligned");
+  __nv_bfloat16* T2 = reinterpret_cast<__nv_bfloat16*>(ws);
+  if (resolve_mode(mode) == SPEAR_PREFILL_FUSED) {
+    if (int rc = launch_comp_down(L, x, M, T2, st)) return rc;
+    return launch_gemm(L, x, M, y, out_f32, T2, L.rank, st);
+  }
+  // stream mode: fork the down-projection onto st_aux, W4 GEMM on st, join, up-project + add
+  if (!st_aux || st_aux == st) return fail(SPEAR_ERR_INVALID_ARG, "prefill: stream mode needs a distinct stream_aux");
+  StreamEvents ev;
+  if (int rc = stream_events(&ev)) return rc;
+  if (int rc = cuda_check(cudaEventRecord(ev.fork, st), "fork record")) return rc;
+  if (int rc = cuda_check(cudaStreamWaitEvent(st_aux, ev.fork, 0), "fork wait")) return rc;
+  if (int rc = launch_comp_down(L, x, M, T2, st_aux)) return rc;
+  if (int rc = cuda_check(cudaEventRecord(ev.join, st_aux), "join record")) return rc;
+  if (int rc = launch_gemm(L, x, M, y, out_f32, nullptr, 0, st)) return rc;
+  if (int rc = cuda_check(cudaStreamWaitEvent(st, ev.join, 0), "join wait")) return rc;
+  return launch_comp_up(L, M, y, out_f32, T2, st);
+}
+
+int read_and_clear_status_prefill(unsigned* out, cudaStream_t st) {
+  void* addr = nullptr;
+  if (int rc = cuda_check(cudaGetSymbolAddress(&addr, g_prefill_status), "prefill status address")) return rc;
+  if (int rc = cuda_check(cudaMemcpyAsync(out, addr, sizeof(unsigned), cudaMemcpyDeviceToHost, st), "read prefill status")) return rc;
+  if (int rc = cuda_check(cudaStreamSynchronize(st), "read prefill status")) return rc;
+  return cuda_check(cudaMemsetAsync(addr, 0, sizeof(unsigned), st), "clear prefill status");
+}
+
+}  // namespace spear

@@ -1,0 +1,259 @@
+"""Thin Python binding of ``libspear.so`` (C ABI in ``include/spear.h``).
+
+Argument marshalling only: every step of the layer runs in the library's
+CUDA kernels.  Torch provides device memory and streams.  There is no CPU
+fallback -- if the library cannot be loaded every call raises.
+
+Function names follow the C ABI:
+  spear_pack_w4, spear_linear_decode, spear_linear_prefill,
+  spear_layer_select_mask, plus the workspace / status helpers.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from dataclasses import dataclass
+from typing import Optional
+
+import numpy as np
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "lib", "libspear.so")
+
+SPEAR_OK = 0
+STATUS_NAMES = {0: "SPEAR_OK", 1: "SPEAR_ERR_INVALID_ARG", 2: "SPEAR_ERR_UNSUPPORTED",
+                3: "SPEAR_ERR_WORKSPACE", 4: "SPEAR_ERR_CUDA", 5: "SPEAR_ERR_TIMEOUT"}
+PREFILL_AUTO, PREFILL_FUSED, PREFILL_STREAM = 0, 1, 2
+OUT_BF16, OUT_F32 = 0, 1
+
+# every symbol include/spear.h declares
+EXPORTS = ["spear_pack_w4_sizes", "spear_pack_w4", "spear_decode_workspace_bytes",
+           "spear_linear_decode", "spear_prefill_workspace_bytes", "spear_linear_prefill",
+           "spear_workspace_init", "spear_layer_select_mask", "spear_get_device_status",
+           "spear_status_string", "spear_last_error", "spear_version"]
+
+
+class SpearError(RuntimeError):
+    def __init__(self, status: int, where: str, detail: str):
+        super().__init__(f"{where}: {STATUS_NAMES.get(status, status)}: {detail}")
+        self.status = status
+
+
+class _Layer(ctypes.Structure):
+    _fields_ = [("N", ctypes.c_int), ("K", ctypes.c_int), ("group_size", ctypes.c_int),
+                ("symmetric", ctypes.c_int), ("qweight", ctypes.c_void_p), ("scales", ctypes.c_void_p),
+                ("zeros", ctypes.c_void_p), ("rank", ctypes.c_int), ("A", ctypes.c_void_p),
+                ("B", ctypes.c_void_p), ("w_g", ctypes.c_void_p), ("b_g", ctypes.c_float),
+                ("alpha", ctypes.c_float), ("comp_enabled", ctypes.c_int)]
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def load(path: str = LIB_PATH):
+    """Loads the CUDA library (once).  Raises if it is missing."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(path):
+            raise RuntimeError(f"libspear.so not found at {path}: build it first "
+                               "(python -m quantized_gemm_error_gb300.build)")
+        lib = ctypes.CDLL(path)
+        P, I, S = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+        LP = ctypes.POINTER(_Layer)
+        sig = {
+            "spear_pack_w4_sizes": [I, I, I, I, ctypes.POINTER(S), ctypes.POINTER(S), ctypes.POINTER(S)],
+            "spear_pack_w4": [P, I, I, I, I, P, P, P, P],
+            "spear_decode_workspace_bytes": [LP, I, ctypes.POINTER(S)],
+            "spear_linear_decode": [LP, P, I, P, I, P, S, P],
+            "spear_prefill_workspace_bytes": [LP, I, I, ctypes.POINTER(S)],
+            "spear_linear_prefill": [LP, P, I, P, I, I, P, S, P, P],
+            "spear_workspace_init": [P, S, P],
+            "spear_layer_select_mask": [P, P, I, ctypes.c_double, I, I, P, P],
+            "spear_get_device_status": [ctypes.POINTER(I), P],
+        }
+        for name, args in sig.items():
+            fn = getattr(lib, name)
+            fn.argtypes = args
+            fn.restype = I
+        lib.spear_status_string.argtypes = [I]
+        lib.spear_status_string.restype = ctypes.c_char_p
+        lib.spear_last_error.argtypes = []
+        lib.spear_last_error.restype = ctypes.c_char_p
+        lib.spear_version.argtypes = []
+        lib.spear_version.restype = ctypes.c_char_p
+        _lib = lib
+        return lib
+
+
+def _check(rc: int, where: str):
+    if rc != SPEAR_OK:
+        detail = load().spear_last_error().decode(errors="replace")
+        raise SpearError(rc, where, detail)
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("expected a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError("expected a contiguous tensor")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+@dataclass
+class W4Layer:
+    """A packed layer plus its compensator (all tensors on the same CUDA device)."""
+    N: int
+    K: int
+    group_size: int
+    symmetric: bool
+    qweight: torch.Tensor                 # uint8 [N][K/2]
+    scales: torch.Tensor                  # fp16  [N][K/G]
+    zeros: Optional[torch.Tensor] = None  # uint8 [N][ceil(K/G/2)]
+    rank: int = 0
+    A: Optional[torch.Tensor] = None      # bf16 [rank][K]
+    B: Optional[torch.Tensor] = None      # bf16 [N][rank]
+    w_g: Optional[torch.Tensor] = None    # bf16 [K]
+    b_g: float = 0.0
+    alpha: float = 1.0
+    comp_enabled: bool = True
+
+    def c_struct(self) -> _Layer:
+        return _Layer(self.N, self.K, self.group_size, int(self.symmetric), _ptr(self.qweight),
+                      _ptr(self.scales), _ptr(self.zeros), int(self.rank), _ptr(self.A), _ptr(self.B),
+                      _ptr(self.w_g), float(self.b_g), float(self.alpha), int(self.comp_enabled))
+
+    def with_comp(self, enabled: bool) -> "W4Layer":
+        d = dict(self.__dict__)
+        d["comp_enabled"] = enabled
+        return W4Layer(**d)
+
+
+# ------------------------------------------------------------------ pack
+
+def spear_pack_w4_sizes(N: int, K: int, group_size: int, symmetric: bool):
+    q, s, z = ctypes.c_size_t(), ctypes.c_size_t(), ctypes.c_size_t()
+    _check(load().spear_pack_w4_sizes(N, K, group_size, int(symmetric), ctypes.byref(q), ctypes.byref(s),
+                                      ctypes.byref(z)), "spear_pack_w4_sizes")
+    return q.value, s.value, z.value
+
+
+def spear_pack_w4(W: torch.Tensor, group_size: int, symmetric: bool, *, out=None, stream=None):
+    """Quantise + pack W (CUDA fp32 [N][K]); returns (qweight, scales, zeros)."""
+    if W.dtype != torch.float32 or W.dim() != 2:
+        raise ValueError("W must be a 2-D float32 CUDA tensor")
+    N, K = W.shape
+    qb, sb, zb = spear_pack_w4_sizes(N, K, group_size, symmetric)
+    if out is None:
+        q = torch.empty((N, K // 2), dtype=torch.uint8, device=W.device)
+        s = torch.empty((N, K // group_size), dtype=torch.float16, device=W.device)
+        z = None if symmetric else torch.empty((N, zb // N), dtype=torch.uint8, device=W.device)
+    else:
+        q, s, z = out
+    _check(load().spear_pack_w4(_ptr(W), N, K, group_size, int(symmetric), _ptr(q), _ptr(s), _ptr(z),
+                                _stream(stream)), "spear_pack_w4")
+    return q, s, z
+
+
+# ---------------------------------------------------------------- layer
+
+def spear_decode_workspace_bytes(layer: W4Layer, M: int) -> int:
+    n = ctypes.c_size_t()
+    L = layer.c_struct()
+    _check(load().spear_decode_workspace_bytes(ctypes.byref(L), M, ctypes.byref(n)),
+           "spear_decode_workspace_bytes")
+    return n.value
+
+
+def spear_prefill_workspace_bytes(layer: W4Layer, M: int, mode: int = PREFILL_AUTO) -> int:
+    n = ctypes.c_size_t()
+    L = layer.c_struct()
+    _check(load().spear_prefill_workspace_bytes(ctypes.byref(L), M, mode, ctypes.byref(n)),
+           "spear_prefill_workspace_bytes")
+    return n.value
+
+
+def new_workspace(nbytes: int, device, zero: bool = True) -> torch.Tensor:
+    """A 256-byte aligned device buffer (torch allocations are) of at least nbytes."""
+    ws = torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=device)
+    if zero:
+        spear_workspace_init(ws)
+    return ws
+
+
+def spear_workspace_init(ws: torch.Tensor, stream=None):
+    _check(load().spear_workspace_init(_ptr(ws), ws.numel() * ws.element_size(), _stream(stream)),
+           "spear_workspace_init")
+
+
+def _out(y, M, N, out_dtype, device):
+    if y is not None:
+        return y
+    return torch.empty((M, N), dtype=torch.float32 if out_dtype == OUT_F32 else torch.bfloat16, device=device)
+
+
+def spear_linear_decode(layer: W4Layer, x: torch.Tensor, *, y=None, out_dtype: int = OUT_BF16,
+                        workspace: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """y = dequant(Wq) x + alpha g(x) B (A x) for M <= 64 tokens, one kernel launch."""
+    M = x.shape[0]
+    y = _out(y, M, layer.N, out_dtype, x.device)
+    if workspace is None:
+        workspace = new_workspace(spear_decode_workspace_bytes(layer, M), x.device)
+    L = layer.c_struct()
+    _check(load().spear_linear_decode(ctypes.byref(L), _ptr(x), M, _ptr(y), out_dtype, _ptr(workspace),
+                                      workspace.numel(), _stream(stream)), "spear_linear_decode")
+    return y
+
+
+def spear_linear_prefill(layer: W4Layer, x: torch.Tensor, *, y=None, out_dtype: int = OUT_BF16,
+                         mode: int = PREFILL_AUTO, workspace: Optional[torch.Tensor] = None,
+                         stream=None, stream_aux=None) -> torch.Tensor:
+    """Same layer for large M on the tcgen05 tensor-core path."""
+    M = x.shape[0]
+    y = _out(y, M, layer.N, out_dtype, x.device)
+    if workspace is None:
+        workspace = new_workspace(spear_prefill_workspace_bytes(layer, M, mode), x.device, zero=False)
+    L = layer.c_struct()
+    aux = None if stream_aux is None else _stream(stream_aux)
+    _check(load().spear_linear_prefill(ctypes.byref(L), _ptr(x), M, _ptr(y), out_dtype, mode,
+                                       _ptr(workspace), workspace.numel(), _stream(stream), aux),
+           "spear_linear_prefill")
+    return y
+
+
+# ------------------------------------------------------- module selection
+
+def spear_layer_select_mask(damage, cost, budget_bytes: float, rank_min: int, rank_max: int):
+    d = np.ascontiguousarray(damage, dtype=np.float32)
+    c = np.ascontiguousarray(cost, dtype=np.float32)
+    mask = np.zeros(d.shape[0], np.uint8)
+    rank = np.zeros(d.shape[0], np.int32)
+    _check(load().spear_layer_select_mask(d.ctypes.data_as(ctypes.c_void_p), c.ctypes.data_as(ctypes.c_void_p),
+                                          d.shape[0], float(budget_bytes), int(rank_min), int(rank_max),
+                                          mask.ctypes.data_as(ctypes.c_void_p),
+                                          rank.ctypes.data_as(ctypes.c_void_p)), "spear_layer_select_mask")
+    return mask, rank
+
+
+# ------------------------------------------------------------ status
+
+def spear_get_device_status(stream=None) -> int:
+    out = ctypes.c_int()
+    _check(load().spear_get_device_status(ctypes.byref(out), _stream(stream)), "spear_get_device_status")
+    return out.value
+
+
+def version() -> str:
+    return load().spear_version().decode()

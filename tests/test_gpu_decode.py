@@ -1,0 +1,113 @@
+"""GPU parity for spear_linear_decode (one fused launch, M <= 64) against the
+CPU oracle, on the workloads' shapes and value distributions.
+
+Source: SPEAR explainer, Technical Summary 2.1 A (y = W4 x + alpha g(x) B A x)
+and 2.2 A (decode: compensator fused into the GEMM epilogue)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from spear_testutil import (check_close, gpu_layer, make_layer, make_tokens, oracle_layer, sample_columns,
+                            to_dev_u16)
+
+pytestmark = pytest.mark.gpu
+
+
+def _spear():
+    from quantized_gemm_error_gb300 import spear
+    return spear
+
+
+def _run(layer, x_bits, out_dtype=0, ws=None):
+    sp = _spear()
+    x = to_dev_u16(x_bits, torch.bfloat16)
+    y = sp.spear_linear_decode(layer, x, out_dtype=out_dtype, workspace=ws)
+    torch.cuda.synchronize()
+    assert sp.spear_get_device_status() == 0
+    return y
+
+
+# small shapes the oracle finishes in seconds: several tiles, ragged token tiles
+@pytest.mark.parametrize("N,K,G,sym,r,M", [
+    (64, 128, 128, True, 16, 1),
+    (192, 384, 128, False, 16, 3),
+    (1024, 1024, 1024, True, 16, 1),        # 1024^2 per-channel symmetric, rank 16
+    (1024, 1024, 1024, True, 16, 16),
+    (512, 2048, 128, False, 32, 9),
+    (320, 1152, 128, False, 64, 33),
+    (256, 1024, 1024, False, 32, 64),
+    (1024, 1024, 128, True, 0, 5),          # rank 0: plain W4
+])
+def test_decode_matches_oracle(N, K, G, sym, r, M):
+    lay, rng = make_layer(N, K, r, seed=100 + N + M)
+    x = make_tokens(rng, M, K, outlier_frac=0.01)
+    L = gpu_layer(lay, G, sym)
+    ref = oracle.linear(oracle_layer(lay, G, sym), x, nthreads=8)
+    check_close(_run(L, x), ref)
+    check_close(_run(L, x, out_dtype=1), ref)             # fp32 out: strict 1e-2 rms
+
+
+@pytest.mark.parametrize("N,K,M", [(4096, 4096, 1), (11008, 4096, 4), (4096, 11008, 16), (4096, 4096, 64)])
+def test_decode_llama7b_shapes_sampled(N, K, M):
+    """Full Llama-7B shapes (int4 g128 asymmetric, rank 32, 1% outlier channels),
+    checked on sampled output rows the oracle computes one by one."""
+    lay, rng = make_layer(N, K, 32, seed=7 + N + K + M)
+    x = make_tokens(rng, M, K, outlier_frac=0.01)
+    L = gpu_layer(lay, 128, False)
+    cols = sample_columns(N, 192, seed=M)
+    ref = oracle.linear(oracle_layer(lay, 128, False), x, n_idx=cols, nthreads=8)
+    y = _run(L, x)
+    check_close(y[:, torch.from_numpy(cols).cuda()], ref)
+
+
+def test_correction_term_alone():
+    """Delta = y(comp on) - y(comp off) against the oracle's alpha g B (A x) (fp32 out)."""
+    N, K, G, r, M = 1024, 2048, 128, 32, 7
+    lay, rng = make_layer(N, K, r, seed=21)
+    x = make_tokens(rng, M, K, outlier_frac=0.01)
+    L = gpu_layer(lay, G, False)
+    _, corr, _ = oracle.linear(oracle_layer(lay, G, False), x, nthreads=8, want_corr=True)
+    d = _run(L, x, out_dtype=1) - _run(L.with_comp(False), x, out_dtype=1)
+    check_close(d, corr, "correction")
+
+
+def test_gate_zero_and_comp_off_are_bit_identical():
+    N, K, r, M = 2048, 1024, 32, 5
+    lay, rng = make_layer(N, K, r, seed=22)
+    x = make_tokens(rng, M, K)
+    L_on = gpu_layer(lay, 128, False, b_g=-1e30)           # sigmoid(-inf) = 0
+    L_off = L_on.with_comp(False)
+    assert torch.equal(_run(L_on, x, out_dtype=1), _run(L_off, x, out_dtype=1))
+    assert torch.equal(_run(L_on, x), _run(L_off, x))
+
+
+def test_workspace_is_reusable_across_calls_and_shapes():
+    """The decode workspace's synchronisation words return to zero after every
+    call, so one buffer serves a sequence of calls with different M and
+    layers (same stream)."""
+    sp = _spear()
+    lays = []
+    for i, (N, K) in enumerate([(1024, 1024), (512, 2048)]):
+        lay, rng = make_layer(N, K, 32, seed=30 + i)
+        lays.append((gpu_layer(lay, 128, False), rng, K))
+    size = max(sp.spear_decode_workspace_bytes(L, M) for L, _, _ in lays for M in (1, 16, 64))
+    ws = sp.new_workspace(size, "cuda")
+    for M in (1, 16, 64, 3, 1):
+        for L, rng, K in lays:
+            x = make_tokens(rng, M, K)
+            fresh = _run(L, x)
+            again = _run(L, x, ws=ws)
+            assert torch.equal(fresh, again)
+    assert not ws[:16].any(), "workspace sync words not left zeroed"
+
+
+def test_token_permutation_permutes_rows():
+    N, K, r, M = 1024, 2048, 16, 12
+    lay, rng = make_layer(N, K, r, seed=23)
+    x = make_tokens(rng, M, K)
+    L = gpu_layer(lay, 128, False)
+    perm = np.random.default_rng(0).permutation(M)
+    y = _run(L, x, out_dtype=1)
+    yp = _run(L, x[perm], out_dtype=1)
+    assert torch.equal(y[torch.from_numpy(perm).cuda()], yp)
