@@ -1,0 +1,520 @@
+"""Benchmark of the gated W4 + low-rank compensated linear on GB300.
+
+One step = one pass of the decode hot path over the Llama-7B decode workload:
+the three decoder linear shapes (K x N = 4096x4096, 4096x11008, 11008x4096),
+int4 group-128 asymmetric weights with uint4 zero points, rank-32
+compensator, each at M = 1, 4, 16 and 64 tokens (x ~ N(0,1) with 1% outlier
+channels x20): 12 fused decode launches.  The headline value is algorithmic
+HBM bytes of those 12 calls per second (GB/s).  A second measurement covers
+the prefill path (TFLOP/s) on the prefill workload (same shapes, M = 512,
+2048, 8192).
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+Under torchrun every rank runs its own replica of the workload (weak scaling);
+rank 0 prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "decode fused W4+comp GB/s (% HBM peak); prefill TFLOP/s (% bf16 peak)"
+DECODE_SHAPES = [(4096, 4096), (4096, 11008), (11008, 4096)]      # (K, N)
+DECODE_M = [1, 4, 16, 64]
+PREFILL_M = [512, 2048, 8192]
+G, SYM, RANK, OUTLIERS = 128, False, 32, 0.01
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def decode_bytes(K: int, N: int, M: int, r: int = RANK, comp: bool = True) -> int:
+    """Algorithmic HBM bytes of one decode call: codes, scales, zero points,
+    compensator factors (A, w_g, B), tokens in, outputs out."""
+    ng = K // G
+    b = N * K // 2 + N * ng * 2 + N * ((ng + 1) // 2) + M * K * 2 + M * N * 2
+    if comp:
+        b += (r + 1) * K * 2 + N * r * 2
+    return b
+
+
+def prefill_flops(K: int, N: int, M: int, r: int = RANK, comp: bool = True) -> int:
+    f = 2 * M * N * K
+    if comp:
+        f += 2 * M * r * (K + N) + 2 * M * K
+    return f
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.dev}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        mhz, maxmhz, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                mhz.append(float(parts[1]))
+                maxmhz.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        if not mhz:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": float(np.median(mhz)), "sm_max_mhz": float(max(maxmhz)),
+                "reasons": sorted(reasons), "samples": len(mhz)}
+
+
+# ------------------------------------------------------------- distributed
+
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        backend = "nccl" if (args.impl == "ours" and torch.cuda.is_available()) else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def reduce_max(value: float, world: int) -> float:
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------- oracle
+
+def oracle_case(K, N, M, seed, rows=None):
+    import oracle
+    from quantized_gemm_error_gb300.inputs import make_layer, make_tokens
+    lay, rng = make_layer(N, K, RANK, seed=seed)
+    x = make_tokens(rng, M, K, outlier_frac=OUTLIERS)
+    q, s, z = oracle.quantize_pack(lay.W, G, SYM)
+    L = dict(N=N, K=K, G=G, sym=SYM, qweight=q, scales=s, zeros=z, r=RANK, A=lay.A, B=lay.B, w_g=lay.w_g,
+             b_g=0.0, alpha=1.0, comp_enabled=1)
+    return L, x
+
+
+def time_oracle(cases, nthreads):
+    """Runs the oracle (as it stands) on each (layer, x, rows) case; returns
+    (seconds, algorithmic bytes covered)."""
+    import oracle
+    t0 = time.perf_counter()
+    nbytes = 0.0
+    for L, x, rows in cases:
+        oracle.linear(L, x, n_idx=rows, nthreads=nthreads)
+        K, N, M = L["K"], L["N"], x.shape[0]
+        frac = 1.0 if rows is None else len(rows) / N
+        nbytes += decode_bytes(K, N, M) * frac
+    return time.perf_counter() - t0, nbytes
+
+
+def cpu_baseline(row_fraction: float = 1.0):
+    """The oracle timed on this host's cores on a bounded sample of the decode
+    step: every (shape, M) call of the step, a fixed seeded subset of output
+    rows (row_fraction of N), fp64 accumulation; throughput scaled to the
+    metric's unit (algorithmic bytes of the rows covered per second)."""
+    nthreads = os.cpu_count() or 1
+    cases = []
+    rng = np.random.default_rng(0)
+    for (K, N) in DECODE_SHAPES:
+        for M in DECODE_M:
+            L, x = oracle_case(K, N, M, seed=K + N)
+            rows = np.sort(rng.choice(N, size=max(16, int(N * row_fraction)), replace=False)).astype(np.int32)
+            cases.append((L, x, rows))
+    secs, nbytes = time_oracle(cases, nthreads)
+    return {"value": nbytes / secs / 1e9, "unit": "GB/s", "cores": nthreads, "kind": "oracle",
+            "sample": f"the 12 decode calls of one step, {row_fraction:.4g} of each layer's output rows "
+                      f"(seeded), fp64 accumulation, {secs:.1f} s"}
+
+
+# ------------------------------------------------------------ reference arm
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return
+    nthreads = os.cpu_count() or 1
+    # size each step's sample so the whole run stays within about two minutes
+    probe_L, probe_x = oracle_case(4096, 4096, 1, seed=1)
+    rows = np.arange(64, dtype=np.int32)
+    dt, _ = time_oracle([(probe_L, probe_x, rows)], nthreads)
+    per_row_m1 = dt / 64
+    budget = 120.0 / max(1, args.steps + args.warmup)
+    cases = []
+    for (K, N) in DECODE_SHAPES:
+        for M in DECODE_M:
+            L, x = oracle_case(K, N, M, seed=K + N)
+            cases.append((L, x))
+    # cost of one row of one call ~ per_row_m1 * (K/4096) * (1 + M)/2; pick rows per case
+    est = sum(per_row_m1 * (L["K"] / 4096) * (1 + x.shape[0]) / 2 for L, x in cases)
+    rows_per_case = int(max(1, min(512, budget / max(est, 1e-9))))
+    rng = np.random.default_rng(0)
+    step_cases = [(L, x, np.sort(rng.choice(L["N"], rows_per_case, replace=False)).astype(np.int32))
+                  for L, x in cases]
+    for _ in range(args.warmup):
+        time_oracle(step_cases, nthreads)
+    total_s, total_b = 0.0, 0.0
+    for _ in range(args.steps):
+        s, b = time_oracle(step_cases, nthreads)
+        total_s += s
+        total_b += b
+    value = total_b / total_s / 1e9
+    sample = (f"each step: the 12 decode calls of the step on {rows_per_case} seeded output rows per "
+              f"call, fp64 accumulation")
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_s / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": "llama7b_decode_g128_r32"},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": nthreads, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+# -------------------------------------------------------------------- ours
+
+def build_decode(torch, spear, device, l2_bytes):
+    from quantized_gemm_error_gb300.inputs import make_layer, make_tokens
+
+    def dev16(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(device)
+
+    base = []
+    for (K, N) in DECODE_SHAPES:
+        lay, rng = make_layer(N, K, RANK, seed=K + N)
+        q, s, z = spear.spear_pack_w4(torch.from_numpy(lay.W).to(device), G, SYM)
+        L = spear.W4Layer(N, K, G, SYM, q, s, z, RANK, dev16(lay.A), dev16(lay.B), dev16(lay.w_g), 0.0, 1.0, True)
+        xs = {M: make_tokens(rng, M, K, outlier_frac=OUTLIERS) for M in DECODE_M}
+        base.append((K, N, L, xs))
+    set_bytes = sum(decode_bytes(K, N, 0) for K, N, _, _ in base)
+    ncopy = int(max(2, np.ceil(2.0 * l2_bytes / set_bytes)))
+    copies = [base]
+    for _ in range(ncopy - 1):
+        cp = []
+        for K, N, L, xs in base:
+            L2 = spear.W4Layer(N, K, G, SYM, L.qweight.clone(), L.scales.clone(), L.zeros.clone(), RANK,
+                               L.A.clone(), L.B.clone(), L.w_g.clone(), 0.0, 1.0, True)
+            cp.append((K, N, L2, xs))
+        copies.append(cp)
+    return copies, ncopy, set_bytes
+
+
+def run_ours(args, world, rank, local):
+    import torch
+
+    from quantized_gemm_error_gb300 import spear
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    peaks, peak_kind = load_peaks()
+    props = torch.cuda.get_device_properties(device)
+    l2_bytes = getattr(props, "L2_cache_size", 129 * 2 ** 20) or 129 * 2 ** 20
+
+    copies, ncopy, set_bytes = build_decode(torch, spear, device, l2_bytes)
+    stream = torch.cuda.Stream(device)
+    xs_dev = {}
+    ys = {}
+    calls = []   # (K, N, M) per call in a step
+    for K, N, L, xs in copies[0]:
+        for M in DECODE_M:
+            xs_dev[(K, M)] = torch.from_numpy(xs[M].view(np.int16)).view(torch.bfloat16).to(device)
+            ys[(N, M)] = torch.empty(M, N, dtype=torch.bfloat16, device=device)
+            calls.append((K, N, M))
+    ws_bytes = max(spear.spear_decode_workspace_bytes(L, M) for _, _, L, _ in copies[0] for M in DECODE_M)
+    ws = spear.new_workspace(ws_bytes, device)
+    step_bytes = sum(decode_bytes(K, N, M) for K, N, M in calls)
+
+    def step(cp, comp=True):
+        for K, N, L, _ in copies[cp]:
+            Lc = L if comp else L.with_comp(False)
+            for M in DECODE_M:
+                spear.spear_linear_decode(Lc, xs_dev[(K, M)], y=ys[(N, M)], workspace=ws, stream=stream)
+
+    # warm the library's launch plans, then capture one graph per weight copy
+    with torch.cuda.stream(stream):
+        for cp in range(ncopy):
+            step(cp)
+            step(cp, comp=False)
+    torch.cuda.synchronize()
+    assert spear.spear_get_device_status() == 0
+    graphs, launch_mode = [], "cuda-graph"
+    try:
+        for cp in range(ncopy):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                step(cp)
+            graphs.append(g)
+    except Exception as e:  # pragma: no cover - capture unsupported
+        graphs, launch_mode = [], f"eager ({type(e).__name__})"
+        torch.cuda.synchronize()
+
+    def replay(i):
+        if graphs:
+            graphs[i % ncopy].replay()
+        else:
+            with torch.cuda.stream(stream):
+                step(i % ncopy)
+
+    for i in range(max(3, args.warmup)):
+        replay(i)
+    torch.cuda.synchronize()
+    barrier(world)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        torch.cuda.synchronize()
+        barrier(world)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for i in range(args.steps):
+                replay(i)
+            e1.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+    t_ms = e0.elapsed_time(e1)
+    t_max = reduce_max(t_ms, world)
+    assert spear.spear_get_device_status(stream) == 0
+    value = world * args.steps * step_bytes / (t_max / 1e3) / 1e9
+
+    # per-call breakdown (graph of one call per copy, rotating): comp on vs off
+    cases = []
+    for (K, N, M) in calls:
+        res = {}
+        for comp in (True, False):
+            gs = []
+            for cp in range(ncopy):
+                L = [l for (k, n, l, _) in copies[cp] if (k, n) == (K, N)][0]
+                Lc = L if comp else L.with_comp(False)
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=stream):
+                    spear.spear_linear_decode(Lc, xs_dev[(K, M)], y=ys[(N, M)], workspace=ws, stream=stream)
+                gs.append(g)
+            reps = 20 * ncopy
+            for i in range(ncopy):
+                gs[i].replay()
+            torch.cuda.synchronize()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            with torch.cuda.stream(stream):
+                for i in range(reps):
+                    gs[i % ncopy].replay()
+            b.record(stream)
+            torch.cuda.synchronize()
+            res[comp] = a.elapsed_time(b) / reps * 1e3
+        gbs = decode_bytes(K, N, M) / res[True] / 1e3
+        cases.append({"K": K, "N": N, "M": M, "us": round(res[True], 3), "GB_s": round(gbs, 1),
+                      "frac_hbm_measured": round(gbs / peaks["hbm_gbs"], 4),
+                      "frac_hbm_8000": round(gbs / 8000.0, 4),
+                      "plain_us": round(res[False], 3), "comp_overhead": round(res[True] / res[False] - 1, 4)})
+    tot_on = sum(c["us"] for c in cases)
+    tot_off = sum(c["plain_us"] for c in cases)
+
+    # end to end through the public API with host buffers (pinned), per step:
+    # H2D of every call's tokens, the 12 decode calls, D2H of every output
+    h_x = {k: v.cpu().pin_memory() for k, v in xs_dev.items()}
+    h_y = {k: torch.empty(v.shape, dtype=v.dtype).pin_memory() for k, v in ys.items()}
+    h2d = sum(v.numel() * 2 for v in h_x.values())
+    d2h = sum(v.numel() * 2 for v in h_y.values())
+    e2e_steps = max(3, min(args.steps, 2000))
+    torch.cuda.synchronize()
+    barrier(world)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        a.record(stream)
+        for i in range(e2e_steps):
+            cp = i % ncopy
+            for K, N, L, _ in copies[cp]:
+                for M in DECODE_M:
+                    xs_dev[(K, M)].copy_(h_x[(K, M)], non_blocking=True)
+                    spear.spear_linear_decode(L, xs_dev[(K, M)], y=ys[(N, M)], workspace=ws, stream=stream)
+                    h_y[(N, M)].copy_(ys[(N, M)], non_blocking=True)
+        b.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = reduce_max(a.elapsed_time(b), world)
+    e2e_value = world * e2e_steps * step_bytes / (e2e_ms / 1e3) / 1e9
+
+    prefill = None if args.no_prefill else run_prefill(torch, spear, device, stream, peaks)
+
+    result = None
+    if rank == 0:
+        cpu = None if args.no_cpu_baseline else cpu_baseline()
+        ach = step_bytes * args.steps / (t_ms / 1e3) / 1e9
+        result = {
+            "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": t_max / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": "llama7b_decode_g128_r32", "shapes_KxN": [list(s) for s in DECODE_SHAPES],
+                       "M": DECODE_M, "group_size": G, "symmetric": SYM, "rank": RANK,
+                       "calls_per_step": len(calls), "bytes_per_step": step_bytes,
+                       "l2": f"inputs rotate through {ncopy} distinct weight copies "
+                             f"({ncopy * set_bytes / 1e6:.0f} MB > 2x L2 {l2_bytes / 1e6:.0f} MB)",
+                       "launch": launch_mode, "parallelism": f"replicas x{world}"},
+            "roofline": {"bound": "hbm", "kernel": "decode_kernel (fused W4 + compensator)",
+                         "achieved": round(ach, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": round(ach / peaks["hbm_gbs"], 4), "peak_kind": peak_kind,
+                         "frac_of_8000": round(ach / 8000.0, 4), "traffic": None},
+            "cpu_baseline": cpu,
+            "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+            "gpu_launches": args.steps * len(calls),
+            "clocks": clk.summary(),
+            "comp_overhead_step": round(tot_on / tot_off - 1, 4),
+            "decode_cases": cases,
+            "prefill": prefill,
+        }
+        print(json.dumps(result), flush=True)
+    return result
+
+
+def run_prefill(torch, spear, device, stream, peaks):
+    """Prefill TFLOP/s on the prefill workload (3 shapes x M in 512/2048/8192),
+    fused and concurrent-stream modes and the plain W4 GEMM."""
+    from quantized_gemm_error_gb300.inputs import make_layer, make_tokens
+
+    def dev16(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(device)
+
+    aux = torch.cuda.Stream(device)
+    out = []
+    tot_flops = 0.0
+    tot_s = 0.0
+    for (K, N) in DECODE_SHAPES:
+        lay, rng = make_layer(N, K, RANK, seed=K + N + 1)
+        q, s, z = spear.spear_pack_w4(torch.from_numpy(lay.W).to(device), G, SYM)
+        L = spear.W4Layer(N, K, G, SYM, q, s, z, RANK, dev16(lay.A), dev16(lay.B), dev16(lay.w_g), 0.0, 1.0, True)
+        for M in PREFILL_M:
+            x = dev16(make_tokens(rng, M, K, outlier_frac=OUTLIERS))
+            y = torch.empty(M, N, dtype=torch.bfloat16, device=device)
+            ws = spear.new_workspace(spear.spear_prefill_workspace_bytes(L, M), device, zero=False)
+            res = {}
+            for name, Lc, mode in (("fused", L, spear.PREFILL_FUSED), ("stream", L, spear.PREFILL_STREAM),
+                                   ("plain", L.with_comp(False), spear.PREFILL_FUSED)):
+                def call():
+                    spear.spear_linear_prefill(Lc, x, y=y, mode=mode, workspace=ws, stream=stream, stream_aux=aux)
+                with torch.cuda.stream(stream):
+                    for _ in range(3):
+                        call()
+                torch.cuda.synchronize()
+                reps = max(3, int(2e13 / prefill_flops(K, N, M)))
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                with torch.cuda.stream(stream):
+                    a.record(stream)
+                    for _ in range(reps):
+                        call()
+                    b.record(stream)
+                torch.cuda.synchronize()
+                res[name] = a.elapsed_time(b) / reps * 1e3
+            assert spear.spear_get_device_status(stream) == 0
+            best = min(res["fused"], res["stream"])
+            fl = prefill_flops(K, N, M)
+            tflops = fl / best / 1e6
+            tot_flops += fl
+            tot_s += best * 1e-6
+            out.append({"K": K, "N": N, "M": M, "fused_us": round(res["fused"], 1), "stream_us": round(res["stream"], 1),
+                        "plain_us": round(res["plain"], 1), "TFLOP_s": round(tflops, 1),
+                        "frac_bf16_burst": round(tflops / peaks["bf16_tflops"], 4),
+                        "comp_overhead": round(best / res["plain"] - 1, 4),
+                        "best_mode": "fused" if res["fused"] <= res["stream"] else "stream"})
+            del x, y, ws
+    agg = tot_flops / tot_s / 1e12
+    return {"metric": "prefill TFLOP/s", "value": round(agg, 1), "unit": "TFLOP/s",
+            "workload": "llama7b_prefill_g128_r32",
+            "roofline": {"bound": "tensor", "achieved": round(agg, 1), "peak": peaks["bf16_tflops"],
+                         "unit": "TFLOP/s", "frac": round(agg / peaks["bf16_tflops"], 4),
+                         "peak_sustained": peaks.get("bf16_tflops_sustained")},
+            "cases": out}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-prefill", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+    world, rank, local = dist_setup(args)
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+    else:
+        run_ours(args, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

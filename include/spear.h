@@ -133,9 +133,14 @@ spear_status spear_linear_decode(const spear_w4_layer* L, const uint16_t* x, int
 
 /*
  * Prefill (Technical Summary 2.2 A, prefill phase, M large): tcgen05 tensor-core
- * GEMM over int4 tiles dequantized to bf16 in shared memory, plus the
- * compensator in one of the modes above.  1 <= M.
+ * GEMM over int4 tiles dequantized in shared memory, plus the compensator in
+ * one of the modes above.  1 <= M.
  *   x : device bf16 [M][K];  y : device [M][N], bf16 or fp32.
+ *   The main GEMM runs on fp16 operands with fp32 accumulation: the
+ *   activations are copied to fp16 (exact for |x| < 65504; a larger value is
+ *   reported as SPEAR_ERR_INVALID_ARG through spear_get_device_status) and a
+ *   group-scaled weight is rounded once to fp16.  The compensator terms stay
+ *   in bf16 with fp32 accumulation.
  *   workspace : device, at least spear_prefill_workspace_bytes(); no zeroing
  *               needed.  stream_aux is used by SPEAR_PREFILL_STREAM only (it
  *               may be NULL otherwise); the call orders it after `stream` and

@@ -86,6 +86,23 @@ __device__ __forceinline__ float bf16x2_hi(uint32_t v) { return __uint_as_float(
 // nibble into an exact small integer.
 __host__ __device__ constexpr uint32_t bf16x2_bias(uint32_t v) { return (0x4300u | v) * 0x00010001u; }
 
+// Four fp16x2 values holding (1024 + nibble) for the 8 nibbles of `w`:
+// out[i] = (1024 + nib_i, 1024 + nib_{i+4}) (fp16 1024 has a mantissa unit of 1).
+__device__ __forceinline__ void nibbles_to_f16x2_biased(uint32_t w, uint32_t (&out)[4]) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i) out[i] = ((w >> (4 * i)) & 0x000F000Fu) | 0x64006400u;
+}
+__host__ __device__ constexpr uint32_t f16x2_bias(uint32_t v) { return (0x6400u | v) * 0x00010001u; }
+
+__device__ __forceinline__ uint32_t f16x2_sub(uint32_t a, uint32_t b) {
+  __half2 r = __hsub2(*reinterpret_cast<__half2*>(&a), *reinterpret_cast<__half2*>(&b));
+  return *reinterpret_cast<uint32_t*>(&r);
+}
+__device__ __forceinline__ uint32_t f16x2_mul(uint32_t a, uint32_t b) {
+  __half2 r = __hmul2(*reinterpret_cast<__half2*>(&a), *reinterpret_cast<__half2*>(&b));
+  return *reinterpret_cast<uint32_t*>(&r);
+}
+
 // Four bf16x2 values holding (128 + nibble) for the 8 nibbles of `w`:
 // out[i] = (128 + nib_i, 128 + nib_{i+4}) for i = 0..3 (nib_j = bits 4j..4j+3).
 __device__ __forceinline__ void nibbles_to_bf16x2_biased(uint32_t w, uint32_t (&out)[4]) {

@@ -627,6 +627,10 @@ int launch_decode(const spear_w4_layer& L, const uint16_t* x, int M, void* y, in
   p.ws_T = reinterpret_cast<float*>(base + pl.off_T);
   p.ws_part = reinterpret_cast<float*>(base + pl.off_part);
 
+  // Plans of other shapes may have changed this kernel's shared-memory limit
+  // since this plan's grid was validated: restore the validated setting.
+  if (int rc = cuda_check(cudaFuncSetAttribute(pl.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pl.smem),
+                          "decode: smem attribute")) return rc;
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(pl.Q + pl.P);
   cfg.blockDim = dim3(kThreads);

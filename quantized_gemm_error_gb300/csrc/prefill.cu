@@ -4,16 +4,20 @@
 //
 // Kernels
 //  * w4_gemm_tc: Y[M][N] = X[M][K] * dequant(Wq)^T on the 5th-generation tensor
-//    cores.  One 128 (tokens) x 256 (outputs) tile per thread block; K in
-//    steps of 64.  A TMA warp loads the bf16 X tile (128-byte swizzle) and the
-//    raw int4 tile; four converter warps expand the int4 tile to bf16 straight
-//    into the tensor core's swizzled K-major layout; one thread issues
-//    tcgen05.mma into a 128 x 256 fp32 accumulator in tensor memory; the same
-//    four warps then drain it (tcgen05.ld) and store Y.
+//    cores, fp16 operands, fp32 accumulation.  One 128 (tokens) x 256
+//    (outputs) tile per thread block; K in steps of 64.  A TMA warp loads the
+//    fp16 copy of the X tile (128-byte swizzle) and the raw int4 tile; four
+//    converter warps expand the int4 tile to fp16 straight into the tensor
+//    core's swizzled K-major layout; one thread issues tcgen05.mma into a
+//    128 x 256 fp32 accumulator in tensor memory; the same four warps then
+//    drain it (tcgen05.ld) and store Y.
 //      - per-channel scales: the tile holds the exact integers (u - z) and the
 //        fp32 scale of each output column is applied in the epilogue;
-//      - group scales: the tile holds (u - z) * s computed in fp32 and rounded
-//        once to bf16.
+//      - group scales: the tile holds (u - z) * s rounded once to fp16
+//        (11 significant bits: a bf16 operand's 8 bits are not enough when a
+//        few outlier channels dominate an output).
+//    The activations are bf16; their fp16 copy is exact for |x| < 65504 and
+//    is written by the pass that already reads X (comp_down) or by to_fp16.
 //    Optionally ("fused" mode) the K loop is extended by the compensator's
 //    up-projection: extra K steps with A = [T_hi | T_lo] (the gated
 //    down-projection split into two bf16 halves) and B = the factor B, into a
@@ -146,7 +150,8 @@ w4_gemm_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
   } else if (warp == 1) {
     // ------------------------------------------------------------- MMA issuer
     if (lane == 0) {
-      const uint32_t idesc = idesc_bf16_f32(kBM, kBN);
+      const uint32_t idesc = idesc_f16_f32(kBM, kBN);            // fp16 X x fp16 W
+      const uint32_t idesc_comp = idesc_bf16_f32(kBM, kBN);      // bf16 T x bf16 B
       bool ok = true;
       for (int s = 0; s < total_stages && ok; ++s) {
         const int slot = s % kStages;
@@ -174,7 +179,7 @@ w4_gemm_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
             const int bstep = (col % p.r) / 16;
             const uint64_t ad = smem_desc(xa + 32 * i, 8 * p.t_row_bytes, a_layout);
             const uint64_t bd = smem_desc(wa + 32 * bstep, 8 * p.b_row_bytes, b_layout);
-            mma_bf16_ss(tmem + kBN, ad, bd, idesc, (j > 0 || i > 0) ? 1u : 0u);
+            mma_bf16_ss(tmem + kBN, ad, bd, idesc_comp, (j > 0 || i > 0) ? 1u : 0u);
           }
         }
         mma_commit(smem_u32(&bar_empty[slot]));             // frees the stage when these MMAs finish
@@ -207,27 +212,20 @@ w4_gemm_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
             const uint8_t zb = p.zeros[(size_t)n * zrow + gi / 2];
             z = (gi & 1) ? (zb >> 4) : (zb & 15);
           }
-          const float sc = p.perch ? 1.0f : __half2float(p.scales[(size_t)n * p.ng + gi]);
-          const uint32_t zb2 = bf16x2_bias((uint32_t)z);
+          const uint32_t s2 = p.perch ? 0x3C003C00u     // fp16 1.0: the scale is applied in the epilogue
+                                      : (uint32_t)__half_as_ushort(p.scales[(size_t)n * p.ng + gi]) * 0x00010001u;
+          const uint32_t zb2 = f16x2_bias((uint32_t)z);
           const uint4 r0 = *reinterpret_cast<const uint4*>(raw + row * 32);
           const uint4 r1 = *reinterpret_cast<const uint4*>(raw + row * 32 + 16);
           const uint32_t words[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
 #pragma unroll
           for (int w = 0; w < 8; ++w) {
             uint32_t v[4];
-            nibbles_to_bf16x2_biased(words[w], v);           // (k_i, k_{i+4}) as 128 + u
+            nibbles_to_f16x2_biased(words[w], v);            // (k_i, k_{i+4}) as 1024 + u
 #pragma unroll
-            for (int i = 0; i < 4; ++i) v[i] = bf16x2_sub(v[i], zb2);   // u - z, exact
-            if (p.perch) {
-              out[w] = make_uint4(__byte_perm(v[0], v[1], 0x5410), __byte_perm(v[2], v[3], 0x5410),
-                                  __byte_perm(v[0], v[1], 0x7632), __byte_perm(v[2], v[3], 0x7632));
-            } else {
-              // (u - z) * s exact in fp32, one rounding to bf16; natural k order
-              out[w] = make_uint4(pack_bf16x2(bf16x2_lo(v[0]) * sc, bf16x2_lo(v[1]) * sc),
-                                  pack_bf16x2(bf16x2_lo(v[2]) * sc, bf16x2_lo(v[3]) * sc),
-                                  pack_bf16x2(bf16x2_hi(v[0]) * sc, bf16x2_hi(v[1]) * sc),
-                                  pack_bf16x2(bf16x2_hi(v[2]) * sc, bf16x2_hi(v[3]) * sc));
-            }
+            for (int i = 0; i < 4; ++i) v[i] = f16x2_mul(f16x2_sub(v[i], zb2), s2);   // (u - z) s, one rounding
+            out[w] = make_uint4(__byte_perm(v[0], v[1], 0x5410), __byte_perm(v[2], v[3], 0x5410),
+                                __byte_perm(v[0], v[1], 0x7632), __byte_perm(v[2], v[3], 0x7632));
           }
         } else {
 #pragma unroll
@@ -319,7 +317,22 @@ struct CompDownParams {
   float b_g, alpha;
   __nv_bfloat16* T2;    // [M][t2_cols]: T_hi in [0, r), T_lo in [r, 2r)
   int t2_cols;
+  __half* x16;          // optional [M][K] fp16 copy of x for the GEMM (NULL: not written)
 };
+
+// 8 bf16 -> 8 fp16 (exact inside the fp16 range); flags values beyond it.
+__device__ __forceinline__ uint4 bf16x8_to_f16x8(uint4 v, bool& out_of_range) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  uint32_t o[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float lo = bf16x2_lo(w[i]), hi = bf16x2_hi(w[i]);
+    out_of_range |= !(fabsf(lo) < 65504.0f) || !(fabsf(hi) < 65504.0f);
+    const __half2 h = __floats2half2_rn(lo, hi);
+    o[i] = *reinterpret_cast<const uint32_t*>(&h);
+  }
+  return make_uint4(o[0], o[1], o[2], o[3]);
+}
 
 template <int RT>
 __global__ void __launch_bounds__(kCdThreads) comp_down_kernel(const CompDownParams p) {
@@ -345,6 +358,11 @@ __global__ void __launch_bounds__(kCdThreads) comp_down_kernel(const CompDownPar
       for (int t = 0; t < kCdMT; ++t) {
         const int tok = tok0 + t * 8 + g;
         xv[t] = tok < p.M ? ldg16(p.x + (size_t)tok * p.K + kb) : make_uint4(0, 0, 0, 0);
+        if (p.x16 && tok < p.M) {
+          bool bad = false;
+          *reinterpret_cast<uint4*>(p.x16 + (size_t)tok * p.K + kb) = bf16x8_to_f16x8(xv[t], bad);
+          if (bad) record_status(&g_prefill_status, DEV_ERR_INVALID);
+        }
       }
 #pragma unroll
       for (int rt = 0; rt < RT; ++rt) {
@@ -393,13 +411,26 @@ __global__ void __launch_bounds__(kCdThreads) comp_down_kernel(const CompDownPar
   }
 }
 
+// --------------------------------------------------------------- to_fp16 --
+// fp16 copy of the activations for the GEMM when no compensator pass reads them.
+__global__ void __launch_bounds__(256) to_fp16_kernel(const uint4* __restrict__ x, uint4* __restrict__ x16,
+                                                      size_t n8) {
+  bool bad = false;
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n8; i += (size_t)gridDim.x * blockDim.x)
+    x16[i] = bf16x8_to_f16x8(__ldg(x + i), bad);
+  if (bad) record_status(&g_prefill_status, DEV_ERR_INVALID);
+}
+
 // ----------------------------------------------------------- comp_up_add --
-// Y[m][n] += sum_j (T_hi + T_lo)[m][j] B[n][j].  One warp = 16 tokens x 64
-// outputs (8 mma n-tiles), A operand = T rows, B operand = rows of B.
+// Y[m][n] = Y32[m][n] + sum_j (T_hi + T_lo)[m][j] B[n][j], rounded once.
+// One warp = 16 tokens x 64 outputs (8 mma n-tiles), A operand = T rows,
+// B operand = rows of B.  Y32 is the plain GEMM's fp32 result (it may be y
+// itself when y is fp32).
 struct CompUpParams {
   int M, N, r, t2_cols, out_f32;
   const __nv_bfloat16* T2;
   const __nv_bfloat16* B;
+  const float* y32;
   void* y;
 };
 
@@ -434,16 +465,13 @@ __global__ void __launch_bounds__(256) comp_up_add_kernel(const CompUpParams p) 
     for (int hh = 0; hh < 2; ++hh) {
       const int tok = tok0 + g + 8 * hh;
       if (tok >= p.M) continue;
+      const float2 m32 = *reinterpret_cast<const float2*>(p.y32 + (size_t)tok * p.N + n);
+      const float v0 = m32.x + acc[t][2 * hh], v1 = m32.y + acc[t][2 * hh + 1];
       if (p.out_f32) {
-        float2* dst = reinterpret_cast<float2*>(reinterpret_cast<float*>(p.y) + (size_t)tok * p.N + n);
-        float2 v = *dst;
-        v.x += acc[t][2 * hh];
-        v.y += acc[t][2 * hh + 1];
-        *dst = v;
+        *reinterpret_cast<float2*>(reinterpret_cast<float*>(p.y) + (size_t)tok * p.N + n) = make_float2(v0, v1);
       } else {
-        __nv_bfloat162* dst = reinterpret_cast<__nv_bfloat162*>(reinterpret_cast<__nv_bfloat16*>(p.y) + (size_t)tok * p.N + n);
-        const float2 v = __bfloat1622float2(*dst);
-        *dst = __floats2bfloat162_rn(v.x + acc[t][2 * hh], v.y + acc[t][2 * hh + 1]);
+        *reinterpret_cast<__nv_bfloat162*>(reinterpret_cast<__nv_bfloat16*>(p.y) + (size_t)tok * p.N + n) =
+            __floats2bfloat162_rn(v0, v1);
       }
     }
   }
@@ -496,10 +524,12 @@ size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
 
 int resolve_mode(int mode) { return mode == SPEAR_PREFILL_AUTO ? SPEAR_PREFILL_FUSED : mode; }
 
-int launch_gemm(const spear_w4_layer& L, const uint16_t* x, int M, void* y, int out_f32, const __nv_bfloat16* T2,
+// x16: fp16 copy of the activations [M][K].
+int launch_gemm(const spear_w4_layer& L, const __half* x16, int M, void* y, int out_f32, const __nv_bfloat16* T2,
                 int r_fused, cudaStream_t st) {
   CUtensorMap tm_x, tm_wq, tm_t, tm_b;
-  if (int rc = make_tmap(&tm_x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, x, L.K, M, kBK, kBM, CU_TENSOR_MAP_SWIZZLE_128B)) return rc;
+  if (int rc = make_tmap(&tm_x, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, x16, L.K, M, kBK, kBM,
+                         CU_TENSOR_MAP_SWIZZLE_128B)) return rc;
   if (int rc = make_tmap(&tm_wq, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, L.qweight, L.K / 2, L.N, kBK / 2, kBN,
                          CU_TENSOR_MAP_SWIZZLE_NONE)) return rc;
   GemmParams p{};
@@ -532,8 +562,10 @@ int launch_gemm(const spear_w4_layer& L, const uint16_t* x, int M, void* y, int 
   return cuda_check(cudaGetLastError(), "prefill gemm launch");
 }
 
-int launch_comp_down(const spear_w4_layer& L, const uint16_t* x, int M, __nv_bfloat16* T2, cudaStream_t st) {
+int launch_comp_down(const spear_w4_layer& L, const uint16_t* x, int M, __nv_bfloat16* T2, __half* x16,
+                     cudaStream_t st) {
   CompDownParams p{};
+  p.x16 = x16;
   p.M = M; p.K = L.K; p.r = L.rank;
   p.x = reinterpret_cast<const __nv_bfloat16*>(x);
   p.A = reinterpret_cast<const __nv_bfloat16*>(L.A);
@@ -549,10 +581,19 @@ int launch_comp_down(const spear_w4_layer& L, const uint16_t* x, int M, __nv_bfl
   return cuda_check(cudaGetLastError(), "comp_down launch");
 }
 
-int launch_comp_up(const spear_w4_layer& L, int M, void* y, int out_f32, const __nv_bfloat16* T2, cudaStream_t st) {
+int launch_to_fp16(const uint16_t* x, __half* x16, size_t n, cudaStream_t st) {
+  const size_t n8 = n / 8;   // K % 128 == 0, so every row is a whole number of 16-byte groups
+  const unsigned blocks = (unsigned)std::min<size_t>((n8 + 255) / 256, 148 * 16);
+  to_fp16_kernel<<<blocks, 256, 0, st>>>(reinterpret_cast<const uint4*>(x), reinterpret_cast<uint4*>(x16), n8);
+  return cuda_check(cudaGetLastError(), "to_fp16 launch");
+}
+
+int launch_comp_up(const spear_w4_layer& L, int M, void* y, int out_f32, const float* y32, const __nv_bfloat16* T2,
+                   cudaStream_t st) {
   CompUpParams p{};
   p.M = M; p.N = L.N; p.r = L.rank; p.t2_cols = t2_cols_for(L.rank); p.out_f32 = out_f32;
   p.T2 = T2;
+  p.y32 = y32;
   p.B = reinterpret_cast<const __nv_bfloat16*>(L.B);
   p.y = y;
   dim3 grid(L.N / 64, (M + 127) / 128);
@@ -581,12 +622,27 @@ int stream_events(StreamEvents* ev) {
   return SPEAR_OK;
 }
 
+// Workspace: [T2: M x 2r bf16][X16: M x K fp16][Y32: M x N fp32, stream mode with bf16 output only]
+struct WsLayout {
+  size_t t2, x16, y32, total;
+};
+
+WsLayout ws_layout(const spear_w4_layer& L, int M, int mode, int out_f32) {
+  const bool comp = L.comp_enabled && L.rank > 0;
+  WsLayout w{};
+  size_t off = 0;
+  w.t2 = off;  off = align256(off + (comp ? (size_t)M * t2_cols_for(L.rank) * 2 : 0));
+  w.x16 = off; off = align256(off + (size_t)M * L.K * 2);
+  w.y32 = off;
+  if (comp && resolve_mode(mode) == SPEAR_PREFILL_STREAM && !out_f32) off = align256(off + (size_t)M * L.N * 4);
+  w.total = off;
+  return w;
+}
+
 }  // namespace
 
 int prefill_workspace_bytes(const spear_w4_layer& L, int M, int mode, size_t* bytes) {
-  const bool comp = L.comp_enabled && L.rank > 0;
-  (void)mode;
-  *bytes = comp ? align256((size_t)M * t2_cols_for(L.rank) * 2) : 0;
+  *bytes = ws_layout(L, M, mode, 0).total;          // the bf16-output size covers fp32 output too
   return SPEAR_OK;
 }
 
@@ -595,29 +651,37 @@ int launch_prefill(const spear_w4_layer& L, const uint16_t* x, int M, void* y, i
   DeviceInfo di;
   if (int rc = device_info(&di)) return rc;
   const bool comp = L.comp_enabled && L.rank > 0;
-  if (!comp) return launch_gemm(L, x, M, y, out_f32, nullptr, 0, st);
-  size_t need = 0;
-  prefill_workspace_bytes(L, M, mode, &need);
-  if (!ws || ws_bytes < need)
-    return fail(SPEAR_ERR_WORKSPACE, "prefill: workspace of %zu B is smaller than the %zu B needed", ws_bytes, need);
+  const WsLayout lay = ws_layout(L, M, mode, out_f32);
+  if (!ws || ws_bytes < lay.total)
+    return fail(SPEAR_ERR_WORKSPACE, "prefill: workspace of %zu B is smaller than the %zu B needed", ws_bytes,
+                lay.total);
   if ((reinterpret_cast<uintptr_t>(ws) & 255) != 0)
     return fail(SPEAR_ERR_INVALID_ARG, "prefill: workspace must be 256-byte aligned");
-  __nv_bfloat16* T2 = reinterpret_cast<__nv_bfloat16*>(ws);
-  if (resolve_mode(mode) == SPEAR_PREFILL_FUSED) {
-    if (int rc = launch_comp_down(L, x, M, T2, st)) return rc;
-    return launch_gemm(L, x, M, y, out_f32, T2, L.rank, st);
+  char* base = reinterpret_cast<char*>(ws);
+  __nv_bfloat16* T2 = reinterpret_cast<__nv_bfloat16*>(base + lay.t2);
+  __half* x16 = reinterpret_cast<__half*>(base + lay.x16);
+  if (!comp) {
+    if (int rc = launch_to_fp16(x, x16, (size_t)M * L.K, st)) return rc;
+    return launch_gemm(L, x16, M, y, out_f32, nullptr, 0, st);
   }
-  // stream mode: fork the down-projection onto st_aux, W4 GEMM on st, join, up-project + add
+  if (resolve_mode(mode) == SPEAR_PREFILL_FUSED) {
+    if (int rc = launch_comp_down(L, x, M, T2, x16, st)) return rc;
+    return launch_gemm(L, x16, M, y, out_f32, T2, L.rank, st);
+  }
+  // stream mode: the down-projection runs on st_aux beside the W4 GEMM on st;
+  // the GEMM writes fp32 so the up-projection-and-add rounds only once
   if (!st_aux || st_aux == st) return fail(SPEAR_ERR_INVALID_ARG, "prefill: stream mode needs a distinct stream_aux");
+  float* y32 = out_f32 ? reinterpret_cast<float*>(y) : reinterpret_cast<float*>(base + lay.y32);
   StreamEvents ev;
   if (int rc = stream_events(&ev)) return rc;
   if (int rc = cuda_check(cudaEventRecord(ev.fork, st), "fork record")) return rc;
   if (int rc = cuda_check(cudaStreamWaitEvent(st_aux, ev.fork, 0), "fork wait")) return rc;
-  if (int rc = launch_comp_down(L, x, M, T2, st_aux)) return rc;
+  if (int rc = launch_comp_down(L, x, M, T2, nullptr, st_aux)) return rc;
   if (int rc = cuda_check(cudaEventRecord(ev.join, st_aux), "join record")) return rc;
-  if (int rc = launch_gemm(L, x, M, y, out_f32, nullptr, 0, st)) return rc;
+  if (int rc = launch_to_fp16(x, x16, (size_t)M * L.K, st)) return rc;
+  if (int rc = launch_gemm(L, x16, M, y32, 1, nullptr, 0, st)) return rc;
   if (int rc = cuda_check(cudaStreamWaitEvent(st, ev.join, 0), "join wait")) return rc;
-  return launch_comp_up(L, M, y, out_f32, T2, st);
+  return launch_comp_up(L, M, y, out_f32, y32, T2, st);
 }
 
 int read_and_clear_status_prefill(unsigned* out, cudaStream_t st) {

@@ -104,3 +104,15 @@ def test_prefill_gate_zero_equals_plain():
     y_off = _run(L_on.with_comp(False), x, FUSED, 1)
     # the fused correction adds exact zeros into its own accumulator
     assert torch.equal(y_on, y_off)
+
+
+def test_prefill_reports_activations_beyond_fp16_range():
+    from quantized_gemm_error_gb300 import spear
+    lay, rng = make_layer(256, 256, 0, seed=47)
+    x = make_tokens(rng, 128, 256)
+    x[3, 7] = 0x4780                                        # bf16 65536: beyond the fp16 range
+    L = gpu_layer(lay, 128, False)
+    spear.spear_linear_prefill(L, to_dev_u16(x, torch.bfloat16), out_dtype=1)
+    torch.cuda.synchronize()
+    assert spear.spear_get_device_status() == 1
+    assert spear.spear_get_device_status() == 0
