@@ -402,7 +402,12 @@ def run_ours(args, world, rank, local):
     e2e_ms = reduce_max(a.elapsed_time(b), world)
     e2e_value = world * e2e_steps * step_bytes / (e2e_ms / 1e3) / 1e9
 
-    prefill = None if args.no_prefill else run_prefill(torch, spear, device, stream, peaks)
+    prefill = None
+    if not args.no_prefill:
+        try:
+            prefill = run_prefill(torch, spear, device, stream, peaks)
+        except Exception as e:  # the decode line still prints; the failure is reported in it
+            prefill = {"error": f"{type(e).__name__}: {e}"}
 
     result = None
     if rank == 0:
@@ -455,7 +460,8 @@ def run_prefill(torch, spear, device, stream, peaks):
         for M in PREFILL_M:
             x = dev16(make_tokens(rng, M, K, outlier_frac=OUTLIERS))
             y = torch.empty(M, N, dtype=torch.bfloat16, device=device)
-            ws = spear.new_workspace(spear.spear_prefill_workspace_bytes(L, M), device, zero=False)
+            ws = spear.new_workspace(max(spear.spear_prefill_workspace_bytes(L, M, m)
+                                         for m in (spear.PREFILL_FUSED, spear.PREFILL_STREAM)), device, zero=False)
             res = {}
             for name, Lc, mode in (("fused", L, spear.PREFILL_FUSED), ("stream", L, spear.PREFILL_STREAM),
                                    ("plain", L.with_comp(False), spear.PREFILL_FUSED)):
