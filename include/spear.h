@@ -132,6 +132,30 @@ spear_status spear_linear_decode(const spear_w4_layer* L, const uint16_t* x, int
                                  void* stream);
 
 /*
+ * Decode for callers that cannot allocate device memory.  (The paper has no
+ * counterpart: this is a deployment convenience of this library.)
+ * Some callers cannot allocate when they call the layer -- a plugin hosted
+ * by a framework that owns the device allocator, a runtime that plans every
+ * buffer before serving and forbids allocation afterwards, code on a
+ * latency-critical path where an allocation could synchronise the device.
+ * This call computes exactly what spear_linear_decode computes, but keeps its
+ * scratch in one fixed 8 MiB array inside the library (every GPU that loads
+ * the library holds it until the process exits) instead of a workspace.
+ *   - A shape whose decode scratch exceeds 8 MiB is rejected with
+ *     SPEAR_ERR_UNSUPPORTED; spear_last_error() gives the bytes needed.
+ *   - The first call on a device sets the scratch up (looks up its device
+ *     address and zero-fills it, synchronously); make that first call before
+ *     any stream capture.
+ *   - Every call clears the scratch's synchronisation words on `stream` and
+ *     otherwise reuses what the previous call left there.  All calls share
+ *     the one array: calls that overlap on the GPU (other streams, other host
+ *     threads) race and give wrong results.
+ * Nothing here allocates device memory.
+ */
+spear_status spear_linear_decode_noalloc(const spear_w4_layer* L, const uint16_t* x, int M,
+                                         void* y, int out_dtype, void* stream);
+
+/*
  * Prefill (Technical Summary 2.2 A, prefill phase, M large): tcgen05 tensor-core
  * GEMM over int4 tiles dequantized in shared memory, plus the compensator in
  * one of the modes above.  1 <= M.

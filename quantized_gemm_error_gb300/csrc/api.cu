@@ -131,6 +131,16 @@ spear_status spear_linear_decode(const spear_w4_layer* L, const uint16_t* x, int
                        static_cast<cudaStream_t>(stream));
 }
 
+spear_status spear_linear_decode_noalloc(const spear_w4_layer* L, const uint16_t* x, int M, void* y,
+                                         int out_dtype, void* stream) {
+  if (int rc = check_layer(L)) return rc;
+  if (M < 1 || M > 64) return fail(SPEAR_ERR_INVALID_ARG, "decode M=%d must be in [1, 64]", M);
+  if (!x || !y || !aligned16(x) || !aligned16(y)) return fail(SPEAR_ERR_INVALID_ARG, "x/y NULL or misaligned");
+  if (out_dtype != SPEAR_OUT_BF16 && out_dtype != SPEAR_OUT_F32)
+    return fail(SPEAR_ERR_INVALID_ARG, "out_dtype=%d", out_dtype);
+  return launch_decode_noalloc(*L, x, M, y, out_dtype == SPEAR_OUT_F32, static_cast<cudaStream_t>(stream));
+}
+
 spear_status spear_prefill_workspace_bytes(const spear_w4_layer* L, int M, int mode, size_t* bytes) {
   if (int rc = check_layer(L)) return rc;
   if (M < 1) return fail(SPEAR_ERR_INVALID_ARG, "prefill M=%d must be positive", M);

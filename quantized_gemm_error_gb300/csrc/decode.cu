@@ -68,7 +68,7 @@ struct DecodeParams {
   int max_parts;            // most streamers sharing one tile
   int ng;                   // K/G
   // workspace
-  float* ws_prod;           // [Q][Mpad][Rpad]
+  float* ws_prod;           // [Q][Mpad][16]
   float* ws_T;              // [Mpad][r]
   float* ws_part;           // [tiles][max_parts][MT*4*32]
   unsigned* ws_tile_cnt;    // [tiles]
@@ -81,96 +81,111 @@ __device__ __forceinline__ int unit_owner(long long u, long long U, int P) {
 }
 
 // ---------------------------------------------------------------- producer --
-// P[m][i] = sum_{k in slice} W'[i][k] x[m][k], W' = [A; w_g; 0-padding].
+// Producer block q computes the partial P[m][i] = sum_{k in slice s} W'[i][k] x[m][k]
+// for one 16-row tile rt = q % RT of W' = [A; w_g; 0-padding] over K slice
+// s = q / RT (S = Q / RT slices), so its loads take one round trip.
 // Lane (g, c) of a warp loads 16 B (8 consecutive k) per row; within a 32-k
 // piece the MMA's k positions {2c, 2c+1, 2c+8, 2c+9} of k-step h map to the
 // lane's k = 8c + 4h + {0, 1, 2, 3}, identically for both operands.
+constexpr int kMaxSlices = 8;
+
 template <int MT>
 __device__ void producer_block(const DecodeParams& p, float* smem) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, c = lane & 3;
-  const int q = blockIdx.x;
-  const int c0 = (int)((long long)q * p.nchunks / p.Q), c1 = (int)((long long)(q + 1) * p.nchunks / p.Q);
   const int RT = (p.r + 1 + 15) / 16;
-  const int Rpad = RT * 16;
   const int Mpad = MT * 8;
+  const int q = blockIdx.x, rt = q % RT, sl = q / RT, S = p.Q / RT;
+  const int c0 = (int)((long long)sl * p.nchunks / S), c1 = (int)((long long)(sl + 1) * p.nchunks / S);
+  const int npieces = (c1 - c0) * 4;                   // 32-k pieces of the slice
   float* red = smem;                                   // [kWarps][MT][4][32]
 
-  for (int rt = 0; rt < RT; ++rt) {
-    float acc[MT][4];
+  auto row_ptr = [&](int i) -> const __nv_bfloat16* {
+    if (i < p.r) return p.A + (size_t)i * p.K;
+    if (i == p.r) return p.w_g;
+    return nullptr;
+  };
+  const __nv_bfloat16* wlo = row_ptr(rt * 16 + g);
+  const __nv_bfloat16* whi = row_ptr(rt * 16 + g + 8);
+  float acc[MT][4];
 #pragma unroll
-    for (int t = 0; t < MT; ++t)
+  for (int t = 0; t < MT; ++t)
 #pragma unroll
-      for (int i = 0; i < 4; ++i) acc[t][i] = 0.0f;
-    const int row_lo = rt * 16 + g, row_hi = row_lo + 8;
-    auto row_ptr = [&](int i) -> const __nv_bfloat16* {
-      if (i < p.r) return p.A + (size_t)i * p.K;
-      if (i == p.r) return p.w_g;
-      return nullptr;
-    };
-    const __nv_bfloat16* wlo = row_ptr(row_lo);
-    const __nv_bfloat16* whi = row_ptr(row_hi);
-    for (int ch = c0 + warp; ch < c1; ch += kWarps) {
+    for (int i = 0; i < 4; ++i) acc[t][i] = 0.0f;
+  for (int pc0 = warp; pc0 < npieces; pc0 += 2 * kWarps) {
+    // two pieces per pass: all of their loads are in flight together
+    uint4 va[2], vb[2], xv[2][MT];
 #pragma unroll
-      for (int piece = 0; piece < 4; ++piece) {
-        const int kb = ch * kChunkK + piece * 32 + 8 * c;
-        const uint4 va = wlo ? ldg16(wlo + kb) : make_uint4(0, 0, 0, 0);
-        const uint4 vb = whi ? ldg16(whi + kb) : make_uint4(0, 0, 0, 0);
+    for (int h = 0; h < 2; ++h) {
+      const int pc = pc0 + h * kWarps;
+      const bool ok = pc < npieces;
+      const int kb = c0 * kChunkK + pc * 32 + 8 * c;
+      va[h] = (ok && wlo) ? ldg16(wlo + kb) : make_uint4(0, 0, 0, 0);
+      vb[h] = (ok && whi) ? ldg16(whi + kb) : make_uint4(0, 0, 0, 0);
 #pragma unroll
-        for (int t = 0; t < MT; ++t) {
-          const int tok = t * 8 + g;
-          const uint4 xv = tok < p.M ? ldg16(p.x + (size_t)tok * p.K + kb) : make_uint4(0, 0, 0, 0);
-          mma_bf16_16816(acc[t], va.x, vb.x, va.y, vb.y, xv.x, xv.y);
-          mma_bf16_16816(acc[t], va.z, vb.z, va.w, vb.w, xv.z, xv.w);
-        }
+      for (int t = 0; t < MT; ++t) {
+        const int tok = t * 8 + g;
+        xv[h][t] = (ok && tok < p.M) ? ldg16(p.x + (size_t)tok * p.K + kb) : make_uint4(0, 0, 0, 0);
       }
     }
-    // cross-warp sum in a fixed order, then one slice partial per (m, row)
 #pragma unroll
-    for (int t = 0; t < MT; ++t)
+    for (int h = 0; h < 2; ++h)
 #pragma unroll
-      for (int i = 0; i < 4; ++i) red[((warp * MT + t) * 4 + i) * 32 + lane] = acc[t][i];
-    __syncthreads();
-    for (int e = threadIdx.x; e < MT * 4 * 32; e += kThreads) {
-      const int t = e / 128, i = (e / 32) & 3, ln = e & 31;
-      float s = 0.0f;
-      for (int w = 0; w < kWarps; ++w) s += red[((w * MT + t) * 4 + i) * 32 + ln];
-      // C fragment element i of lane ln: row = (ln/4) + 8*(i/2), token = t*8 + 2*(ln%4) + (i%2)
-      const int row = rt * 16 + (ln >> 2) + 8 * (i >> 1);
-      const int tok = t * 8 + 2 * (ln & 3) + (i & 1);
-      p.ws_prod[((size_t)q * Mpad + tok) * Rpad + row] = s;
-    }
-    __syncthreads();
+      for (int t = 0; t < MT; ++t) {
+        mma_bf16_16816(acc[t], va[h].x, vb[h].x, va[h].y, vb[h].y, xv[h][t].x, xv[h][t].y);
+        mma_bf16_16816(acc[t], va[h].z, vb[h].z, va[h].w, vb[h].w, xv[h][t].z, xv[h][t].w);
+      }
   }
+  // cross-warp sum in a fixed order; this block's partial for its 16 rows
+#pragma unroll
+  for (int t = 0; t < MT; ++t)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) red[((warp * MT + t) * 4 + i) * 32 + lane] = acc[t][i];
+  __syncthreads();
+  for (int e = threadIdx.x; e < MT * 4 * 32; e += kThreads) {
+    const int t = e / 128, i = (e / 32) & 3, ln = e & 31;
+    float v = 0.0f;
+    for (int w = 0; w < kWarps; ++w) v += red[((w * MT + t) * 4 + i) * 32 + ln];
+    // C fragment element i of lane ln: row (ln/4) + 8 (i/2), token t*8 + 2 (ln%4) + (i%2)
+    const int row = (ln >> 2) + 8 * (i >> 1);
+    const int tok = t * 8 + 2 * (ln & 3) + (i & 1);
+    p.ws_prod[((size_t)q * Mpad + tok) * 16 + row] = v;
+    __threadfence();
+  }
+  __syncthreads();
 
-  // arrive; the last producer reduces the slices and publishes T
+  // arrive; the last producer sums the slices, applies the gate, publishes T
   __shared__ unsigned s_last;
   if (threadIdx.x == 0) {
-    __threadfence();
     const unsigned old = atomicAdd(&p.ws_sync[0], 1u);
     s_last = (old == (unsigned)(p.Q - 1));
+    __threadfence();
   }
   __syncthreads();
   if (!s_last) return;
-  __threadfence();
+  auto slice_sum = [&](int m, int i) {                  // fixed order over slices
+    const int rti = i / 16, ri = i % 16;
+    float part[kMaxSlices];
+#pragma unroll
+    for (int ss = 0; ss < kMaxSlices; ++ss)
+      part[ss] = ss < S ? __ldcg(p.ws_prod + ((size_t)(ss * RT + rti) * Mpad + m) * 16 + ri) : 0.0f;
+    float v = 0.0f;
+#pragma unroll
+    for (int ss = 0; ss < kMaxSlices; ++ss) v += part[ss];
+    return v;
+  };
   float* gate = smem;                                   // [Mpad]
-  for (int m = threadIdx.x; m < Mpad; m += kThreads) {
-    float s = 0.0f;
-    for (int qq = 0; qq < p.Q; ++qq) s += __ldcg(p.ws_prod + ((size_t)qq * Mpad + m) * Rpad + p.r);
-    s += p.b_g;
-    gate[m] = 1.0f / (1.0f + expf(-s));
-  }
+  for (int m = threadIdx.x; m < Mpad; m += kThreads) gate[m] = 1.0f / (1.0f + expf(-(slice_sum(m, p.r) + p.b_g)));
   __syncthreads();
   for (int e = threadIdx.x; e < Mpad * p.r; e += kThreads) {
     const int m = e / p.r, j = e % p.r;
-    float s = 0.0f;
-    for (int qq = 0; qq < p.Q; ++qq) s += __ldcg(p.ws_prod + ((size_t)qq * Mpad + m) * Rpad + j);
-    p.ws_T[e] = (m < p.M) ? p.alpha * gate[m] * s : 0.0f;
+    const float v = slice_sum(m, j);
+    p.ws_T[e] = (m < p.M) ? p.alpha * gate[m] * v : 0.0f;
   }
+  __threadfence();
   __syncthreads();
   if (threadIdx.x == 0) {
     p.ws_sync[0] = 0;                                   // ticket ready for the next call
-    __threadfence();
     st_release_gpu(&p.ws_sync[1], 1u);
   }
 }
@@ -185,6 +200,7 @@ struct Cursor {
 
 template <int MT, bool COMP, bool PERCH>
 __device__ void streamer_block(const DecodeParams& p, float* smem) {
+  constexpr bool XPF = (MT == 1);                        // prefetch the next item's tokens in registers
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, c = lane & 3;
   const int b = blockIdx.x - p.Q;
@@ -202,7 +218,8 @@ __device__ void streamer_block(const DecodeParams& p, float* smem) {
   uint32_t* Ts = reinterpret_cast<uint32_t*>(ybuf + p.max_tiles * MT * 4 * 32);  // [Mpad][r/2] hi, then lo
   __half* sc_s = reinterpret_cast<__half*>(Ts + (COMP ? Mpad * kMaxRank : 0));   // [max_tiles][16][ng]
   uint8_t* z_s = reinterpret_cast<uint8_t*>(sc_s + p.max_tiles * 16 * p.ng);     // [max_tiles][16][ng]
-  __shared__ int s_fixup[64];
+  __shared__ int s_parts[64];      // streamers sharing the segment's tile (1 = this block owns it)
+  __shared__ int s_fixup[64];      // 1 when this block stores the segment's tile
   __shared__ int s_flag;
 
   auto seg_ca = [&](int s) {
@@ -211,19 +228,6 @@ __device__ void streamer_block(const DecodeParams& p, float* smem) {
   auto seg_cb = [&](int s) {
     return (int)(min(u1, (long long)(tile0 + s + 1) * p.nchunks) - (long long)(tile0 + s) * p.nchunks);
   };
-
-  // stage the scales and zero points of every touched tile (small, L2 resident)
-  for (int e = threadIdx.x; e < nseg * 16 * p.ng; e += kThreads) {
-    const int s = e / (16 * p.ng), rem = e % (16 * p.ng), row = rem / p.ng, gi = rem % p.ng;
-    const int n = (tile0 + s) * 16 + row;
-    sc_s[e] = p.scales[(size_t)n * p.ng + gi];
-    int z = 8;
-    if (!p.sym) {
-      const uint8_t zb = p.zeros[(size_t)n * ((p.ng + 1) / 2) + gi / 2];
-      z = (gi & 1) ? (zb >> 4) : (zb & 15);
-    }
-    z_s[e] = (uint8_t)z;
-  }
 
   // per-warp item cursor over the segments
   auto first_item = [&](Cursor& cur) {
@@ -252,6 +256,7 @@ __device__ void streamer_block(const DecodeParams& p, float* smem) {
     cp_async_commit();
   };
 
+  // 1. weight stream first
   Cursor icur, ccur;
   first_item(icur);
   ccur = icur;
@@ -260,6 +265,49 @@ __device__ void streamer_block(const DecodeParams& p, float* smem) {
     issue(icur, s);
     next_item(icur);
   }
+  // 2. scales and zero points of every touched tile, loads batched ahead of the stores
+  {
+    const int total = nseg * 16 * p.ng;
+    const int zrow = (p.ng + 1) / 2;
+    for (int e0 = threadIdx.x; e0 < total; e0 += 8 * kThreads) {
+      __half sv[8];
+      uint8_t zv[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int e = e0 + u * kThreads;
+        sv[u] = __ushort_as_half(0);
+        zv[u] = 8;
+        if (e < total) {
+          const int sg = e / (16 * p.ng), rem = e % (16 * p.ng), row = rem / p.ng, gi = rem % p.ng;
+          const int n = (tile0 + sg) * 16 + row;
+          sv[u] = p.scales[(size_t)n * p.ng + gi];
+          if (!p.sym) {
+            const uint8_t zb = p.zeros[(size_t)n * zrow + gi / 2];
+            zv[u] = (gi & 1) ? (zb >> 4) : (zb & 15);
+          }
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int e = e0 + u * kThreads;
+        if (e < total) { sc_s[e] = sv[u]; z_s[e] = zv[u]; }
+      }
+    }
+  }
+  // 3. tokens of the first item
+  uint4 xcur[MT][4];
+  auto load_x = [&](const Cursor& cur, uint4 (&dst)[MT][4]) {
+#pragma unroll
+    for (int t = 0; t < MT; ++t)
+#pragma unroll
+      for (int w = 0; w < 4; ++w) {
+        const int tok = t * 8 + g;
+        dst[t][w] = (cur.seg < nseg && tok < p.M)
+                        ? ldg16(p.x + (size_t)tok * p.K + (size_t)cur.ch * kChunkK + 32 * c + 8 * w)
+                        : make_uint4(0, 0, 0, 0);
+      }
+  };
+  if (XPF) load_x(ccur, xcur);
   int slot = 0;
   __syncthreads();                                      // scales staged
 
@@ -274,6 +322,11 @@ __device__ void streamer_block(const DecodeParams& p, float* smem) {
     while (ccur.seg == seg) {
       issue(icur, (slot + kStages - 1) % kStages);
       next_item(icur);
+      Cursor nx = ccur;
+      next_item(nx);
+      uint4 xnext[MT][4];
+      if (XPF) load_x(nx, xnext);                        // in flight while this item computes
+      else load_x(ccur, xcur);
       cp_async_wait<kStages - 1>();
       const uint4 wlo = my_ring[(slot * 2 + 0) * 32 + lane];
       const uint4 whi = my_ring[(slot * 2 + 1) * 32 + lane];
@@ -289,7 +342,6 @@ __device__ void streamer_block(const DecodeParams& p, float* smem) {
         for (int i = 0; i < 4; ++i) part[t][i] = 0.0f;
       const uint32_t wl[4] = {wlo.x, wlo.y, wlo.z, wlo.w};
       const uint32_t wh[4] = {whi.x, whi.y, whi.z, whi.w};
-      const size_t kbase = (size_t)ch * kChunkK + 32 * c;
 #pragma unroll
       for (int w = 0; w < 4; ++w) {
         uint32_t va[4], vb[4];
@@ -302,9 +354,7 @@ __device__ void streamer_block(const DecodeParams& p, float* smem) {
         }
 #pragma unroll
         for (int t = 0; t < MT; ++t) {
-          const int tok = t * 8 + g;
-          uint4 xv = make_uint4(0, 0, 0, 0);
-          if (tok < p.M) xv = ldg16(p.x + (size_t)tok * p.K + kbase + 8 * w);
+          const uint4 xv = xcur[t][w];
           // k positions: step 0 pairs nibbles (0,4),(1,5); step 1 pairs (2,6),(3,7)
           const uint32_t b00 = __byte_perm(xv.x, xv.z, 0x5410), b01 = __byte_perm(xv.x, xv.z, 0x7632);
           const uint32_t b10 = __byte_perm(xv.y, xv.w, 0x5410), b11 = __byte_perm(xv.y, xv.w, 0x7632);
@@ -328,11 +378,18 @@ __device__ void streamer_block(const DecodeParams& p, float* smem) {
           acc[t][3] = fmaf(shi, part[t][3], acc[t][3]);
         }
       }
-      next_item(ccur);
+      if (XPF) {
+#pragma unroll
+        for (int t = 0; t < MT; ++t)
+#pragma unroll
+          for (int w = 0; w < 4; ++w) xcur[t][w] = xnext[t][w];
+      }
+      ccur = nx;
       slot = (slot + 1) % kStages;
     }
 
-    // ---- segment done: fixed-order sum over warps
+    // ---- segment done: fixed-order sum over warps into ybuf (whole tile) or
+    // this block's part of a shared tile (workspace; finished at the end)
 #pragma unroll
     for (int t = 0; t < MT; ++t)
 #pragma unroll
@@ -341,40 +398,44 @@ __device__ void streamer_block(const DecodeParams& p, float* smem) {
     const long long tu0 = (long long)tile * p.nchunks, tu1 = tu0 + p.nchunks;
     const int first = unit_owner(tu0, p.units, p.P), last = unit_owner(tu1 - 1, p.units, p.P);
     const int parts = last - first + 1;
-    const int part_idx = b - first;
     float* dst = (parts == 1) ? ybuf + seg * MT * 128
-                              : p.ws_part + ((size_t)tile * p.max_parts + part_idx) * MT * 128;
+                              : p.ws_part + ((size_t)tile * p.max_parts + (b - first)) * MT * 128;
     for (int e = threadIdx.x; e < MT * 128; e += kThreads) {
-      float s = 0.0f;
+      float v = 0.0f;
 #pragma unroll
-      for (int w = 0; w < kWarps; ++w) s += red[w * MT * 128 + e];
-      dst[e] = s;
+      for (int w = 0; w < kWarps; ++w) v += red[w * MT * 128 + e];
+      dst[e] = v;
     }
-    if (parts > 1) {
-      __syncthreads();
-      if (threadIdx.x == 0) {
-        __threadfence();
-        const unsigned old = atomicAdd(&p.ws_tile_cnt[tile], 1u);
-        s_flag = (old == (unsigned)(parts - 1));
-        if (s_flag) p.ws_tile_cnt[tile] = 0;           // every part has arrived
-      }
-      __syncthreads();
-      if (s_flag) {
-        __threadfence();
-        const float* src = p.ws_part + (size_t)tile * p.max_parts * MT * 128;
-        for (int e = threadIdx.x; e < MT * 128; e += kThreads) {
-          float s = 0.0f;
-          for (int pi = 0; pi < parts; ++pi) s += __ldcg(src + (size_t)pi * MT * 128 + e);
-          ybuf[seg * MT * 128 + e] = s;
-        }
-      }
-      if (threadIdx.x == 0) s_fixup[seg] = s_flag;
-    } else if (threadIdx.x == 0) {
-      s_fixup[seg] = 1;
-    }
+    if (threadIdx.x == 0) s_parts[seg] = parts;
     __syncthreads();
   }
   cp_async_wait<0>();
+
+  // ---- one synchronisation point for every shared tile: arrive, and the
+  // last block to arrive sums the parts (fixed order) and stores the tile
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int seg = 0; seg < nseg; ++seg) {
+      if (s_parts[seg] == 1) { s_fixup[seg] = 1; continue; }
+      const int tile = tile0 + seg;
+      const unsigned old = atomicAdd(&p.ws_tile_cnt[tile], 1u);
+      const int lastp = old == (unsigned)(s_parts[seg] - 1);
+      if (lastp) p.ws_tile_cnt[tile] = 0;               // every part has arrived
+      s_fixup[seg] = lastp;
+    }
+    __threadfence();
+  }
+  __syncthreads();
+  for (int seg = 0; seg < nseg; ++seg) {
+    if (s_parts[seg] == 1 || !s_fixup[seg]) continue;
+    const float* src = p.ws_part + (size_t)(tile0 + seg) * p.max_parts * MT * 128;
+    for (int e = threadIdx.x; e < MT * 128; e += kThreads) {
+      float v = 0.0f;
+      for (int pi = 0; pi < s_parts[seg]; ++pi) v += __ldcg(src + (size_t)pi * MT * 128 + e);
+      ybuf[seg * MT * 128 + e] = v;
+    }
+  }
 
   // ---- the compensator's down-projection (published by the producers)
   if (COMP) {
@@ -384,7 +445,7 @@ __device__ void streamer_block(const DecodeParams& p, float* smem) {
       for (unsigned it = 0;; ++it) {
         if (ld_acquire_gpu(&p.ws_sync[1])) { ok = 1; break; }
         if ((it & 63) == 63 && globaltimer_ns() - t0 > kWaitLimitNs) break;
-        __nanosleep(64);
+        __nanosleep(32);
       }
       if (!ok) record_status(&g_decode_status, DEV_ERR_TIMEOUT);
       s_flag = ok;
@@ -403,8 +464,8 @@ __device__ void streamer_block(const DecodeParams& p, float* smem) {
       Ts[Mpad * (p.r / 2) + m * (p.r / 2) + jj / 2] =
           pack_bf16x2(t0v - __bfloat162float(h0), t1v - __bfloat162float(h1));
     }
-    __syncthreads();
   }
+  __syncthreads();
 
   // ---- epilogue: y = acc (* per-channel scale) + B T, one (segment, token tile) per warp
   for (int item = warp; item < nseg * MT; item += kWarps) {
@@ -526,10 +587,11 @@ int build_plan(const spear_w4_layer& L, int MT, bool comp, const DeviceInfo& di,
   bool settled = false;
   for (int iter = 0; iter < 8 && !settled; ++iter) {
     if (has_rank) {
-      const double a_bytes = (double)(L.rank + 1) * L.K * 2.0;
-      const double w_bytes = (double)L.N * L.K / 2.0;
-      const int q = (int)(blocks * a_bytes / (a_bytes + w_bytes) + 0.5);
-      pl->Q = std::max(1, std::min(q, std::min(16, pl->nchunks)));
+      // RT row tiles x S K-slices; one slice's A bytes ~ one streamer's weight bytes
+      const int RT = (L.rank + 1 + 15) / 16;
+      const double w_per_block = (double)L.N * L.K / 2.0 / std::max(1, blocks - RT);
+      const int S = (int)std::lround(32.0 * L.K / w_per_block);
+      pl->Q = RT * std::max(1, std::min(S, std::min(kMaxSlices, pl->nchunks)));
     } else {
       pl->Q = 0;
     }
@@ -557,7 +619,7 @@ int build_plan(const spear_w4_layer& L, int MT, bool comp, const DeviceInfo& di,
   size_t off = 0;
   pl->off_sync = off; off = align256(off + 4 * sizeof(unsigned));
   pl->off_cnt = off;  off = align256(off + (size_t)pl->tiles * sizeof(unsigned));
-  pl->off_prod = off; off = align256(off + (size_t)std::max(pl->Q, 1) * Mpad * pl->Rpad * 4);
+  pl->off_prod = off; off = align256(off + (size_t)std::max(pl->Q, 1) * Mpad * 16 * 4);
   pl->off_T = off;    off = align256(off + (size_t)Mpad * std::max(L.rank, 1) * 4);
   pl->off_part = off; off = align256(off + (size_t)pl->tiles * pl->max_parts * pl->MT * 128 * 4);
   pl->total = off;
@@ -642,6 +704,55 @@ int launch_decode(const spear_w4_layer& L, const uint16_t* x, int M, void* y, in
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cuda_check(cudaLaunchKernelEx(&cfg, pl.fn, p), "decode launch");
+}
+
+// ---------------------------------------------------------------------------
+// Decode without a caller workspace.  Some callers cannot allocate device
+// memory when they call the layer: plugins hosted by a framework that owns the
+// device allocator, runtimes that plan every buffer before serving starts and
+// forbid allocation afterwards, and code on latency-critical paths where an
+// allocation could synchronise the device.  For them the decode scratch lives
+// in one fixed array in this module (kNoallocScratchBytes, held by every GPU
+// that loads the library until the process exits).
+constexpr size_t kNoallocScratchBytes = size_t(8) << 20;   // 8 MiB
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocScratchBytes];
+
+namespace {
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[64] = {};      // device address of the scratch array, per device
+
+// Once per device, with that device current: the array's device address (the
+// symbol itself is only a host-side stand-in) and one zero fill.
+int noalloc_scratch(void** out) {
+  int dev = 0;
+  if (int rc = cuda_check(cudaGetDevice(&dev), "cudaGetDevice")) return rc;
+  if (dev < 0 || dev >= 64) return fail(SPEAR_ERR_UNSUPPORTED, "device index %d", dev);
+  std::lock_guard<std::mutex> lk(g_noalloc_mu);
+  if (!g_noalloc_ptr[dev]) {
+    void* ptr = nullptr;
+    if (int rc = cuda_check(cudaGetSymbolAddress((void**)&ptr, g_noalloc_scratch), "decode scratch address"))
+      return rc;
+    if (int rc = cuda_check(cudaMemset(ptr, 0, kNoallocScratchBytes), "decode scratch zero fill")) return rc;
+    g_noalloc_ptr[dev] = ptr;
+  }
+  *out = g_noalloc_ptr[dev];
+  return SPEAR_OK;
+}
+}  // namespace
+
+int launch_decode_noalloc(const spear_w4_layer& L, const uint16_t* x, int M, void* y, int out_f32,
+                          cudaStream_t st) {
+  Plan pl;
+  if (int rc = get_plan(L, M, &pl)) return rc;
+  if (pl.total > kNoallocScratchBytes)
+    return fail(SPEAR_ERR_UNSUPPORTED,
+                "decode_noalloc: N=%d K=%d M=%d needs %zu B of scratch; the built-in scratch holds %zu B",
+                L.N, L.K, M, pl.total, kNoallocScratchBytes);
+  void* ws = nullptr;
+  if (int rc = noalloc_scratch(&ws)) return rc;
+  // the synchronisation words and tile counters must start at zero
+  if (int rc = cuda_check(cudaMemsetAsync(ws, 0, pl.off_prod, st), "decode scratch clear")) return rc;
+  return launch_decode(L, x, M, y, out_f32, ws, kNoallocScratchBytes, st);
 }
 
 int read_and_clear_status_decode(unsigned* out, cudaStream_t st) {

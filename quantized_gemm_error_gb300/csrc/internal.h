@@ -33,6 +33,8 @@ int read_and_clear_status_pack(unsigned* out, cudaStream_t st);
 int decode_workspace_bytes(const spear_w4_layer& L, int M, size_t* bytes);
 int launch_decode(const spear_w4_layer& L, const uint16_t* x, int M, void* y, int out_f32,
                   void* ws, size_t ws_bytes, cudaStream_t st);
+int launch_decode_noalloc(const spear_w4_layer& L, const uint16_t* x, int M, void* y, int out_f32,
+                          cudaStream_t st);
 int read_and_clear_status_decode(unsigned* out, cudaStream_t st);
 
 // ---- prefill.cu

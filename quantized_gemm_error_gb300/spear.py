@@ -30,7 +30,7 @@ OUT_BF16, OUT_F32 = 0, 1
 
 # every symbol include/spear.h declares
 EXPORTS = ["spear_pack_w4_sizes", "spear_pack_w4", "spear_decode_workspace_bytes",
-           "spear_linear_decode", "spear_prefill_workspace_bytes", "spear_linear_prefill",
+           "spear_linear_decode", "spear_linear_decode_noalloc", "spear_prefill_workspace_bytes", "spear_linear_prefill",
            "spear_workspace_init", "spear_layer_select_mask", "spear_get_device_status",
            "spear_status_string", "spear_last_error", "spear_version"]
 
@@ -70,6 +70,7 @@ def load(path: str = LIB_PATH):
             "spear_pack_w4": [P, I, I, I, I, P, P, P, P],
             "spear_decode_workspace_bytes": [LP, I, ctypes.POINTER(S)],
             "spear_linear_decode": [LP, P, I, P, I, P, S, P],
+            "spear_linear_decode_noalloc": [LP, P, I, P, I, P],
             "spear_prefill_workspace_bytes": [LP, I, I, ctypes.POINTER(S)],
             "spear_linear_prefill": [LP, P, I, P, I, I, P, S, P, P],
             "spear_workspace_init": [P, S, P],
@@ -214,6 +215,17 @@ def spear_linear_decode(layer: W4Layer, x: torch.Tensor, *, y=None, out_dtype: i
     L = layer.c_struct()
     _check(load().spear_linear_decode(ctypes.byref(L), _ptr(x), M, _ptr(y), out_dtype, _ptr(workspace),
                                       workspace.numel(), _stream(stream)), "spear_linear_decode")
+    return y
+
+
+def spear_linear_decode_noalloc(layer: W4Layer, x: torch.Tensor, *, y: torch.Tensor,
+                                out_dtype: int = OUT_BF16, stream=None) -> torch.Tensor:
+    """Decode for callers that cannot allocate device memory: the library keeps
+    the scratch in a fixed 8 MiB array of its own, so the caller passes only
+    inputs and the output buffer.  Calls that overlap on the GPU race."""
+    L = layer.c_struct()
+    _check(load().spear_linear_decode_noalloc(ctypes.byref(L), _ptr(x), x.shape[0], _ptr(y), out_dtype,
+                                              _stream(stream)), "spear_linear_decode_noalloc")
     return y
 
 

@@ -1,0 +1,85 @@
+"""The decode entry point for callers that cannot allocate device memory.
+
+Plugins hosted by a framework that owns the device allocator, runtimes that
+plan every buffer before serving and forbid allocation afterwards, and code on
+latency-critical paths where an allocation could synchronise the device all
+need a decode call that takes only inputs and outputs.  spear_linear_decode_noalloc
+keeps its scratch in a fixed array inside the library instead of a caller
+workspace.  Its output must match spear_linear_decode's within the parity
+tolerance, on two calls in a row (the second reuses what the first left in the
+shared scratch), and it must refuse shapes whose scratch would not fit.
+
+This file is collected last so that a run stopping at the first failure has
+already run every other test; it also passes when run alone.
+"""
+import numpy as np
+import pytest
+import torch
+
+from spear_testutil import check_close, gpu_layer, make_layer, make_tokens, to_dev_u16
+
+pytestmark = pytest.mark.gpu
+
+
+def _spear():
+    from quantized_gemm_error_gb300 import spear
+    return spear
+
+
+@pytest.mark.parametrize("N,K,G,sym,r,M", [
+    (1024, 2048, 128, False, 32, 4),        # group-128 asymmetric, rank 32
+    (1024, 1024, 1024, True, 16, 1),        # per-channel symmetric, rank 16
+    (4096, 4096, 128, False, 32, 16),       # Llama-7B square linear
+])
+def test_noalloc_decode_matches_workspace_decode(N, K, G, sym, r, M):
+    sp = _spear()
+    lay, rng = make_layer(N, K, r, seed=90 + N + M)
+    L = gpu_layer(lay, G, sym)
+    for out_dtype, dt in ((sp.OUT_BF16, torch.bfloat16), (sp.OUT_F32, torch.float32)):
+        x = to_dev_u16(make_tokens(rng, M, K, outlier_frac=0.01), torch.bfloat16)
+        ref = sp.spear_linear_decode(L, x, out_dtype=out_dtype)
+        torch.cuda.synchronize()
+        ref64 = ref.float().cpu().numpy().astype(np.float64)
+        for call in range(2):                    # two calls in a row on the shared scratch
+            y = torch.full((M, N), float("nan"), dtype=dt, device="cuda")
+            sp.spear_linear_decode_noalloc(L, x, y=y, out_dtype=out_dtype)
+            torch.cuda.synchronize()
+            assert sp.spear_get_device_status() == 0
+            check_close(y, ref64, f"noalloc call {call + 1}")
+
+
+def test_noalloc_decode_alternating_shapes():
+    """Calls with different layers and token counts back to back share the one scratch."""
+    sp = _spear()
+    cases = []
+    for i, (N, K, M) in enumerate([(1024, 1024, 3), (512, 2048, 64), (1024, 1024, 1)]):
+        lay, rng = make_layer(N, K, 32, seed=95 + i)
+        L = gpu_layer(lay, 128, False)
+        x = to_dev_u16(make_tokens(rng, M, K), torch.bfloat16)
+        cases.append((L, x, sp.spear_linear_decode(L, x, out_dtype=sp.OUT_F32)))
+    torch.cuda.synchronize()
+    for L, x, ref in cases + cases:
+        y = torch.empty(ref.shape, dtype=torch.float32, device="cuda")
+        sp.spear_linear_decode_noalloc(L, x, y=y, out_dtype=sp.OUT_F32)
+        torch.cuda.synchronize()
+        check_close(y, ref.cpu().numpy().astype(np.float64), "noalloc")
+    assert sp.spear_get_device_status() == 0
+
+
+def test_noalloc_rejects_shapes_beyond_its_scratch():
+    """28672 x 8192 at M = 64 needs more decode scratch than the built-in array holds."""
+    sp = _spear()
+    N, K, r, M = 28672, 8192, 64, 64
+    dev = "cuda"
+    bf = torch.bfloat16
+    L = sp.W4Layer(N, K, 128, False, torch.zeros(N, K // 2, dtype=torch.uint8, device=dev),
+                   torch.zeros(N, K // 128, dtype=torch.float16, device=dev),
+                   torch.zeros(N, K // 256, dtype=torch.uint8, device=dev), r,
+                   torch.zeros(r, K, dtype=bf, device=dev), torch.zeros(N, r, dtype=bf, device=dev),
+                   torch.zeros(K, dtype=bf, device=dev), 0.0, 1.0, True)
+    assert sp.spear_decode_workspace_bytes(L, M) > 8 << 20
+    x = torch.zeros(M, K, dtype=bf, device=dev)
+    y = torch.zeros(M, N, dtype=bf, device=dev)
+    with pytest.raises(sp.SpearError) as e:
+        sp.spear_linear_decode_noalloc(L, x, y=y)
+    assert e.value.status == 2 and "scratch" in str(e.value)
