@@ -63,22 +63,14 @@ struct DecodeParams {
   // work split
   int Q, P;                 // producer / streamer blocks
   int tiles, nchunks;       // N/16, K/128
-  long long units;          // tiles * nchunks
-  int max_tiles;            // most tiles one streamer touches
-  int max_parts;            // most streamers sharing one tile
+  int max_tiles;            // most tiles one streamer owns
   int ng;                   // K/G
   // workspace
   float* ws_prod;           // [Q][Mpad][16]
   float* ws_T;              // [Mpad][r]
-  float* ws_part;           // [tiles][max_parts][MT*4*32]
-  unsigned* ws_tile_cnt;    // [tiles]
   unsigned* ws_sync;        // [0] producer ticket, [1] T flag, [2] streamer ticket
 };
 
-__device__ __forceinline__ long long unit_begin(long long b, long long U, int P) { return b * U / P; }
-__device__ __forceinline__ int unit_owner(long long u, long long U, int P) {
-  return (int)(((u + 1) * P + U - 1) / U - 1);
-}
 
 // ---------------------------------------------------------------- producer --
 // Producer block q computes the partial P[m][i] = sum_{k in slice s} W'[i][k] x[m][k]
@@ -191,175 +183,226 @@ __device__ void producer_block(const DecodeParams& p, float* smem) {
 }
 
 // ---------------------------------------------------------------- streamer --
-
-// Work cursor of one warp over its items: (segment, chunk) with chunk stepping
-// by kWarps inside [ca, cb) of each segment.
-struct Cursor {
-  int seg, ch;
-};
-
-template <int MT, bool COMP, bool PERCH>
+// Block b owns whole 16-row tiles [t0, t1) of Wq (t = b * tiles / P), so no
+// partial sum ever leaves the block.  Its 8 warps split each tile's K range
+// (warp w takes chunks w, w + 8, ...); weights stream through a per-warp
+// cp.async ring in the order (tile, chunk) and become exact small integers in
+// registers; the tokens enter mma.sync as B fragments.
+//
+// XS (M <= 8, tokens small enough for shared memory): the block first copies x
+// as fp16 (exact for |x| < 65504) in B-fragment order and keeps per-128-k sums
+// of the even-k and odd-k tokens.  The weights then enter fp16 MMAs straight
+// from the nibbles with no subtraction -- the low nibble of each byte becomes
+// 1024 + u through an fp16 exponent bias, the high nibble (left in place)
+// 64 + u -- and the constant parts and the zero point are removed per 128-k
+// chunk in fp32:
+//   sum_k (u_k - z) x_k = sum_k (c_k + u_k) x_k - (1024 + z) E - (64 + z) O,
+//   c_k = 1024 (k even) or 64 (k odd),  E / O = sums of x over even / odd k.
+// Otherwise the nibbles become 128 + u through a bf16 bias, the biased zero
+// point is subtracted (exact), and bf16 MMAs read the tokens from L1.
+template <int MT, bool COMP, bool PERCH, bool XS>
 __device__ void streamer_block(const DecodeParams& p, float* smem) {
-  constexpr bool XPF = (MT == 1);                        // prefetch the next item's tokens in registers
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, c = lane & 3;
   const int b = blockIdx.x - p.Q;
-  const long long u0 = unit_begin(b, p.units, p.P), u1 = unit_begin(b + 1, p.units, p.P);
-  const int tile0 = (int)(u0 / p.nchunks);
-  const int tile_last = u1 > u0 ? (int)((u1 - 1) / p.nchunks) : tile0 - 1;
-  const int nseg = tile_last - tile0 + 1;                  // 0 for an empty range
+  const int t0 = (int)((long long)b * p.tiles / p.P), t1 = (int)((long long)(b + 1) * p.tiles / p.P);
+  const int ntl = t1 - t0;                                   // tiles of this block
   const int Mpad = MT * 8;
   const size_t half_k = (size_t)p.K / 2;
+  const int k8 = p.K / 8;
+  const int xrow = k8 + 1;
 
-  // shared memory carve-up
   uint4* ring = reinterpret_cast<uint4*>(smem);                       // [kWarps][kStages][2][32]
   float* red = smem + kWarps * kStages * 2 * 32 * 4;                  // [kWarps][MT][4][32]
   float* ybuf = red + kWarps * MT * 4 * 32;                           // [max_tiles][MT][4][32]
   uint32_t* Ts = reinterpret_cast<uint32_t*>(ybuf + p.max_tiles * MT * 4 * 32);  // [Mpad][r/2] hi, then lo
   __half* sc_s = reinterpret_cast<__half*>(Ts + (COMP ? Mpad * kMaxRank : 0));   // [max_tiles][16][ng]
   uint8_t* z_s = reinterpret_cast<uint8_t*>(sc_s + p.max_tiles * 16 * p.ng);     // [max_tiles][16][ng]
-  __shared__ int s_parts[64];      // streamers sharing the segment's tile (1 = this block owns it)
-  __shared__ int s_fixup[64];      // 1 when this block stores the segment's tile
+  uint4* xs = reinterpret_cast<uint4*>((reinterpret_cast<uintptr_t>(z_s + p.max_tiles * 16 * p.ng) + 15) &
+                                       ~uintptr_t(15));                           // [M][xrow] (XS)
+  float* Ps = reinterpret_cast<float*>(xs + (XS ? p.M * xrow : 0));  // [M][nchunks] 1024 E + 64 O (XS)
+  float* Xs = Ps + (XS ? p.M * p.nchunks : 0);                       // [M][nchunks] E + O (XS)
   __shared__ int s_flag;
 
-  auto seg_ca = [&](int s) {
-    return (int)(max(u0, (long long)(tile0 + s) * p.nchunks) - (long long)(tile0 + s) * p.nchunks);
-  };
-  auto seg_cb = [&](int s) {
-    return (int)(min(u1, (long long)(tile0 + s + 1) * p.nchunks) - (long long)(tile0 + s) * p.nchunks);
-  };
-
-  // per-warp item cursor over the segments
-  auto first_item = [&](Cursor& cur) {
-    cur.seg = 0;
-    cur.ch = nseg > 0 ? seg_ca(0) + warp : 0;
-    while (cur.seg < nseg && cur.ch >= seg_cb(cur.seg)) {
-      ++cur.seg;
-      if (cur.seg < nseg) cur.ch = seg_ca(cur.seg) + warp;
-    }
-  };
-  auto next_item = [&](Cursor& cur) {
-    cur.ch += kWarps;
-    while (cur.seg < nseg && cur.ch >= seg_cb(cur.seg)) {
-      ++cur.seg;
-      if (cur.seg < nseg) cur.ch = seg_ca(cur.seg) + warp;
-    }
-  };
+  // work items of this warp: (tile, chunk), chunk = warp + 8 j; the issue
+  // cursor walks them with pointer increments only
+  const int per_tile = (p.nchunks - warp + kWarps - 1) / kWarps;     // chunks of each tile for this warp
+  const int nitems = ntl * per_tile;
   uint4* my_ring = ring + warp * kStages * 2 * 32;
-  auto issue = [&](const Cursor& cur, int slot) {
-    if (cur.seg < nseg) {
-      const int n0 = (tile0 + cur.seg) * 16;
-      const uint8_t* src = p.qweight + (size_t)(n0 + g) * half_k + (size_t)cur.ch * (kChunkK / 2) + c * 16;
+  const uint8_t* tile_base = p.qweight + (size_t)(t0 * 16 + g) * half_k + (size_t)warp * (kChunkK / 2) + c * 16;
+  const size_t tile_step = 16 * half_k;                              // bytes between tiles
+  const uint8_t* src = tile_base;
+  int issued = 0, ij = 0;
+  auto issue = [&](int slot) {
+    if (issued < nitems) {
       cp_async16(my_ring + (slot * 2 + 0) * 32 + lane, src);
       cp_async16(my_ring + (slot * 2 + 1) * 32 + lane, src + 8 * half_k);
+      ++issued;
+      if (++ij == per_tile) { ij = 0; tile_base += tile_step; src = tile_base; }
+      else src += kWarps * (kChunkK / 2);
     }
     cp_async_commit();
   };
 
-  // 1. weight stream first
-  Cursor icur, ccur;
-  first_item(icur);
-  ccur = icur;
+  // 1. tokens (XS) and scales first -- they gate the first MMA -- then the weight stream
+  const int xunits = XS ? p.M * k8 : 0;
+  constexpr int kXBatch = XS ? 4 : 1;
+  uint4 xr[kXBatch];
+  if (XS) {
 #pragma unroll
-  for (int s = 0; s < kStages - 1; ++s) {
-    issue(icur, s);
-    next_item(icur);
-  }
-  // 2. scales and zero points of every touched tile, loads batched ahead of the stores
-  {
-    const int total = nseg * 16 * p.ng;
-    const int zrow = (p.ng + 1) / 2;
-    for (int e0 = threadIdx.x; e0 < total; e0 += 8 * kThreads) {
-      __half sv[8];
-      uint8_t zv[8];
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const int e = e0 + u * kThreads;
-        sv[u] = __ushort_as_half(0);
-        zv[u] = 8;
-        if (e < total) {
-          const int sg = e / (16 * p.ng), rem = e % (16 * p.ng), row = rem / p.ng, gi = rem % p.ng;
-          const int n = (tile0 + sg) * 16 + row;
-          sv[u] = p.scales[(size_t)n * p.ng + gi];
-          if (!p.sym) {
-            const uint8_t zb = p.zeros[(size_t)n * zrow + gi / 2];
-            zv[u] = (gi & 1) ? (zb >> 4) : (zb & 15);
-          }
-        }
-      }
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const int e = e0 + u * kThreads;
-        if (e < total) { sc_s[e] = sv[u]; z_s[e] = zv[u]; }
-      }
+    for (int j = 0; j < kXBatch; ++j) {
+      const int e = threadIdx.x + j * kThreads;
+      xr[j] = e < xunits ? ldg16(p.x + (size_t)e * 8) : make_uint4(0, 0, 0, 0);
     }
   }
-  // 3. tokens of the first item
-  uint4 xcur[MT][4];
-  auto load_x = [&](const Cursor& cur, uint4 (&dst)[MT][4]) {
-#pragma unroll
-    for (int t = 0; t < MT; ++t)
-#pragma unroll
-      for (int w = 0; w < 4; ++w) {
-        const int tok = t * 8 + g;
-        dst[t][w] = (cur.seg < nseg && tok < p.M)
-                        ? ldg16(p.x + (size_t)tok * p.K + (size_t)cur.ch * kChunkK + 32 * c + 8 * w)
-                        : make_uint4(0, 0, 0, 0);
-      }
+  const int total_sc = ntl * 16 * p.ng;
+  const int zrow = (p.ng + 1) / 2;
+  auto load_sc = [&](int e, __half& sv, uint8_t& zv) {
+    const int tl = e / (16 * p.ng), rem = e % (16 * p.ng), row = rem / p.ng, gi = rem % p.ng;
+    const int n = (t0 + tl) * 16 + row;
+    sv = p.scales[(size_t)n * p.ng + gi];
+    zv = 8;
+    if (!p.sym) {
+      const uint8_t zb = p.zeros[(size_t)n * zrow + gi / 2];
+      zv = (gi & 1) ? (zb >> 4) : (zb & 15);
+    }
   };
-  if (XPF) load_x(ccur, xcur);
-  int slot = 0;
-  __syncthreads();                                      // scales staged
+  __half sv[8];
+  uint8_t zv[8];
+#pragma unroll
+  for (int u = 0; u < 8; ++u) {
+    const int e = threadIdx.x + u * kThreads;
+    sv[u] = __ushort_as_half(0);
+    zv[u] = 8;
+    if (e < total_sc) load_sc(e, sv[u], zv[u]);
+  }
+#pragma unroll
+  for (int s = 0; s < kStages - 1; ++s) issue(s);
 
-  for (int seg = 0; seg < nseg; ++seg) {
-    const int tile = tile0 + seg;
+  // 2. stage scales / zero points (and the tokens for XS)
+#pragma unroll
+  for (int u = 0; u < 8; ++u) {
+    const int e = threadIdx.x + u * kThreads;
+    if (e < total_sc) { sc_s[e] = sv[u]; z_s[e] = zv[u]; }
+  }
+  for (int e = threadIdx.x + 8 * kThreads; e < total_sc; e += kThreads) load_sc(e, sc_s[e], z_s[e]);
+  if (XS) {
+    bool bad = false;
+    // 16 consecutive units (128 k) of one token are 16 consecutive lanes: their
+    // E / O partials reduce with 4 shuffles (padding units contribute zeros).
+    for (int j0 = 0; j0 < xunits; j0 += kThreads * kXBatch) {
+#pragma unroll
+      for (int j = 0; j < kXBatch; ++j) {
+        const int e = threadIdx.x + j0 + j * kThreads;
+        uint4 v;
+        if (j0 == 0) v = xr[j];
+        else v = e < xunits ? ldg16(p.x + (size_t)e * 8) : make_uint4(0, 0, 0, 0);
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};          // (x0,x1) (x2,x3) (x4,x5) (x6,x7)
+        float f[8];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) { f[2 * i] = bf16x2_lo(w[i]); f[2 * i + 1] = bf16x2_hi(w[i]); }
+        float ev = (f[0] + f[2]) + (f[4] + f[6]);
+        float od = (f[1] + f[3]) + (f[5] + f[7]);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) bad |= !(fabsf(f[i]) < 65504.0f);
+        auto h2 = [](float lo, float hi) {
+          const __half2 h = __floats2half2_rn(lo, hi);
+          return *reinterpret_cast<const uint32_t*>(&h);
+        };
+        if (e < xunits) {
+          const int m = e / k8, kk = e % k8;
+          xs[m * xrow + kk] = make_uint4(h2(f[0], f[4]), h2(f[1], f[5]), h2(f[2], f[6]), h2(f[3], f[7]));
+        }
+#pragma unroll
+        for (int o = 1; o < 16; o <<= 1) {
+          ev += __shfl_xor_sync(0xffffffffu, ev, o);
+          od += __shfl_xor_sync(0xffffffffu, od, o);
+        }
+        if ((lane & 15) == 0 && e < xunits) {
+          const int m = e / k8, ch = (e % k8) / 16;
+          Ps[m * p.nchunks + ch] = 1024.0f * ev + 64.0f * od;
+          Xs[m * p.nchunks + ch] = ev + od;
+        }
+      }
+    }
+    if (bad) record_status(&g_decode_status, DEV_ERR_INVALID);
+  }
+  __syncthreads();
+
+  // 3. main loop
+  int slot = 0;
+  const bool tok_ok = g < p.M;
+  const int u0 = 2 * c, u1 = 2 * c + 1;                   // this lane's output tokens (XS)
+  const bool ok0 = u0 < p.M, ok1 = u1 < p.M;
+  for (int tl = 0; tl < ntl; ++tl) {
     float acc[MT][4];
 #pragma unroll
     for (int t = 0; t < MT; ++t)
 #pragma unroll
       for (int i = 0; i < 4; ++i) acc[t][i] = 0.0f;
-
-    while (ccur.seg == seg) {
-      issue(icur, (slot + kStages - 1) % kStages);
-      next_item(icur);
-      Cursor nx = ccur;
-      next_item(nx);
-      uint4 xnext[MT][4];
-      if (XPF) load_x(nx, xnext);                        // in flight while this item computes
-      else load_x(ccur, xcur);
+    const int srow = tl * 16 * p.ng;
+    const __half* sc_lo = sc_s + srow + g * p.ng;
+    const __half* sc_hi = sc_lo + 8 * p.ng;
+    const uint8_t* z_lo = z_s + srow + g * p.ng;
+    const uint8_t* z_hi = z_lo + 8 * p.ng;
+    for (int j = 0; j < per_tile; ++j) {
+      issue((slot + kStages - 1) % kStages);
       cp_async_wait<kStages - 1>();
+      const int ch = warp + kWarps * j;
+      const int gi = PERCH ? 0 : ch;                       // group 128 = one chunk
       const uint4 wlo = my_ring[(slot * 2 + 0) * 32 + lane];
       const uint4 whi = my_ring[(slot * 2 + 1) * 32 + lane];
-      const int ch = ccur.ch;
-      const int gi = ch * kChunkK / p.G;
-      const int srow = seg * 16 * p.ng;
-      const uint32_t zlo = bf16x2_bias(z_s[srow + g * p.ng + gi]);
-      const uint32_t zhi = bf16x2_bias(z_s[srow + (g + 8) * p.ng + gi]);
+      const uint32_t wl[4] = {wlo.x, wlo.y, wlo.z, wlo.w};
+      const uint32_t wh[4] = {whi.x, whi.y, whi.z, whi.w};
+      const int zl = z_lo[gi], zh = z_hi[gi];
       float part[MT][4];
 #pragma unroll
       for (int t = 0; t < MT; ++t)
 #pragma unroll
         for (int i = 0; i < 4; ++i) part[t][i] = 0.0f;
-      const uint32_t wl[4] = {wlo.x, wlo.y, wlo.z, wlo.w};
-      const uint32_t wh[4] = {whi.x, whi.y, whi.z, whi.w};
+      if constexpr (XS) {
+        const uint4* xrowp = xs + g * xrow + ch * 16 + 4 * c;
 #pragma unroll
-      for (int w = 0; w < 4; ++w) {
-        uint32_t va[4], vb[4];
-        nibbles_to_bf16x2_biased(wl[w], va);
-        nibbles_to_bf16x2_biased(wh[w], vb);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          va[i] = bf16x2_sub(va[i], zlo);                // exact (u - z)
-          vb[i] = bf16x2_sub(vb[i], zhi);
+        for (int w = 0; w < 4; ++w) {
+          const uint32_t l8 = wl[w] >> 8, h8 = wh[w] >> 8;
+          // step 0: (n0, n4) as 1024 + u, (n1, n5) as 64 + u; step 1: the same for n2 .. n7
+          const uint32_t a0 = (wl[w] & 0x000F000Fu) | 0x64006400u, a1 = (wh[w] & 0x000F000Fu) | 0x64006400u;
+          const uint32_t a2 = (wl[w] & 0x00F000F0u) | 0x54005400u, a3 = (wh[w] & 0x00F000F0u) | 0x54005400u;
+          const uint32_t e0 = (l8 & 0x000F000Fu) | 0x64006400u, e1 = (h8 & 0x000F000Fu) | 0x64006400u;
+          const uint32_t e2 = (l8 & 0x00F000F0u) | 0x54005400u, e3 = (h8 & 0x00F000F0u) | 0x54005400u;
+          const uint4 xv = tok_ok ? xrowp[w] : make_uint4(0, 0, 0, 0);
+          mma_f16_16816(part[0], a0, a1, a2, a3, xv.x, xv.y);
+          mma_f16_16816(part[0], e0, e1, e2, e3, xv.z, xv.w);
         }
+        const float P0 = ok0 ? Ps[u0 * p.nchunks + ch] : 0.0f, X0 = ok0 ? Xs[u0 * p.nchunks + ch] : 0.0f;
+        const float P1 = ok1 ? Ps[u1 * p.nchunks + ch] : 0.0f, X1 = ok1 ? Xs[u1 * p.nchunks + ch] : 0.0f;
+        part[0][0] -= fmaf((float)zl, X0, P0);
+        part[0][1] -= fmaf((float)zl, X1, P1);
+        part[0][2] -= fmaf((float)zh, X0, P0);
+        part[0][3] -= fmaf((float)zh, X1, P1);
+      } else {
+        const uint32_t zlo = bf16x2_bias((uint32_t)zl), zhi = bf16x2_bias((uint32_t)zh);
+        const size_t kbase = (size_t)ch * kChunkK + 32 * c;
 #pragma unroll
-        for (int t = 0; t < MT; ++t) {
-          const uint4 xv = xcur[t][w];
-          // k positions: step 0 pairs nibbles (0,4),(1,5); step 1 pairs (2,6),(3,7)
-          const uint32_t b00 = __byte_perm(xv.x, xv.z, 0x5410), b01 = __byte_perm(xv.x, xv.z, 0x7632);
-          const uint32_t b10 = __byte_perm(xv.y, xv.w, 0x5410), b11 = __byte_perm(xv.y, xv.w, 0x7632);
-          mma_bf16_16816(part[t], va[0], vb[0], va[1], vb[1], b00, b01);
-          mma_bf16_16816(part[t], va[2], vb[2], va[3], vb[3], b10, b11);
+        for (int w = 0; w < 4; ++w) {
+          uint32_t va[4], vb[4];
+          nibbles_to_bf16x2_biased(wl[w], va);
+          nibbles_to_bf16x2_biased(wh[w], vb);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            va[i] = bf16x2_sub(va[i], zlo);                  // exact (u - z)
+            vb[i] = bf16x2_sub(vb[i], zhi);
+          }
+#pragma unroll
+          for (int t = 0; t < MT; ++t) {
+            const int tok = t * 8 + g;
+            const uint4 xv = tok < p.M ? ldg16(p.x + (size_t)tok * p.K + kbase + 8 * w) : make_uint4(0, 0, 0, 0);
+            // k positions: step 0 pairs nibbles (0,4),(1,5); step 1 pairs (2,6),(3,7)
+            const uint32_t b00 = __byte_perm(xv.x, xv.z, 0x5410), b01 = __byte_perm(xv.x, xv.z, 0x7632);
+            const uint32_t b10 = __byte_perm(xv.y, xv.w, 0x5410), b11 = __byte_perm(xv.y, xv.w, 0x7632);
+            mma_bf16_16816(part[t], va[0], vb[0], va[1], vb[1], b00, b01);
+            mma_bf16_16816(part[t], va[2], vb[2], va[3], vb[3], b10, b11);
+          }
         }
       }
       if (PERCH) {
@@ -368,8 +411,8 @@ __device__ void streamer_block(const DecodeParams& p, float* smem) {
 #pragma unroll
           for (int i = 0; i < 4; ++i) acc[t][i] += part[t][i];
       } else {
-        const float slo = __half2float(sc_s[srow + g * p.ng + gi]);
-        const float shi = __half2float(sc_s[srow + (g + 8) * p.ng + gi]);
+        const float slo = __half2float(sc_lo[gi]);
+        const float shi = __half2float(sc_hi[gi]);
 #pragma unroll
         for (int t = 0; t < MT; ++t) {
           acc[t][0] = fmaf(slo, part[t][0], acc[t][0]);
@@ -378,73 +421,32 @@ __device__ void streamer_block(const DecodeParams& p, float* smem) {
           acc[t][3] = fmaf(shi, part[t][3], acc[t][3]);
         }
       }
-      if (XPF) {
-#pragma unroll
-        for (int t = 0; t < MT; ++t)
-#pragma unroll
-          for (int w = 0; w < 4; ++w) xcur[t][w] = xnext[t][w];
-      }
-      ccur = nx;
       slot = (slot + 1) % kStages;
     }
-
-    // ---- segment done: fixed-order sum over warps into ybuf (whole tile) or
-    // this block's part of a shared tile (workspace; finished at the end)
+    // tile done: fixed-order sum over the warps
 #pragma unroll
     for (int t = 0; t < MT; ++t)
 #pragma unroll
       for (int i = 0; i < 4; ++i) red[((warp * MT + t) * 4 + i) * 32 + lane] = acc[t][i];
     __syncthreads();
-    const long long tu0 = (long long)tile * p.nchunks, tu1 = tu0 + p.nchunks;
-    const int first = unit_owner(tu0, p.units, p.P), last = unit_owner(tu1 - 1, p.units, p.P);
-    const int parts = last - first + 1;
-    float* dst = (parts == 1) ? ybuf + seg * MT * 128
-                              : p.ws_part + ((size_t)tile * p.max_parts + (b - first)) * MT * 128;
     for (int e = threadIdx.x; e < MT * 128; e += kThreads) {
       float v = 0.0f;
 #pragma unroll
       for (int w = 0; w < kWarps; ++w) v += red[w * MT * 128 + e];
-      dst[e] = v;
+      ybuf[tl * MT * 128 + e] = v;
     }
-    if (threadIdx.x == 0) s_parts[seg] = parts;
     __syncthreads();
   }
   cp_async_wait<0>();
 
-  // ---- one synchronisation point for every shared tile: arrive, and the
-  // last block to arrive sums the parts (fixed order) and stores the tile
-  __threadfence();
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    for (int seg = 0; seg < nseg; ++seg) {
-      if (s_parts[seg] == 1) { s_fixup[seg] = 1; continue; }
-      const int tile = tile0 + seg;
-      const unsigned old = atomicAdd(&p.ws_tile_cnt[tile], 1u);
-      const int lastp = old == (unsigned)(s_parts[seg] - 1);
-      if (lastp) p.ws_tile_cnt[tile] = 0;               // every part has arrived
-      s_fixup[seg] = lastp;
-    }
-    __threadfence();
-  }
-  __syncthreads();
-  for (int seg = 0; seg < nseg; ++seg) {
-    if (s_parts[seg] == 1 || !s_fixup[seg]) continue;
-    const float* src = p.ws_part + (size_t)(tile0 + seg) * p.max_parts * MT * 128;
-    for (int e = threadIdx.x; e < MT * 128; e += kThreads) {
-      float v = 0.0f;
-      for (int pi = 0; pi < s_parts[seg]; ++pi) v += __ldcg(src + (size_t)pi * MT * 128 + e);
-      ybuf[seg * MT * 128 + e] = v;
-    }
-  }
-
-  // ---- the compensator's down-projection (published by the producers)
+  // 4. the compensator's down-projection (published by the producers)
   if (COMP) {
     if (threadIdx.x == 0) {
-      const uint64_t t0 = globaltimer_ns();
+      const uint64_t tw = globaltimer_ns();
       unsigned ok = 0;
-      for (unsigned it = 0;; ++it) {
+      for (unsigned i = 0;; ++i) {
         if (ld_acquire_gpu(&p.ws_sync[1])) { ok = 1; break; }
-        if ((it & 63) == 63 && globaltimer_ns() - t0 > kWaitLimitNs) break;
+        if ((i & 63) == 63 && globaltimer_ns() - tw > kWaitLimitNs) break;
         __nanosleep(32);
       }
       if (!ok) record_status(&g_decode_status, DEV_ERR_TIMEOUT);
@@ -454,31 +456,28 @@ __device__ void streamer_block(const DecodeParams& p, float* smem) {
     // T as bf16 hi + lo (T = hi + lo to ~2^-16 relative)
     for (int e = threadIdx.x; e < Mpad * p.r / 2; e += kThreads) {
       const int m = e / (p.r / 2), jj = (e % (p.r / 2)) * 2;
-      float t0v = 0.0f, t1v = 0.0f;
+      float ta = 0.0f, tb = 0.0f;
       if (s_flag) {
-        t0v = __ldcg(p.ws_T + m * p.r + jj);
-        t1v = __ldcg(p.ws_T + m * p.r + jj + 1);
+        ta = __ldcg(p.ws_T + m * p.r + jj);
+        tb = __ldcg(p.ws_T + m * p.r + jj + 1);
       }
-      const __nv_bfloat16 h0 = __float2bfloat16_rn(t0v), h1 = __float2bfloat16_rn(t1v);
+      const __nv_bfloat16 h0 = __float2bfloat16_rn(ta), h1 = __float2bfloat16_rn(tb);
       Ts[m * (p.r / 2) + jj / 2] = pack_bf16x2(__bfloat162float(h0), __bfloat162float(h1));
-      Ts[Mpad * (p.r / 2) + m * (p.r / 2) + jj / 2] =
-          pack_bf16x2(t0v - __bfloat162float(h0), t1v - __bfloat162float(h1));
+      Ts[Mpad * (p.r / 2) + m * (p.r / 2) + jj / 2] = pack_bf16x2(ta - __bfloat162float(h0), tb - __bfloat162float(h1));
     }
+    __syncthreads();
   }
-  __syncthreads();
 
-  // ---- epilogue: y = acc (* per-channel scale) + B T, one (segment, token tile) per warp
-  for (int item = warp; item < nseg * MT; item += kWarps) {
-    const int seg = item / MT, t = item % MT;
-    if (!s_fixup[seg]) continue;
-    const int tile = tile0 + seg;
-    const int n_lo = tile * 16 + g, n_hi = n_lo + 8;
+  // 5. epilogue: y = acc (* per-channel scale) + B T, one (tile, token tile) per warp
+  for (int item = warp; item < ntl * MT; item += kWarps) {
+    const int tl = item / MT, t = item % MT;
+    const int n_lo = (t0 + tl) * 16 + g, n_hi = n_lo + 8;
     float v[4];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) v[i] = ybuf[(seg * MT + t) * 128 + i * 32 + lane];
+    for (int i = 0; i < 4; ++i) v[i] = ybuf[(tl * MT + t) * 128 + i * 32 + lane];
     if (PERCH) {
-      const float slo = __half2float(sc_s[seg * 16 * p.ng + g * p.ng]);
-      const float shi = __half2float(sc_s[seg * 16 * p.ng + (g + 8) * p.ng]);
+      const float slo = __half2float(sc_s[tl * 16 * p.ng + g * p.ng]);
+      const float shi = __half2float(sc_s[tl * 16 * p.ng + (g + 8) * p.ng]);
       v[0] *= slo; v[1] *= slo; v[2] *= shi; v[3] *= shi;
     }
     if (COMP) {
@@ -489,9 +488,9 @@ __device__ void streamer_block(const DecodeParams& p, float* smem) {
         const uint32_t a0 = __ldg(Blo + c), a1 = __ldg(Bhi + c), a2 = __ldg(Blo + c + 4), a3 = __ldg(Bhi + c + 4);
         const int tok = t * 8 + g;
         const uint32_t* th = Ts + tok * rh + j0 / 2;
-        const uint32_t* tl = Ts + Mpad * rh + tok * rh + j0 / 2;
+        const uint32_t* tlo = Ts + Mpad * rh + tok * rh + j0 / 2;
         mma_bf16_16816(v, a0, a1, a2, a3, th[c], th[c + 4]);
-        mma_bf16_16816(v, a0, a1, a2, a3, tl[c], tl[c + 4]);
+        mma_bf16_16816(v, a0, a1, a2, a3, tlo[c], tlo[c + 4]);
       }
     }
 #pragma unroll
@@ -517,7 +516,7 @@ __device__ void streamer_block(const DecodeParams& p, float* smem) {
   }
 }
 
-template <int MT, bool COMP, bool PERCH>
+template <int MT, bool COMP, bool PERCH, bool XS>
 __global__ void __launch_bounds__(kThreads, (MT <= 2 ? 2 : 1)) decode_kernel(const DecodeParams p) {
   extern __shared__ __align__(16) float smem[];
   if ((int)blockIdx.x < p.Q) {
@@ -525,43 +524,47 @@ __global__ void __launch_bounds__(kThreads, (MT <= 2 ? 2 : 1)) decode_kernel(con
     // producer blocks idle), so forcing the gate to zero reproduces it bit for bit.
     if (COMP) producer_block<MT>(p, smem);
   } else {
-    streamer_block<MT, COMP, PERCH>(p, smem);
+    streamer_block<MT, COMP, PERCH, XS>(p, smem);
   }
 }
 
 using KernelFn = void (*)(const DecodeParams);
 
-template <int MT>
+template <int MT, bool XS>
 KernelFn pick_kernel(bool comp, bool perch) {
-  if (comp) return perch ? decode_kernel<MT, true, true> : decode_kernel<MT, true, false>;
-  return perch ? decode_kernel<MT, false, true> : decode_kernel<MT, false, false>;
+  if (comp) return perch ? decode_kernel<MT, true, true, XS> : decode_kernel<MT, true, false, XS>;
+  return perch ? decode_kernel<MT, false, true, XS> : decode_kernel<MT, false, false, XS>;
 }
 
-KernelFn pick(int MT, bool comp, bool perch) {
+KernelFn pick(int MT, bool comp, bool perch, bool xs) {
   switch (MT) {
-    case 1: return pick_kernel<1>(comp, perch);
-    case 2: return pick_kernel<2>(comp, perch);
-    case 4: return pick_kernel<4>(comp, perch);
-    default: return pick_kernel<8>(comp, perch);
+    case 1: return xs ? pick_kernel<1, true>(comp, perch) : pick_kernel<1, false>(comp, perch);
+    case 2: return pick_kernel<2, false>(comp, perch);
+    case 4: return pick_kernel<4, false>(comp, perch);
+    default: return pick_kernel<8, false>(comp, perch);
   }
 }
 
 int mt_for(int M) { return M <= 8 ? 1 : M <= 16 ? 2 : M <= 32 ? 4 : 8; }
 
-// Host-side plan: block counts, the stream-K split and the workspace layout.
+// Host-side plan: block counts, the tile split and the workspace layout.
 struct Plan {
-  int device, N, K, G, rank, comp, MT;      // key
-  int Q, P, tiles, nchunks, max_tiles, max_parts, ng, Rpad;
-  long long units;
+  int device, N, K, G, rank, comp, MT, M;   // key (M matters only for the staged-token variant)
+  int xs;                                   // tokens staged in shared memory (M <= 8)
+  int Q, P, tiles, nchunks, max_tiles, ng;
   size_t smem;
-  size_t off_prod, off_T, off_part, off_cnt, off_sync, total;
+  size_t off_prod, off_T, off_sync, total;
   KernelFn fn;
 };
 
 size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
 
-size_t streamer_smem(int MT, bool comp, int max_tiles, int ng) {
-  size_t s = (size_t)kWarps * kStages * 2 * 32 * 16;         // ring
+size_t xs_smem(int M, int K) {
+  return 16 + (size_t)M * (K / 8 + 1) * 16 + 2 * (size_t)M * (K / kChunkK) * 4;
+}
+
+size_t streamer_smem(int MT, bool comp, int max_tiles, int ng, size_t extra = 0) {
+  size_t s = extra + (size_t)kWarps * kStages * 2 * 32 * 16; // ring (+ staged tokens)
   s += (size_t)kWarps * MT * 128 * 4;                        // red
   s += (size_t)max_tiles * MT * 128 * 4;                     // ybuf
   if (comp) s += (size_t)MT * 8 * kMaxRank * 4;              // T hi/lo
@@ -569,20 +572,20 @@ size_t streamer_smem(int MT, bool comp, int max_tiles, int ng) {
   return s;
 }
 
-int build_plan(const spear_w4_layer& L, int MT, bool comp, const DeviceInfo& di, Plan* pl) {
+int build_plan(const spear_w4_layer& L, int MT, int M, bool comp, bool try_xs, const DeviceInfo& di, Plan* pl) {
   const bool has_rank = L.rank > 0;          // the split depends on this, not on comp_enabled
   pl->MT = MT;
   pl->tiles = L.N / 16;
   pl->nchunks = L.K / kChunkK;
   pl->ng = L.K / L.group_size;
-  pl->units = (long long)pl->tiles * pl->nchunks;
-  pl->Rpad = ((L.rank + 1 + 15) / 16) * 16;
   const bool perch = L.group_size == L.K;
-  pl->fn = pick(pl->MT, comp, perch);
+  pl->xs = (MT == 1 && try_xs) ? 1 : 0;
+  pl->fn = pick(pl->MT, comp, perch, pl->xs != 0);
+  const size_t extra = pl->xs ? xs_smem(M, L.K) : 0;
 
   // The block count depends on occupancy, which depends on shared memory,
-  // which depends on how many tiles one block touches: iterate to a fixed
-  // point, then validate occupancy at the final size.
+  // which depends on how many tiles one block owns: iterate to a fixed point,
+  // then validate occupancy at the final size.
   int blocks = 2 * di.num_sms;
   bool settled = false;
   for (int iter = 0; iter < 8 && !settled; ++iter) {
@@ -595,12 +598,11 @@ int build_plan(const spear_w4_layer& L, int MT, bool comp, const DeviceInfo& di,
     } else {
       pl->Q = 0;
     }
-    pl->P = (int)std::max<long long>(1, std::min<long long>(blocks - pl->Q, pl->units));
-    const long long per = std::max<long long>(1, pl->units / pl->P);   // floor of units per streamer
-    pl->max_tiles = (int)std::min<long long>((per + pl->nchunks - 1) / pl->nchunks + 2, pl->tiles);
-    pl->max_parts = (int)std::min<long long>((pl->nchunks + per - 1) / per + 1, pl->P);
+    pl->P = std::max(1, std::min(blocks - pl->Q, pl->tiles));
+    pl->max_tiles = (pl->tiles + pl->P - 1) / pl->P;
     if (pl->max_tiles > 64) return fail(SPEAR_ERR_UNSUPPORTED, "decode: too many tiles per block");
-    pl->smem = std::max(streamer_smem(pl->MT, has_rank, pl->max_tiles, pl->ng), (size_t)kWarps * pl->MT * 128 * 4);
+    pl->smem = std::max(streamer_smem(pl->MT, has_rank, pl->max_tiles, pl->ng, extra),
+                        (size_t)kWarps * pl->MT * 128 * 4);
     if (pl->smem > di.smem_optin)
       return fail(SPEAR_ERR_UNSUPPORTED, "decode: shape needs %zu B of shared memory", pl->smem);
     if (cudaFuncSetAttribute(pl->fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pl->smem) != cudaSuccess)
@@ -618,10 +620,8 @@ int build_plan(const spear_w4_layer& L, int MT, bool comp, const DeviceInfo& di,
   const int Mpad = pl->MT * 8;
   size_t off = 0;
   pl->off_sync = off; off = align256(off + 4 * sizeof(unsigned));
-  pl->off_cnt = off;  off = align256(off + (size_t)pl->tiles * sizeof(unsigned));
   pl->off_prod = off; off = align256(off + (size_t)std::max(pl->Q, 1) * Mpad * 16 * 4);
   pl->off_T = off;    off = align256(off + (size_t)Mpad * std::max(L.rank, 1) * 4);
-  pl->off_part = off; off = align256(off + (size_t)pl->tiles * pl->max_parts * pl->MT * 128 * 4);
   pl->total = off;
   return SPEAR_OK;
 }
@@ -638,13 +638,17 @@ int get_plan(const spear_w4_layer& L, int M, Plan* out) {
   std::lock_guard<std::mutex> lk(mu);
   for (const Plan& p : cache)
     if (p.device == di.device && p.N == L.N && p.K == L.K && p.G == L.group_size && p.rank == L.rank &&
-        p.comp == comp && p.MT == MT) {
+        p.comp == comp && p.MT == MT && (MT > 1 || p.M == M)) {
       *out = p;
       return SPEAR_OK;
     }
   Plan p{};
-  if (int rc = build_plan(L, MT, comp != 0, di, &p)) return rc;
-  p.device = di.device; p.N = L.N; p.K = L.K; p.G = L.group_size; p.rank = L.rank; p.comp = comp;
+  // staged tokens when they fit (M <= 8), else tokens from L1
+  if (build_plan(L, MT, M, comp != 0, MT == 1, di, &p) != SPEAR_OK) {
+    if (MT != 1) return SPEAR_ERR_UNSUPPORTED;
+    if (int rc = build_plan(L, MT, M, comp != 0, false, di, &p)) return rc;
+  }
+  p.device = di.device; p.N = L.N; p.K = L.K; p.G = L.group_size; p.rank = L.rank; p.comp = comp; p.M = M;
   if (cache.size() > 4096) cache.clear();
   cache.push_back(p);
   *out = p;
@@ -680,14 +684,12 @@ int launch_decode(const spear_w4_layer& L, const uint16_t* x, int M, void* y, in
   p.B = reinterpret_cast<const __nv_bfloat16*>(L.B);
   p.w_g = reinterpret_cast<const __nv_bfloat16*>(L.w_g);
   p.b_g = L.b_g; p.alpha = L.alpha;
-  p.Q = pl.Q; p.P = pl.P; p.tiles = pl.tiles; p.nchunks = pl.nchunks; p.units = pl.units;
-  p.max_tiles = pl.max_tiles; p.max_parts = pl.max_parts; p.ng = pl.ng;
+  p.Q = pl.Q; p.P = pl.P; p.tiles = pl.tiles; p.nchunks = pl.nchunks;
+  p.max_tiles = pl.max_tiles; p.ng = pl.ng;
   char* base = reinterpret_cast<char*>(ws);
   p.ws_sync = reinterpret_cast<unsigned*>(base + pl.off_sync);
-  p.ws_tile_cnt = reinterpret_cast<unsigned*>(base + pl.off_cnt);
   p.ws_prod = reinterpret_cast<float*>(base + pl.off_prod);
   p.ws_T = reinterpret_cast<float*>(base + pl.off_T);
-  p.ws_part = reinterpret_cast<float*>(base + pl.off_part);
 
   // Plans of other shapes may have changed this kernel's shared-memory limit
   // since this plan's grid was validated: restore the validated setting.
