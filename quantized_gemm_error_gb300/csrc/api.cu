@@ -4,6 +4,7 @@
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 #include <numeric>
@@ -58,6 +59,14 @@ int fail(int status, const char* fmt, ...) {
 int cuda_check(cudaError_t e, const char* what) {
   if (e == cudaSuccess) return SPEAR_OK;
   return fail(SPEAR_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+bool log_plans() {
+  static const bool on = [] {
+    const char* v = std::getenv("SPEAR_LOG_PLANS");
+    return v && v[0] && std::strcmp(v, "0") != 0;
+  }();
+  return on;
 }
 
 int device_info(DeviceInfo* out) {
@@ -221,7 +230,10 @@ spear_status spear_get_device_status(int* out, void* stream) {
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   unsigned s_pack = 0, s_dec = 0, s_pre = 0;
   if (int rc = read_and_clear_status_pack(&s_pack, st)) return rc;
+  unsigned s_dtc = 0;
   if (int rc = read_and_clear_status_decode(&s_dec, st)) return rc;
+  if (int rc = read_and_clear_status_decode_tc(&s_dtc, st)) return rc;
+  if (!s_dec) s_dec = s_dtc;
   if (int rc = read_and_clear_status_prefill(&s_pre, st)) return rc;
   if (int rc = cuda_check(cudaStreamSynchronize(st), "status sync")) return rc;
   *out = (int)(s_pack ? s_pack : s_dec ? s_dec : s_pre);

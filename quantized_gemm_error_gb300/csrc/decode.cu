@@ -29,6 +29,7 @@
 // HBM traffic per call: N K / 2 (codes) + N K/G * 2 (scales) + zeros + (r+1) K 2
 // (A, w_g) + N r 2 (B) + M K 2 (x) + M N 2 (y): the roofline of this kernel.
 #include <algorithm>
+#include <cstdio>
 #include <mutex>
 #include <vector>
 
@@ -649,6 +650,9 @@ int get_plan(const spear_w4_layer& L, int M, Plan* out) {
     if (int rc = build_plan(L, MT, M, comp != 0, false, di, &p)) return rc;
   }
   p.device = di.device; p.N = L.N; p.K = L.K; p.G = L.group_size; p.rank = L.rank; p.comp = comp; p.M = M;
+  if (log_plans())
+    fprintf(stderr, "[spear] decode plan N=%d K=%d G=%d rank=%d comp=%d M=%d: MT=%d xs=%d Q=%d P=%d max_tiles=%d "
+            "smem=%zu\n", L.N, L.K, L.group_size, L.rank, comp, M, p.MT, p.xs, p.Q, p.P, p.max_tiles, p.smem);
   if (cache.size() > 4096) cache.clear();
   cache.push_back(p);
   *out = p;
@@ -657,7 +661,17 @@ int get_plan(const spear_w4_layer& L, int M, Plan* out) {
 
 }  // namespace
 
+// Token counts from which the tensor-core kernel (decode_tc.cu) serves the
+// call: from there on its MMA throughput beats the warp-level MMAs below,
+// whose token fragments are reloaded for every 16 weight rows.
+#ifndef SPEAR_TC_MIN_M
+#define SPEAR_TC_MIN_M 33
+#endif
+constexpr int kTcMinM = SPEAR_TC_MIN_M;
+bool use_tc(int M) { return M >= kTcMinM; }
+
 int decode_workspace_bytes(const spear_w4_layer& L, int M, size_t* bytes) {
+  if (use_tc(M)) return decode_tc_workspace_bytes(L, M, bytes);
   Plan pl;
   if (int rc = get_plan(L, M, &pl)) return rc;
   *bytes = pl.total;
@@ -666,6 +680,7 @@ int decode_workspace_bytes(const spear_w4_layer& L, int M, size_t* bytes) {
 
 int launch_decode(const spear_w4_layer& L, const uint16_t* x, int M, void* y, int out_f32, void* ws,
                   size_t ws_bytes, cudaStream_t st) {
+  if (use_tc(M)) return launch_decode_tc(L, x, M, y, out_f32, ws, ws_bytes, st);
   Plan pl;
   if (int rc = get_plan(L, M, &pl)) return rc;
   if (!ws || ws_bytes < pl.total)
@@ -744,16 +759,24 @@ int noalloc_scratch(void** out) {
 
 int launch_decode_noalloc(const spear_w4_layer& L, const uint16_t* x, int M, void* y, int out_f32,
                           cudaStream_t st) {
-  Plan pl;
-  if (int rc = get_plan(L, M, &pl)) return rc;
-  if (pl.total > kNoallocScratchBytes)
+  size_t total = 0, sync_bytes = 0;
+  if (use_tc(M)) {
+    if (int rc = decode_tc_workspace_bytes(L, M, &total)) return rc;
+    sync_bytes = decode_tc_sync_bytes();
+  } else {
+    Plan pl;
+    if (int rc = get_plan(L, M, &pl)) return rc;
+    total = pl.total;
+    sync_bytes = pl.off_prod;
+  }
+  if (total > kNoallocScratchBytes)
     return fail(SPEAR_ERR_UNSUPPORTED,
                 "decode_noalloc: N=%d K=%d M=%d needs %zu B of scratch; the built-in scratch holds %zu B",
-                L.N, L.K, M, pl.total, kNoallocScratchBytes);
+                L.N, L.K, M, total, kNoallocScratchBytes);
   void* ws = nullptr;
   if (int rc = noalloc_scratch(&ws)) return rc;
-  // the synchronisation words and tile counters must start at zero
-  if (int rc = cuda_check(cudaMemsetAsync(ws, 0, pl.off_prod, st), "decode scratch clear")) return rc;
+  // the synchronisation words must start at zero
+  if (int rc = cuda_check(cudaMemsetAsync(ws, 0, sync_bytes, st), "decode scratch clear")) return rc;
   return launch_decode(L, x, M, y, out_f32, ws, kNoallocScratchBytes, st);
 }
 

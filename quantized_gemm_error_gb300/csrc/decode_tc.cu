@@ -1,0 +1,846 @@
+// decode_tc.cu -- decode path of the gated W4 + low-rank compensated linear on
+// the 5th-generation tensor cores, one launch per layer (SPEAR explainer,
+// Technical Summary 2.2 A: in the memory-bound decode phase the compensator
+// runs inside the low-bit GEMM's launch).  Serves the larger token counts
+// (33..64), where the per-weight arithmetic outgrows the warp-level MMAs of
+// decode.cu.
+//
+//   y[m][n] = sum_k (u[n][k] - z[n][g]) s[n][g] x[m][k]  +  sum_j B[n][j] T[m][j]
+//   T[m][j] = alpha g_m (A x_m)[j],   g_m = sigmoid(w_g . x_m + b_g)
+//
+// Work split.  The weight is cut into 256-row tiles; each tile belongs to one
+// thread-block cluster of S CTAs (one per SM) that split its K range in
+// 256-k units (rank j takes units j, j + S, ...), so a tile's partial sums
+// meet in distributed shared memory and never touch HBM.  Before the tile
+// clusters come RT x Kp small "producer" clusters that compute
+// P = [A; w_g] x (rank r + 1 rows) over K slices with mma.sync and publish it
+// through the workspace; the tile CTAs read it only in their epilogue.
+//
+// Tile CTA (704 threads):
+//   warp 20   TMA: raw int4 units (256 rows x 128 bytes, 128-byte swizzle) and
+//             token tiles x[0:NP][k:k+64] (bf16), each into its own ring;
+//   warps 4-19 turn each 64-k step of int4 codes into (u - z) s in fp16 (one
+//             rounding; the nibble enters as the mantissa of 1024 or 64, so
+//             the subtraction of 1024 + z or 64 + z is exact), written in the
+//             tensor core's swizzled K-major layout;
+//   warps 0-3 convert the token tile to fp16 (exact for |x| < 65504, larger
+//             values are reported), later drain the accumulator;
+//   warp 21   one thread issues tcgen05.mma with the tokens as the 64-row A
+//             operand and the weights as the 256-column B operand:
+//             D[64 x 256] (+)= X[64 x 16] W[256 x 16]^T, fp32 in tensor memory.
+// Epilogue: the S partials are summed in a fixed order through DSMEM, each CTA
+// of the cluster finishing 256 / S rows: + B T from the published P, then y.
+//
+// Shared memory carries every weight several times (int4 in, fp16 out, fp16
+// read by the tensor core: ~10 bytes per int4 byte), which bounds this kernel
+// near a quarter of what an SM draws from HBM; decode.cu's register path does
+// not have that cost and serves M <= 32.
+#include <cuda.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdio>
+#include <mutex>
+#include <vector>
+
+#include "common.cuh"
+#include "internal.h"
+#include "sm100_ptx.cuh"
+#include "tmap.h"
+
+namespace spear {
+namespace {
+
+__device__ unsigned g_dtc_status;
+
+using namespace sm100;
+
+constexpr int kTileRows = 256;                  // weight rows per tile CTA (MMA N)
+constexpr int kStepK = 64;                      // k per MMA step: one 128-byte row of fp16
+constexpr int kUnitK = 256;                     // k per raw int4 unit: 128 bytes per row
+constexpr int kRawBytes = kTileRows * kUnitK / 2;   // 32 KB
+constexpr int kBfBytes = kTileRows * kStepK * 2;    // 32 KB of fp16 weights per step
+constexpr int kX16Bytes = 64 * kStepK * 2;          // 8 KB: 64 token rows (MMA M = 64)
+constexpr int kRawStages = 2, kXrStages = 2, kX16Stages = 3, kMaxBfStages = 3;
+constexpr int kRedStride = kTileRows + 1;       // floats per token row of the partial
+constexpr int kXWarps = 4;                      // warps 0-3: token conversion, TMEM drain
+constexpr int kConvWarp0 = 4, kConvWarps = 16;  // warps 4-19: weight conversion (two threads per row)
+constexpr int kTmaWarp = 20, kMmaWarp = 21;
+constexpr int kThreads = 704;
+constexpr int kMaxRank = 64;
+constexpr int kMaxS = 8;
+constexpr uint64_t kPipeWaitNs = 2000ull * 1000 * 1000;   // 2 s: far beyond any legitimate wait
+constexpr uint64_t kTWaitNs = 200ull * 1000 * 1000;       // 200 ms for the published P
+
+struct TcParams {
+  int N, K, M, ng, sym;
+  const uint8_t* qweight;
+  int S;                    // CTAs per cluster
+  int RT, Kp;               // producer clusters: RT row tiles x Kp K ranges (RT = 0: none)
+  int units;                // 256-k units of K
+  int bf_stages;             // fp16 weight steps in flight (2 or 3)
+  int r;                    // rank (0 when the compensator is off)
+  int n_consumers;          // tile CTAs (they read P)
+  const __half* scales;
+  const uint8_t* zeros;
+  const __nv_bfloat16* x;
+  void* y;
+  int out_f32;
+  const __nv_bfloat16* A;
+  const __nv_bfloat16* B;
+  const __nv_bfloat16* w_g;
+  float b_g, alpha;
+  float* ws_part;           // [Kp][RT][16][NP] producer-cluster partials
+  float* ws_P;              // [NP][r + 1]: (A x)[j] for j < r, w_g . x at j = r
+  unsigned* ws_sync;        // [0] producer row tiles published, [1] tile-CTA ticket, [2 + rt] Kp tickets
+  uint32_t off_bf, off_x16, off_xr, off_B;   // dynamic shared memory layout
+};
+
+__device__ __forceinline__ void give_up(int* abort_flag) {
+  record_status(&g_dtc_status, DEV_ERR_TIMEOUT);
+  atomicExch(abort_flag, 1);
+}
+
+// ------------------------------------------------------------- producers --
+// Producer cluster pc = (row tile rt, K range kp): CTA `rank` of it covers K
+// slice kp * S + rank of Kp * S (128-k chunks).  Lane (g, c) of a warp loads
+// 8 consecutive k of a projection row and of a token; both operands use the
+// same k permutation, so the mma.sync sums are the plain dot products.
+template <int NP>
+__device__ void tc_producer(const TcParams& p, uint8_t* smem, int pc, int rank) {
+  constexpr int MT = NP / 8;
+  constexpr int NW = kThreads / 32;
+  constexpr int U = MT <= 2 ? 2 : 1;                       // 32-k pieces per pass
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane >> 2, c = lane & 3;
+  const int rt = pc % p.RT, kp = pc / p.RT;
+  const int nsl = p.Kp * p.S, sl = kp * p.S + rank;
+  const int nch = p.K / 128;
+  const int c0 = (int)((long long)sl * nch / nsl), c1 = (int)((long long)(sl + 1) * nch / nsl);
+  const int npieces = (c1 - c0) * 4;
+  float* red = reinterpret_cast<float*>(smem);             // [NW][MT][4][32]
+  float* part = red + NW * MT * 128;                        // [16][NP]
+
+  auto row_ptr = [&](int i) -> const __nv_bfloat16* {
+    if (i < p.r) return p.A + (size_t)i * p.K;
+    if (i == p.r) return p.w_g;
+    return nullptr;
+  };
+  const __nv_bfloat16* wlo = row_ptr(rt * 16 + g);
+  const __nv_bfloat16* whi = row_ptr(rt * 16 + g + 8);
+  float acc[MT][4];
+#pragma unroll
+  for (int t = 0; t < MT; ++t)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) acc[t][i] = 0.0f;
+  for (int pc0 = warp; pc0 < npieces; pc0 += U * NW) {
+    uint4 va[U], vb[U], xv[U][MT];
+#pragma unroll
+    for (int h = 0; h < U; ++h) {
+      const int pcs = pc0 + h * NW;
+      const bool ok = pcs < npieces;
+      const int kb = c0 * 128 + pcs * 32 + 8 * c;
+      va[h] = (ok && wlo) ? ldg16(wlo + kb) : make_uint4(0, 0, 0, 0);
+      vb[h] = (ok && whi) ? ldg16(whi + kb) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+      for (int t = 0; t < MT; ++t) {
+        const int tok = t * 8 + g;
+        xv[h][t] = (ok && tok < p.M) ? ldg16(p.x + (size_t)tok * p.K + kb) : make_uint4(0, 0, 0, 0);
+      }
+    }
+#pragma unroll
+    for (int h = 0; h < U; ++h)
+#pragma unroll
+      for (int t = 0; t < MT; ++t) {
+        mma_bf16_16816(acc[t], va[h].x, vb[h].x, va[h].y, vb[h].y, xv[h][t].x, xv[h][t].y);
+        mma_bf16_16816(acc[t], va[h].z, vb[h].z, va[h].w, vb[h].w, xv[h][t].z, xv[h][t].w);
+      }
+  }
+  // fixed-order sum over the warps: this CTA's partial [16 rows][NP tokens]
+#pragma unroll
+  for (int t = 0; t < MT; ++t)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) red[((warp * MT + t) * 4 + i) * 32 + lane] = acc[t][i];
+  __syncthreads();
+  for (int e = threadIdx.x; e < MT * 128; e += kThreads) {
+    const int t = e / 128, i = (e / 32) & 3, ln = e & 31;
+    float v = 0.0f;
+    for (int w = 0; w < NW; ++w) v += red[((w * MT + t) * 4 + i) * 32 + ln];
+    // C fragment element i of lane ln: row (ln/4) + 8 (i/2), token t*8 + 2 (ln%4) + (i%2)
+    part[((ln >> 2) + 8 * (i >> 1)) * NP + t * 8 + 2 * (ln & 3) + (i & 1)] = v;
+  }
+  __syncthreads();
+  cluster_sync();                                          // every CTA's partial is in its shared memory
+
+  __shared__ unsigned s_last;
+  if (rank == 0) {
+    // sum the S partials in rank order
+    float* dst = p.Kp == 1 ? nullptr : p.ws_part + ((size_t)kp * p.RT + rt) * 16 * NP;
+    for (int e = threadIdx.x; e < 16 * NP; e += kThreads) {
+      const uint32_t la = smem_u32(part + e);
+      float v = 0.0f;
+      for (int q = 0; q < p.S; ++q) v += dsmem_ld_f32(dsmem_addr(la, (uint32_t)q));
+      if (dst) {
+        dst[e] = v;
+      } else {
+        const int row = e / NP, tok = e % NP, i = rt * 16 + row;
+        if (i <= p.r) p.ws_P[(size_t)tok * (p.r + 1) + i] = v;
+      }
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      __threadfence();
+      s_last = (p.Kp == 1) ? 1u : (atomicAdd(&p.ws_sync[2 + rt], 1u) == (unsigned)(p.Kp - 1));
+    }
+    __syncthreads();
+    if (s_last && p.Kp > 1) {
+      // the last of the Kp clusters of this row tile sums them in K order
+      __threadfence();
+      for (int e = threadIdx.x; e < 16 * NP; e += kThreads) {
+        float v = 0.0f;
+        for (int q = 0; q < p.Kp; ++q) v += __ldcg(p.ws_part + ((size_t)q * p.RT + rt) * 16 * NP + e);
+        const int row = e / NP, tok = e % NP, i = rt * 16 + row;
+        if (i <= p.r) p.ws_P[(size_t)tok * (p.r + 1) + i] = v;
+      }
+      __syncthreads();
+    }
+    if (s_last && threadIdx.x == 0) {
+      if (p.Kp > 1) p.ws_sync[2 + rt] = 0;                 // ticket ready for the next call
+      __threadfence();
+      atomicAdd(&p.ws_sync[0], 1u);                        // row tile rt of P is published
+    }
+  }
+  cluster_sync();                                          // peers keep their shared memory until read
+}
+
+// ---------------------------------------------------------- tile CTAs --
+// One CTA = 256 weight rows x its K units.  The tensor core sees the tokens
+// as the 64-row A operand (M = 64: accumulator row m lives in TMEM lane
+// (m mod 16) + 32 (m / 16)) and the weights as the 256-column B operand, so
+// one instruction covers 256 rows x 16 k of int4.  Within each 8-k chunk both
+// operands hold k in the order 0,4,1,5,2,6,3,7: the order in which the
+// converters take nibble pairs out of a 32-bit word; every 16-k MMA still
+// sums the same products.
+template <int NP, bool PERCH, bool COMP>
+__device__ void tc_tile(const CUtensorMap* tm_w, const CUtensorMap* tm_x, const TcParams& p, uint8_t* smem,
+                        int tile, int rank) {
+  __shared__ __align__(8) uint64_t raw_full[kRawStages], raw_empty[kRawStages];
+  __shared__ __align__(8) uint64_t xr_full[kXrStages], xr_empty[kXrStages];
+  __shared__ __align__(8) uint64_t x16_full[kX16Stages], x16_empty[kX16Stages];
+  __shared__ __align__(8) uint64_t bf_full[kMaxBfStages], bf_empty[kMaxBfStages];
+  __shared__ __align__(8) uint64_t acc_full;
+  __shared__ uint32_t s_tmem;
+  __shared__ int s_abort;
+  __shared__ int s_pok;
+  __shared__ float s_scale[kTileRows];                     // per-channel scales of the tile rows
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int S = p.S, BF = p.bf_stages;
+  const int n0 = tile * kTileRows;
+  // K units of this CTA: rank, rank + S, rank + 2S, ... (the cluster walks
+  // each row's bytes together); the last unit of K may hold only 128 k
+  const int nunits = (p.units - rank + S - 1) / S;
+  const bool half_tail = (p.K % kUnitK) != 0 && (p.units - 1) % S == rank;
+  const int nsteps = 4 * nunits - (half_tail ? 2 : 0);     // 64-k steps (even)
+  const int ngroups = nsteps / 2;                          // 128-k groups
+  auto unit_of = [&](int i) { return rank + i * S; };      // global unit of local unit i
+  const int e_r0 = rank * kTileRows / S, e_r1 = (rank + 1) * kTileRows / S;   // rows finished here
+  const int nr = e_r1 - e_r0;
+
+  uint8_t* raw_ring = smem;                                // [2][256 rows][128 B] int4
+  uint8_t* bf_ring = smem + p.off_bf;                      // [BF][256 rows][128 B] fp16 weights
+  uint8_t* x16_ring = smem + p.off_x16;                    // [3][64 tokens][128 B] fp16 tokens
+  uint8_t* xr_ring = smem + p.off_xr;                      // [2][NP tokens][128 B] bf16 tokens (TMA)
+  uint8_t* B_s = smem + p.off_B;                           // [nr][2r + 16 bytes]
+  // after the main loop: the partial [64 tokens][257] over the raw ring and
+  // the start of the weight ring, T and the gates further into the weight ring
+  float* red = reinterpret_cast<float*>(smem);
+  float* T_s = reinterpret_cast<float*>(bf_ring + kBfBytes);       // [NP][r]
+  float* gate_s = T_s + NP * kMaxRank;                              // [NP]
+  const int b_stride = 2 * p.r + 16;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kRawStages; ++i) {
+      mbar_init(smem_u32(&raw_full[i]), 1);
+      mbar_init(smem_u32(&raw_empty[i]), kConvWarps);
+    }
+    for (int i = 0; i < kXrStages; ++i) {
+      mbar_init(smem_u32(&xr_full[i]), 1);
+      mbar_init(smem_u32(&xr_empty[i]), kXWarps);
+    }
+    for (int i = 0; i < kX16Stages; ++i) {
+      mbar_init(smem_u32(&x16_full[i]), kXWarps);
+      mbar_init(smem_u32(&x16_empty[i]), 1);
+    }
+    for (int i = 0; i < kMaxBfStages; ++i) {
+      mbar_init(smem_u32(&bf_full[i]), kConvWarps);
+      mbar_init(smem_u32(&bf_empty[i]), 1);
+    }
+    mbar_init(smem_u32(&acc_full), 1);
+    s_abort = 0;
+    s_pok = 0;
+    fence_mbar_init();
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(smem_u32(&s_tmem), kTileRows);
+    tmem_relinquish();
+  }
+  if (warp < kXWarps) {
+    // token rows NP..63 of every fp16 token slot stay zero
+    if constexpr (NP < 64) {
+      constexpr int kPad = (64 - NP) * 8;                  // 16-byte chunks per slot
+      for (int i = threadIdx.x; i < kX16Stages * kPad; i += kXWarps * 32)
+        *reinterpret_cast<uint4*>(x16_ring + (i / kPad) * kX16Bytes + NP * 128 + (i % kPad) * 16) =
+            make_uint4(0, 0, 0, 0);
+    }
+    for (int r = threadIdx.x; r < kTileRows; r += kXWarps * 32)
+      s_scale[r] = (PERCH && n0 + r < p.N) ? __half2float(__ldg(p.scales + (size_t)(n0 + r) * p.ng)) : 1.0f;
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = s_tmem;
+
+  if (warp == kTmaWarp) {
+    // ------------------------------------------------------------- TMA
+    if (lane == 0) {
+      prefetch_tmap(tm_w);
+      prefetch_tmap(tm_x);
+      int ri = 0, xi = 0;
+      bool ok = true;
+      uint64_t t0 = globaltimer_ns();
+      uint32_t idle = 0;
+      while (ok && (ri < nunits || xi < nsteps)) {
+        bool prog = false;
+        if (ri < nunits) {
+          const int slot = ri % kRawStages;
+          if (mbar_test_wait(smem_u32(&raw_empty[slot]), ((ri / kRawStages) & 1) ^ 1)) {
+            const uint32_t full = smem_u32(&raw_full[slot]);
+            mbar_arrive_expect_tx(full, kRawBytes);
+            tma_load_2d(smem_u32(raw_ring + slot * kRawBytes), tm_w, unit_of(ri) * (kUnitK / 2), n0, full);
+            ++ri;
+            prog = true;
+          }
+        }
+        if (xi < nsteps) {
+          const int slot = xi % kXrStages;
+          if (mbar_test_wait(smem_u32(&xr_empty[slot]), ((xi / kXrStages) & 1) ^ 1)) {
+            const uint32_t full = smem_u32(&xr_full[slot]);
+            mbar_arrive_expect_tx(full, NP * 128);
+            tma_load_2d(smem_u32(xr_ring + slot * NP * 128), tm_x, unit_of(xi >> 2) * kUnitK + (xi & 3) * kStepK,
+                        0, full);
+            ++xi;
+            prog = true;
+          }
+        }
+        if (prog) {
+          idle = 0;
+        } else {
+          __nanosleep(64);                                 // leave the issue slots to the converters
+          if ((++idle & 63) == 0) {
+            if (idle == 64) t0 = globaltimer_ns();
+            else if (globaltimer_ns() - t0 > kPipeWaitNs || s_abort) ok = false;
+          }
+        }
+      }
+      if (!ok) {
+        give_up(&s_abort);
+        // never leave with copies in flight: wait (bounded) for every issued fill
+        for (int i = std::max(0, ri - kRawStages); i < ri; ++i)
+          mbar_wait(smem_u32(&raw_full[i % kRawStages]), (i / kRawStages) & 1, kPipeWaitNs);
+        for (int i = std::max(0, xi - kXrStages); i < xi; ++i)
+          mbar_wait(smem_u32(&xr_full[i % kXrStages]), (i / kXrStages) & 1, kPipeWaitNs);
+      }
+    }
+  } else if (warp == kMmaWarp) {
+    // ------------------------------------------------------------- MMA
+    if (lane == 0) {
+      const uint32_t idesc = idesc_f16_f32(64, kTileRows);
+      bool ok = true;
+      for (int s = 0; s < nsteps; ++s) {
+        ok = mbar_wait(smem_u32(&bf_full[s % BF]), (s / BF) & 1, kPipeWaitNs) &&
+             mbar_wait(smem_u32(&x16_full[s % kX16Stages]), (s / kX16Stages) & 1, kPipeWaitNs) && !s_abort;
+        if (!ok) {
+          give_up(&s_abort);
+          break;
+        }
+        tc_fence_after();
+        const uint32_t a0 = smem_u32(x16_ring + (s % kX16Stages) * kX16Bytes);
+        const uint32_t b0 = smem_u32(bf_ring + (s % BF) * kBfBytes);
+#pragma unroll
+        for (int kk = 0; kk < kStepK / 16; ++kk)
+          mma_bf16_ss(tmem, smem_desc(a0 + 32 * kk, 1024, LAYOUT_SW128), smem_desc(b0 + 32 * kk, 1024, LAYOUT_SW128),
+                      idesc, (s > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(smem_u32(&bf_empty[s % BF]));
+        mma_commit(smem_u32(&x16_empty[s % kX16Stages]));
+      }
+      if (ok) mma_commit(smem_u32(&acc_full));
+    }
+  } else if (warp >= kConvWarp0) {
+    // -------------------------------------- weight converters (16 warps)
+    const int cw = warp - kConvWarp0;
+    const int half = cw >> 3;
+    const int row = 32 * (cw & 7) + lane;                  // 0..255
+    const int n = n0 + row;
+    const bool row_ok = n < p.N;
+    const int zrow = (p.ng + 1) / 2;
+    auto gidx = [&](int gl) { return PERCH ? 0 : 2 * unit_of(gl >> 1) + (gl & 1); };
+    auto load_z = [&](int gl) -> uint32_t {
+      if (p.sym || !row_ok || gl >= ngroups) return 8u;
+      const int gi = gidx(gl);
+      const uint32_t b = __ldg(p.zeros + (size_t)n * zrow + gi / 2);
+      return (gi & 1) ? (b >> 4) : (b & 15u);
+    };
+    // fp16x2 of the group scale (per-channel: 1.0, the scale is applied in the epilogue)
+    auto load_s = [&](int gl) -> uint32_t {
+      if (PERCH) return 0x3C003C00u;
+      if (!row_ok || gl >= ngroups) return 0u;
+      return (uint32_t)__half_as_ushort(__ldg(p.scales + (size_t)n * p.ng + gidx(gl))) * 0x00010001u;
+    };
+    bool ok = true;
+    auto wait_all = [&](uint64_t* bar, uint32_t parity) {
+      ok = ok && mbar_wait(smem_u32(bar), parity, kPipeWaitNs) && !s_abort;
+      ok = __all_sync(0xffffffffu, ok);
+    };
+    // one 64-k step: this thread's 32 k of its row, as (u - z) * s in fp16
+    auto convert = [&](int s, uint32_t z, uint32_t s2) {
+      const int u = s >> 2, j = s & 3, slot = u % kRawStages;
+      if (j == 0) wait_all(&raw_full[slot], (u / kRawStages) & 1);
+      wait_all(&bf_empty[s % BF], ((s / BF) & 1) ^ 1);
+      if (ok) {
+        const uint4 rv = *reinterpret_cast<const uint4*>(raw_ring + slot * kRawBytes + row * 128 +
+                                                          (((2 * j + half) ^ (row & 7)) << 4));
+        uint8_t* brow = bf_ring + (s % BF) * kBfBytes + row * 128;
+        const uint32_t z_lo = f16x2_bias(z);                       // 1024 + z
+        const uint32_t z_hi = (0x5400u | (z << 4)) * 0x00010001u;  // 64 + z
+        const uint32_t words[4] = {rv.x, rv.y, rv.z, rv.w};
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+          const uint32_t a = words[w], b = words[w] >> 8;
+          // (k0,k4) and (k2,k6) as 1024 + u; (k1,k5) and (k3,k7) as 64 + u (the
+          // nibble left in place, one fp16 mantissa unit = 1/16 at 64)
+          uint32_t v0 = (a & 0x000F000Fu) | 0x64006400u, v1 = (a & 0x00F000F0u) | 0x54005400u;
+          uint32_t v2 = (b & 0x000F000Fu) | 0x64006400u, v3 = (b & 0x00F000F0u) | 0x54005400u;
+          v0 = f16x2_sub(v0, z_lo); v2 = f16x2_sub(v2, z_lo);     // exact u - z
+          v1 = f16x2_sub(v1, z_hi); v3 = f16x2_sub(v3, z_hi);
+          if (!PERCH) { v0 = f16x2_mul(v0, s2); v1 = f16x2_mul(v1, s2); v2 = f16x2_mul(v2, s2); v3 = f16x2_mul(v3, s2); }
+          *reinterpret_cast<uint4*>(brow + (((4 * half + w) ^ (row & 7)) << 4)) = make_uint4(v0, v1, v2, v3);
+        }
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(smem_u32(&bf_full[s % BF]));
+        if (j == 3 || s == nsteps - 1) mbar_arrive(smem_u32(&raw_empty[slot]));
+      }
+    };
+    // zero points and scales travel 4 groups ahead of their use in named
+    // registers (slot = group mod 4, never indexed at run time)
+    uint32_t z0 = load_z(0), z1 = load_z(1), z2 = load_z(2), z3 = load_z(3);
+    uint32_t c0 = load_s(0), c1 = load_s(1), c2 = load_s(2), c3 = load_s(3);
+    auto group = [&](int gl, uint32_t& zs, uint32_t& cs) {
+      convert(2 * gl, zs, cs);
+      convert(2 * gl + 1, zs, cs);
+      zs = load_z(gl + 4);
+      cs = load_s(gl + 4);
+    };
+    for (int gl0 = 0; gl0 < ngroups; gl0 += 4) {
+      if (gl0 + 0 < ngroups) group(gl0 + 0, z0, c0);
+      if (gl0 + 1 < ngroups) group(gl0 + 1, z1, c1);
+      if (gl0 + 2 < ngroups) group(gl0 + 2, z2, c2);
+      if (gl0 + 3 < ngroups) group(gl0 + 3, z3, c3);
+    }
+    // the factor-B rows of the rows finished here, for the epilogue
+    if (COMP) {
+      const int per = p.r / 8;                             // 16-byte pieces per row
+      for (int e = threadIdx.x - kConvWarp0 * 32; e < nr * per; e += kConvWarps * 32) {
+        const int rr = e / per, cc = e % per, nn = n0 + e_r0 + rr;
+        if (nn < p.N) cp_async16(B_s + rr * b_stride + cc * 16, p.B + (size_t)nn * p.r + cc * 8);
+      }
+      cp_async_commit();
+      cp_async_wait<0>();
+    }
+  } else {
+    // --------------------------- token converters + epilogue (warps 0-3)
+    const int tid = threadIdx.x;                           // 0..127
+    bool ok = true, bad = false;
+    for (int s = 0; s < nsteps; ++s) {
+      const int rs = s % kXrStages, xs = s % kX16Stages;
+      ok = ok && mbar_wait(smem_u32(&xr_full[rs]), (s / kXrStages) & 1, kPipeWaitNs) &&
+           mbar_wait(smem_u32(&x16_empty[xs]), ((s / kX16Stages) & 1) ^ 1, kPipeWaitNs) && !s_abort;
+      ok = __all_sync(0xffffffffu, ok);
+      if (ok) {
+        const uint8_t* src = xr_ring + rs * NP * 128;
+        uint8_t* dst = x16_ring + xs * kX16Bytes;
+#pragma unroll
+        for (int c = tid; c < NP * 8; c += kXWarps * 32) {
+          // 16-byte chunk c: token c / 8, k 8 (c % 8) .. +7; same swizzled place in both tiles
+          const int t = c >> 3, off = t * 128 + (((c & 7) ^ (t & 7)) << 4);
+          const uint4 v = *reinterpret_cast<const uint4*>(src + off);
+          const float x0 = bf16x2_lo(v.x), x1 = bf16x2_hi(v.x), x2 = bf16x2_lo(v.y), x3 = bf16x2_hi(v.y);
+          const float x4 = bf16x2_lo(v.z), x5 = bf16x2_hi(v.z), x6 = bf16x2_lo(v.w), x7 = bf16x2_hi(v.w);
+          const float m = fmaxf(fmaxf(fmaxf(fabsf(x0), fabsf(x1)), fmaxf(fabsf(x2), fabsf(x3))),
+                                fmaxf(fmaxf(fabsf(x4), fabsf(x5)), fmaxf(fabsf(x6), fabsf(x7))));
+          bad |= !(m < 65504.0f);
+          auto h2 = [](float lo, float hi) {
+            const __half2 h = __floats2half2_rn(lo, hi);
+            return *reinterpret_cast<const uint32_t*>(&h);
+          };
+          *reinterpret_cast<uint4*>(dst + off) = make_uint4(h2(x0, x4), h2(x1, x5), h2(x2, x6), h2(x3, x7));
+        }
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(smem_u32(&x16_full[xs]));
+        mbar_arrive(smem_u32(&xr_empty[rs]));
+      }
+    }
+    if (bad) record_status(&g_dtc_status, DEV_ERR_INVALID);
+
+    // accumulator [64 tokens][256 rows] -> this CTA's partial, token-major (row stride 257)
+    ok = ok && mbar_wait(smem_u32(&acc_full), 0, kPipeWaitNs) && !s_abort;
+    ok = __all_sync(0xffffffffu, ok);
+    if (ok) {
+      tc_fence_after();
+      const int t = 16 * warp + lane;                      // token of this lane (lanes 0-15)
+      const bool t_ok = lane < 16 && t < NP;
+#pragma unroll 1
+      for (int c0 = 0; c0 < kTileRows; c0 += 32) {
+        uint32_t v[32];
+        tmem_ld_32cols(tmem + ((uint32_t)(32 * warp) << 16) + c0, v);
+        tmem_ld_wait();
+        if (t_ok) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) red[t * kRedStride + c0 + i] = s_scale[c0 + i] * __uint_as_float(v[i]);
+        }
+      }
+    } else {
+      give_up(&s_abort);
+    }
+
+    if (COMP) {
+      // the published P: gate per token, then T = alpha g P
+      if (tid == 0) {
+        const uint64_t tw = globaltimer_ns();
+        int pok = 0;
+        for (unsigned i = 0;; ++i) {
+          if (ld_acquire_gpu(&p.ws_sync[0]) >= (unsigned)p.RT) { pok = 1; break; }
+          if ((i & 63) == 63 && globaltimer_ns() - tw > kTWaitNs) break;
+          __nanosleep(64);
+        }
+        if (!pok) record_status(&g_dtc_status, DEV_ERR_TIMEOUT);
+        s_pok = pok;
+      }
+      named_sync(1, kXWarps * 32);
+      const int rp = p.r + 1;
+      for (int t = tid; t < NP; t += kXWarps * 32) {
+        float gt = 0.0f;
+        if (s_pok && t < p.M) gt = p.alpha / (1.0f + expf(-(__ldcg(p.ws_P + (size_t)t * rp + p.r) + p.b_g)));
+        gate_s[t] = gt;
+      }
+      named_sync(1, kXWarps * 32);
+      for (int e = tid; e < NP * p.r; e += kXWarps * 32) {
+        const int t = e / p.r, jj = e % p.r;
+        T_s[e] = s_pok ? gate_s[t] * __ldcg(p.ws_P + (size_t)t * rp + jj) : 0.0f;
+      }
+      named_sync(1, kXWarps * 32);
+      if (tid == 0) {
+        const unsigned old = atomicAdd(&p.ws_sync[1], 1u);
+        if (old == (unsigned)(p.n_consumers - 1)) {        // every tile CTA has read P
+          p.ws_sync[1] = 0;
+          atomicExch(&p.ws_sync[0], 0u);
+        }
+      }
+    }
+  }
+
+  // ---------------------------------------------- epilogue (whole cluster)
+  cluster_sync();                                          // every partial is in place
+  if (warp < kTmaWarp && !s_abort) {
+    const int tid = threadIdx.x;
+    const uint32_t red_base = smem_u32(red);
+    for (int e = tid; e < nr * p.M; e += kTmaWarp * 32) {
+      const int rl = e % nr, t = e / nr;
+      const int rowt = e_r0 + rl, nn = n0 + rowt;
+      const uint32_t la = red_base + (uint32_t)(t * kRedStride + rowt) * 4u;
+      float v = 0.0f;
+      for (int qq = 0; qq < S; ++qq) v += dsmem_ld_f32(dsmem_addr(la, (uint32_t)qq));
+      if (COMP) {
+        const uint8_t* br = B_s + rl * b_stride;
+        const float* tr = T_s + t * p.r;
+        float bt = 0.0f;
+        for (int jj = 0; jj < p.r; jj += 8) {
+          const uint4 b8 = *reinterpret_cast<const uint4*>(br + jj * 2);
+          const uint32_t bw[4] = {b8.x, b8.y, b8.z, b8.w};
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            bt = fmaf(bf16x2_lo(bw[i]), tr[jj + 2 * i], bt);
+            bt = fmaf(bf16x2_hi(bw[i]), tr[jj + 2 * i + 1], bt);
+          }
+        }
+        v += bt;
+      }
+      if (nn < p.N) {
+        if (p.out_f32) reinterpret_cast<float*>(p.y)[(size_t)t * p.N + nn] = v;
+        else reinterpret_cast<__nv_bfloat16*>(p.y)[(size_t)t * p.N + nn] = __float2bfloat16_rn(v);
+      }
+    }
+  }
+  tc_fence_before();
+  cluster_sync();                                          // peers are done reading this CTA
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTileRows);
+  }
+}
+
+template <int NP, bool PERCH, bool COMP>
+__global__ void __launch_bounds__(kThreads, 1)
+decode_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_x,
+                 const TcParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int rank = (int)cluster_ctarank();
+  const int cid = (int)blockIdx.x / p.S;
+  const int npc = p.RT * p.Kp;
+  if (cid < npc) {
+    // producer clusters; with the compensator off they idle (the tile split
+    // stays the one of the compensated layer, so a zero gate reproduces the
+    // plain layer bit for bit)
+    if (COMP) tc_producer<NP>(p, smem, cid, rank);
+    return;
+  }
+  tc_tile<NP, PERCH, COMP>(&tm_w, &tm_x, p, smem, cid - npc, rank);
+}
+
+using TcKernel = void (*)(CUtensorMap, CUtensorMap, TcParams);
+
+template <int NP>
+TcKernel pick_np(bool perch, bool comp) {
+  if (perch) return comp ? decode_tc_kernel<NP, true, true> : decode_tc_kernel<NP, true, false>;
+  return comp ? decode_tc_kernel<NP, false, true> : decode_tc_kernel<NP, false, false>;
+}
+
+TcKernel pick_tc(int NP, bool perch, bool comp) {
+  switch (NP) {
+    case 16: return pick_np<16>(perch, comp);
+    case 32: return pick_np<32>(perch, comp);
+    default: return pick_np<64>(perch, comp);
+  }
+}
+
+int np_for(int M) { return M <= 16 ? 16 : M <= 32 ? 32 : 64; }
+
+// ---------------------------------------------------------------- plan --
+struct TcPlan {
+  int device, N, K, G, rank, comp, NP;     // key
+  int S, RT, Kp, tiles, units, BF;
+  size_t smem;
+  uint32_t off_bf, off_x16, off_xr, off_B;
+  size_t off_sync, off_part, off_P, total;
+  TcKernel fn;
+};
+
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+size_t tile_smem(int NP, int BF, int nr_max, int rank, TcPlan* c) {
+  size_t off = (size_t)kRawStages * kRawBytes;
+  c->off_bf = (uint32_t)off;
+  off += (size_t)BF * kBfBytes;
+  c->off_x16 = (uint32_t)off;
+  off += (size_t)kX16Stages * kX16Bytes;
+  c->off_xr = (uint32_t)off;
+  off += (size_t)kXrStages * NP * 128;
+  c->off_B = (uint32_t)off;
+  off += (size_t)nr_max * (2 * std::max(rank, 8) + 16);
+  return align_up(off, 1024) + 1024;            // + alignment slack of the dynamic base
+}
+
+int build_tc_plan(const spear_w4_layer& L, int NP, bool comp, const DeviceInfo& di, TcPlan* pl) {
+  const bool has_rank = L.rank > 0;             // the split depends on this, not on comp_enabled
+  const bool perch = L.group_size == L.K;
+  pl->NP = NP;
+  pl->tiles = (L.N + kTileRows - 1) / kTileRows;
+  pl->units = (L.K + kUnitK - 1) / kUnitK;
+  pl->RT = has_rank ? (L.rank + 1 + 15) / 16 : 0;
+  pl->fn = pick_tc(NP, perch, comp);
+
+  // Producer smem: [NW][MT][4][32] + [16][NP] floats
+  const size_t prod_smem = ((size_t)(kThreads / 32) * (NP / 8) * 128 + 16 * NP) * 4 + 1024;
+
+  int best_cost = INT32_MAX;
+  TcPlan best{};
+  bool found = false;
+  for (int S = 1; S <= std::min(kMaxS, pl->units); ++S) {
+    TcPlan c = *pl;
+    c.S = S;
+    const int units_per = (pl->units + S - 1) / S;      // most units one CTA takes
+    c.Kp = has_rank ? std::max(1, std::min(8, (int)std::ceil((double)L.K / (S * 512.0)))) : 1;
+    const int nr_max = (kTileRows + S - 1) / S;
+    // three fp16 weight steps in flight when they fit, else two
+    c.BF = kMaxBfStages;
+    size_t sm = tile_smem(NP, c.BF, nr_max, L.rank, &c);
+    if (sm > di.smem_optin) {
+      c.BF = 2;
+      sm = tile_smem(NP, c.BF, nr_max, L.rank, &c);
+    }
+    c.smem = std::max(sm, prod_smem);
+    if (c.smem > di.smem_optin) continue;
+    // all of the unified L1 / shared-memory array as shared memory (one CTA
+    // per SM holds up to ~220 KB of rings)
+    if (cudaFuncSetAttribute(c.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)c.smem) != cudaSuccess ||
+        cudaFuncSetAttribute(c.fn, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             (int)cudaSharedmemCarveoutMaxShared) != cudaSuccess)
+      return fail(SPEAR_ERR_CUDA, "decode: cudaFuncSetAttribute failed");
+    const int clusters = pl->tiles + c.RT * c.Kp;
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(clusters * S);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = c.smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = S;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int max_clusters = 0;
+    if (cudaOccupancyMaxActiveClusters(&max_clusters, c.fn, &cfg) != cudaSuccess) {
+      cudaGetLastError();
+      continue;
+    }
+    if (log_plans()) {
+      int per_sm = 0, smem_sm = 0, regs_sm = 0;
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, c.fn, kThreads, c.smem);
+      cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, di.device);
+      cudaDeviceGetAttribute(&regs_sm, cudaDevAttrMaxRegistersPerMultiprocessor, di.device);
+      cudaFuncAttributes fa{};
+      cudaFuncGetAttributes(&fa, c.fn);
+      fprintf(stderr, "[spear]   NP=%d S=%d: smem=%zu blocks/SM=%d max clusters=%d needed=%d | regs=%d static=%zu "
+              "local=%zu maxthr=%d carveout=%d | SM smem=%d regs=%d\n", NP, S, c.smem, per_sm, max_clusters,
+              clusters, fa.numRegs, fa.sharedSizeBytes, fa.localSizeBytes, fa.maxThreadsPerBlock,
+              fa.preferredShmemCarveout, smem_sm, regs_sm);
+    }
+    if (clusters > max_clusters) continue;       // every CTA must be resident at once
+    const int cost = units_per;
+    if (cost < best_cost) {
+      best_cost = cost;
+      best = c;
+      found = true;
+    }
+  }
+  if (!found) return fail(SPEAR_ERR_UNSUPPORTED, "decode: no resident cluster configuration for N=%d K=%d", L.N, L.K);
+  *pl = best;
+  // restore the chosen shared-memory limit (the search set others)
+  if (cudaFuncSetAttribute(pl->fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pl->smem) != cudaSuccess)
+    return fail(SPEAR_ERR_CUDA, "decode: cudaFuncSetAttribute failed");
+
+  size_t off = 0;
+  pl->off_sync = off; off = align_up(off + (2 + 8) * sizeof(unsigned), 256);
+  pl->off_part = off; off = align_up(off + (has_rank ? (size_t)pl->Kp * pl->RT * 16 * NP * 4 : 4), 256);
+  pl->off_P = off;    off = align_up(off + (size_t)NP * (std::max(L.rank, 1) + 1) * 4, 256);
+  pl->total = off;
+  return SPEAR_OK;
+}
+
+int get_tc_plan(const spear_w4_layer& L, int M, TcPlan* out) {
+  DeviceInfo di;
+  if (int rc = device_info(&di)) return rc;
+  const int NP = np_for(M);
+  const int comp = (L.comp_enabled && L.rank > 0) ? 1 : 0;
+  static std::mutex mu;
+  static std::vector<TcPlan> cache;
+  std::lock_guard<std::mutex> lk(mu);
+  for (const TcPlan& p : cache)
+    if (p.device == di.device && p.N == L.N && p.K == L.K && p.G == L.group_size && p.rank == L.rank &&
+        p.comp == comp && p.NP == NP) {
+      *out = p;
+      return SPEAR_OK;
+    }
+  TcPlan p{};
+  if (int rc = build_tc_plan(L, NP, comp != 0, di, &p)) return rc;
+  if (log_plans())
+    fprintf(stderr, "[spear] decode tc plan N=%d K=%d G=%d rank=%d comp=%d NP=%d: S=%d RT=%d Kp=%d tiles=%d "
+            "units=%d BF=%d smem=%zu grid=%d\n", L.N, L.K, L.group_size, L.rank, comp, NP, p.S, p.RT, p.Kp,
+            p.tiles, p.units, p.BF, p.smem, (p.tiles + p.RT * p.Kp) * p.S);
+  p.device = di.device; p.N = L.N; p.K = L.K; p.G = L.group_size; p.rank = L.rank; p.comp = comp;
+  if (cache.size() > 4096) cache.clear();
+  cache.push_back(p);
+  *out = p;
+  return SPEAR_OK;
+}
+
+}  // namespace
+
+int decode_tc_workspace_bytes(const spear_w4_layer& L, int M, size_t* bytes) {
+  TcPlan pl;
+  if (int rc = get_tc_plan(L, M, &pl)) return rc;
+  *bytes = pl.total;
+  return SPEAR_OK;
+}
+
+size_t decode_tc_sync_bytes() { return 256; }
+
+int launch_decode_tc(const spear_w4_layer& L, const uint16_t* x, int M, void* y, int out_f32, void* ws,
+                     size_t ws_bytes, cudaStream_t st) {
+  TcPlan pl;
+  if (int rc = get_tc_plan(L, M, &pl)) return rc;
+  if (!ws || ws_bytes < pl.total)
+    return fail(SPEAR_ERR_WORKSPACE, "decode: workspace of %zu B is smaller than the %zu B needed", ws_bytes, pl.total);
+  if ((reinterpret_cast<uintptr_t>(ws) & 255) != 0)
+    return fail(SPEAR_ERR_INVALID_ARG, "decode: workspace must be 256-byte aligned");
+  CUtensorMap tm_w, tm_x;
+  if (int rc = make_tmap(&tm_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, L.qweight, L.K / 2, L.N, kUnitK / 2, kTileRows,
+                         CU_TENSOR_MAP_SWIZZLE_128B)) return rc;
+  if (int rc = make_tmap(&tm_x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, x, L.K, M, kStepK, pl.NP,
+                         CU_TENSOR_MAP_SWIZZLE_128B)) return rc;
+  TcParams p{};
+  p.N = L.N; p.K = L.K; p.M = M; p.ng = L.K / L.group_size; p.sym = L.symmetric;
+  p.qweight = L.qweight;
+  p.S = pl.S; p.RT = pl.RT; p.Kp = pl.Kp; p.units = pl.units; p.bf_stages = pl.BF;
+  p.r = pl.comp ? L.rank : 0;
+  p.n_consumers = pl.tiles * pl.S;
+  p.scales = reinterpret_cast<const __half*>(L.scales);
+  p.zeros = L.zeros;
+  p.x = reinterpret_cast<const __nv_bfloat16*>(x);
+  p.y = y; p.out_f32 = out_f32;
+  p.A = reinterpret_cast<const __nv_bfloat16*>(L.A);
+  p.B = reinterpret_cast<const __nv_bfloat16*>(L.B);
+  p.w_g = reinterpret_cast<const __nv_bfloat16*>(L.w_g);
+  p.b_g = L.b_g; p.alpha = L.alpha;
+  char* base = reinterpret_cast<char*>(ws);
+  p.ws_sync = reinterpret_cast<unsigned*>(base + pl.off_sync);
+  p.ws_part = reinterpret_cast<float*>(base + pl.off_part);
+  p.ws_P = reinterpret_cast<float*>(base + pl.off_P);
+  p.off_bf = pl.off_bf; p.off_x16 = pl.off_x16; p.off_xr = pl.off_xr; p.off_B = pl.off_B;
+
+  // other plans may have changed this kernel's shared-memory limit since this
+  // plan was validated: restore it
+  if (int rc = cuda_check(cudaFuncSetAttribute(pl.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pl.smem),
+                          "decode: smem attribute")) return rc;
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3((pl.tiles + pl.RT * pl.Kp) * pl.S);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = pl.smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = pl.S;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cuda_check(cudaLaunchKernelEx(&cfg, pl.fn, tm_w, tm_x, p), "decode launch");
+}
+
+int read_and_clear_status_decode_tc(unsigned* out, cudaStream_t st) {
+  void* addr = nullptr;
+  if (int rc = cuda_check(cudaGetSymbolAddress(&addr, g_dtc_status), "decode status address")) return rc;
+  if (int rc = cuda_check(cudaMemcpyAsync(out, addr, sizeof(unsigned), cudaMemcpyDeviceToHost, st),
+                          "read decode status")) return rc;
+  if (int rc = cuda_check(cudaStreamSynchronize(st), "read decode status")) return rc;
+  return cuda_check(cudaMemsetAsync(addr, 0, sizeof(unsigned), st), "clear decode status");
+}
+
+}  // namespace spear

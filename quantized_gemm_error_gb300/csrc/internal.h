@@ -24,6 +24,10 @@ struct DeviceInfo {
 };
 int device_info(DeviceInfo* out);
 
+// True when the environment variable SPEAR_LOG_PLANS is set to a non-empty
+// value other than "0": launch plans are then printed to stderr once each.
+bool log_plans();
+
 // ---- pack.cu
 int launch_pack_w4(const float* W, int N, int K, int G, int sym, uint8_t* qweight,
                    uint16_t* scales, uint8_t* zeros, cudaStream_t st);
@@ -36,6 +40,13 @@ int launch_decode(const spear_w4_layer& L, const uint16_t* x, int M, void* y, in
 int launch_decode_noalloc(const spear_w4_layer& L, const uint16_t* x, int M, void* y, int out_f32,
                           cudaStream_t st);
 int read_and_clear_status_decode(unsigned* out, cudaStream_t st);
+
+// ---- decode_tc.cu (tensor-core decode path)
+int decode_tc_workspace_bytes(const spear_w4_layer& L, int M, size_t* bytes);
+size_t decode_tc_sync_bytes();
+int launch_decode_tc(const spear_w4_layer& L, const uint16_t* x, int M, void* y, int out_f32, void* ws,
+                     size_t ws_bytes, cudaStream_t st);
+int read_and_clear_status_decode_tc(unsigned* out, cudaStream_t st);
 
 // ---- prefill.cu
 int prefill_workspace_bytes(const spear_w4_layer& L, int M, int mode, size_t* bytes);
