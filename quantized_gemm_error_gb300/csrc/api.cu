@@ -69,6 +69,27 @@ bool log_plans() {
   return on;
 }
 
+int ensure_smem_limit(const void* fn, size_t bytes) {
+  struct Entry { int device; const void* fn; size_t bytes; };
+  static std::mutex mu;
+  static std::vector<Entry> limits;
+  int dev = 0;
+  if (int rc = cuda_check(cudaGetDevice(&dev), "cudaGetDevice")) return rc;
+  std::lock_guard<std::mutex> lk(mu);
+  for (Entry& e : limits)
+    if (e.device == dev && e.fn == fn) {
+      if (bytes <= e.bytes) return SPEAR_OK;
+      if (int rc = cuda_check(cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes),
+                              "shared-memory limit")) return rc;
+      e.bytes = bytes;
+      return SPEAR_OK;
+    }
+  if (int rc = cuda_check(cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes),
+                          "shared-memory limit")) return rc;
+  limits.push_back({dev, fn, bytes});
+  return SPEAR_OK;
+}
+
 int device_info(DeviceInfo* out) {
   static std::mutex mu;
   static std::vector<DeviceInfo> cache;

@@ -6,7 +6,8 @@
 //   y[m][n] = sum_k (u[n][k] - z[n][g]) s[n][g] x[m][k]  +  alpha g_m sum_j B[n][j] t_m[j]
 //   t_m = A x_m,  g_m = sigmoid(w_g . x_m + b_g)
 //
-// Design (one cooperative launch, every thread block resident):
+// Design (one launch; the plan keeps every block resident at once, and the
+// producers, which wait for nothing, have the lowest block indices):
 //  * Producer blocks (the first Q) compute the rank-(r+1) down-projection
 //    P = [A; w_g] x over disjoint K slices with bf16 mma.sync, write their
 //    slice partials to the workspace, and the last producer to arrive sums
@@ -606,8 +607,7 @@ int build_plan(const spear_w4_layer& L, int MT, int M, bool comp, bool try_xs, c
                         (size_t)kWarps * pl->MT * 128 * 4);
     if (pl->smem > di.smem_optin)
       return fail(SPEAR_ERR_UNSUPPORTED, "decode: shape needs %zu B of shared memory", pl->smem);
-    if (cudaFuncSetAttribute(pl->fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pl->smem) != cudaSuccess)
-      return fail(SPEAR_ERR_CUDA, "decode: cudaFuncSetAttribute failed");
+    if (int rc = ensure_smem_limit(reinterpret_cast<const void*>(pl->fn), pl->smem)) return rc;
     int per_sm = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, pl->fn, kThreads, pl->smem) != cudaSuccess ||
         per_sm < 1)
@@ -706,20 +706,12 @@ int launch_decode(const spear_w4_layer& L, const uint16_t* x, int M, void* y, in
   p.ws_prod = reinterpret_cast<float*>(base + pl.off_prod);
   p.ws_T = reinterpret_cast<float*>(base + pl.off_T);
 
-  // Plans of other shapes may have changed this kernel's shared-memory limit
-  // since this plan's grid was validated: restore the validated setting.
-  if (int rc = cuda_check(cudaFuncSetAttribute(pl.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pl.smem),
-                          "decode: smem attribute")) return rc;
+  if (int rc = ensure_smem_limit(reinterpret_cast<const void*>(pl.fn), pl.smem)) return rc;
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(pl.Q + pl.P);
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = pl.smem;
   cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeCooperative;        // every block resident: the T wait always ends
-  attr[0].val.cooperative = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
   return cuda_check(cudaLaunchKernelEx(&cfg, pl.fn, p), "decode launch");
 }
 

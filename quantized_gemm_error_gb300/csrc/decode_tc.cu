@@ -689,8 +689,8 @@ int build_tc_plan(const spear_w4_layer& L, int NP, bool comp, const DeviceInfo& 
     if (c.smem > di.smem_optin) continue;
     // all of the unified L1 / shared-memory array as shared memory (one CTA
     // per SM holds up to ~220 KB of rings)
-    if (cudaFuncSetAttribute(c.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)c.smem) != cudaSuccess ||
-        cudaFuncSetAttribute(c.fn, cudaFuncAttributePreferredSharedMemoryCarveout,
+    if (int rc = ensure_smem_limit(reinterpret_cast<const void*>(c.fn), c.smem)) return rc;
+    if (cudaFuncSetAttribute(c.fn, cudaFuncAttributePreferredSharedMemoryCarveout,
                              (int)cudaSharedmemCarveoutMaxShared) != cudaSuccess)
       return fail(SPEAR_ERR_CUDA, "decode: cudaFuncSetAttribute failed");
     const int clusters = pl->tiles + c.RT * c.Kp;
@@ -732,9 +732,6 @@ int build_tc_plan(const spear_w4_layer& L, int NP, bool comp, const DeviceInfo& 
   }
   if (!found) return fail(SPEAR_ERR_UNSUPPORTED, "decode: no resident cluster configuration for N=%d K=%d", L.N, L.K);
   *pl = best;
-  // restore the chosen shared-memory limit (the search set others)
-  if (cudaFuncSetAttribute(pl->fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pl->smem) != cudaSuccess)
-    return fail(SPEAR_ERR_CUDA, "decode: cudaFuncSetAttribute failed");
 
   size_t off = 0;
   pl->off_sync = off; off = align_up(off + (2 + 8) * sizeof(unsigned), 256);
@@ -815,10 +812,7 @@ int launch_decode_tc(const spear_w4_layer& L, const uint16_t* x, int M, void* y,
   p.ws_P = reinterpret_cast<float*>(base + pl.off_P);
   p.off_bf = pl.off_bf; p.off_x16 = pl.off_x16; p.off_xr = pl.off_xr; p.off_B = pl.off_B;
 
-  // other plans may have changed this kernel's shared-memory limit since this
-  // plan was validated: restore it
-  if (int rc = cuda_check(cudaFuncSetAttribute(pl.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pl.smem),
-                          "decode: smem attribute")) return rc;
+  if (int rc = ensure_smem_limit(reinterpret_cast<const void*>(pl.fn), pl.smem)) return rc;
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3((pl.tiles + pl.RT * pl.Kp) * pl.S);
   cfg.blockDim = dim3(kThreads);

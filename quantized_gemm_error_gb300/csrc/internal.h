@@ -28,6 +28,12 @@ int device_info(DeviceInfo* out);
 // value other than "0": launch plans are then printed to stderr once each.
 bool log_plans();
 
+// Raises (never lowers) the dynamic shared-memory limit of kernel `fn` on the
+// current device to at least `bytes`.  Launches captured in CUDA graphs keep
+// the size they were captured with, so a limit that a later plan lowered
+// would make an earlier graph fail; the limit therefore only grows.
+int ensure_smem_limit(const void* fn, size_t bytes);
+
 // ---- pack.cu
 int launch_pack_w4(const float* W, int N, int K, int G, int sym, uint8_t* qweight,
                    uint16_t* scales, uint8_t* zeros, cudaStream_t st);

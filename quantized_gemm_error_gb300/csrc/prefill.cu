@@ -17,7 +17,11 @@
 //        (11 significant bits: a bf16 operand's 8 bits are not enough when a
 //        few outlier channels dominate an output).
 //    The activations are bf16; their fp16 copy is exact for |x| < 65504 and
-//    is written by the pass that already reads X (comp_down) or by to_fp16.
+//    is written by the pass that already reads X (comp_down) or by to_fp16,
+//    with each 8-k chunk in the order 0,4,1,5,2,6,3,7 -- the order in which
+//    the converters take nibble pairs out of a 32-bit word -- so neither side
+//    permutes bytes.  Eight converter warps (one weight row per thread) keep
+//    the zero points and scales of the next four groups in flight.
 //    Optionally ("fused" mode) the K loop is extended by the compensator's
 //    up-projection: extra K steps with A = [T_hi | T_lo] (the gated
 //    down-projection split into two bf16 halves) and B = the factor B, into a
@@ -52,7 +56,7 @@ constexpr int kXBytes = kBM * kBK * 2;    // 16 KB
 constexpr int kWBytes = kBN * kBK * 2;    // 32 KB
 constexpr int kRawBytes = kBN * kBK / 2;  // 8 KB
 constexpr int kStageBytes = kXBytes + kWBytes + kRawBytes;
-constexpr int kGemmThreads = 192;         // warp 0: TMA, warp 1: MMA, warps 2-5: convert + epilogue
+constexpr int kGemmThreads = 320;         // warp 0: TMA, warp 1: MMA, warps 2-9: convert + epilogue
 constexpr uint32_t kTmemCols = 512;       // main accumulator in [0, 256), correction in [256, 512)
 constexpr uint64_t kWaitNs = 2000ull * 1000 * 1000;   // 2 s: far beyond any legitimate wait
 
@@ -94,7 +98,7 @@ w4_gemm_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(smem_u32(&bar_full[s]), 1);
-      mbar_init(smem_u32(&bar_cvt[s]), 4);
+      mbar_init(smem_u32(&bar_cvt[s]), 8);
       mbar_init(smem_u32(&bar_empty[s]), 1);
     }
     mbar_init(smem_u32(&bar_acc), 1);
@@ -189,66 +193,90 @@ w4_gemm_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
     }
   } else {
     // ------------------------------------------ converters, then the epilogue
-    const int ct = threadIdx.x - 64;                         // 0..127
+    // 8 warps: thread ct converts row ct of the 256-row weight tile each stage.
+    // Within each 8-k chunk the fp16 tile holds k in the order 0,4,1,5,2,6,3,7
+    // (nibble pairs as they sit in a 32-bit word); the fp16 token copy is
+    // written in the same order, so every 16-k MMA sums the same products.
+    const int ct = threadIdx.x - 64;                         // 0..255
+    const int n = n0 + ct;
+    const bool row_ok = n < p.N;
     const int zrow = (p.ng + 1) / 2;
+    const int stages_per_group = p.perch ? k_stages : p.G / kBK;
+    const int ngroups = (k_stages + stages_per_group - 1) / stages_per_group;
+    auto load_z = [&](int gi) -> uint32_t {
+      if (p.sym || !row_ok || gi >= ngroups) return 8u;
+      const uint32_t zb = __ldg(p.zeros + (size_t)n * zrow + gi / 2);
+      return (gi & 1) ? (zb >> 4) : (zb & 15u);
+    };
+    // fp16x2 of the group scale; per-channel: 1.0 (the scale is applied in the epilogue)
+    auto load_s = [&](int gi) -> uint32_t {
+      if (p.perch) return 0x3C003C00u;
+      if (!row_ok || gi >= ngroups) return 0u;
+      return (uint32_t)__half_as_ushort(__ldg(p.scales + (size_t)n * p.ng + gi)) * 0x00010001u;
+    };
     bool ok = true;
-    for (int s = 0; s < k_stages; ++s) {
+    auto convert = [&](int s, uint32_t z, uint32_t s2) {
       const int slot = s % kStages;
-      if (!mbar_wait(smem_u32(&bar_full[slot]), (s / kStages) & 1, kWaitNs) || s_abort) {
-        give_up();
-        ok = false;
-        break;
-      }
-      const int gi = (s * kBK) / p.G;
-      const uint8_t* raw = raw_slot(slot);
-      uint8_t* wdst = w_slot(slot);
+      ok = ok && mbar_wait(smem_u32(&bar_full[slot]), (s / kStages) & 1, kWaitNs) && !s_abort;
+      ok = __all_sync(0xffffffffu, ok);
+      if (ok) {
+        const uint8_t* raw = raw_slot(slot) + ct * 32;
+        uint8_t* wrow = w_slot(slot) + ct * 128;
+        const uint32_t z_lo = f16x2_bias(z);                       // 1024 + z
+        const uint32_t z_hi = (0x5400u | (z << 4)) * 0x00010001u;  // 64 + z
+        const uint4 r0 = *reinterpret_cast<const uint4*>(raw);
+        const uint4 r1 = *reinterpret_cast<const uint4*>(raw + 16);
+        const uint32_t words[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int row = ct + 128 * h;
-        const int n = n0 + row;
-        uint4 out[8];
-        if (n < p.N) {
-          int z = 8;
-          if (!p.sym) {
-            const uint8_t zb = p.zeros[(size_t)n * zrow + gi / 2];
-            z = (gi & 1) ? (zb >> 4) : (zb & 15);
+        for (int w = 0; w < 8; ++w) {
+          const uint32_t a = words[w], b = words[w] >> 8;
+          // (k0,k4), (k2,k6) as 1024 + u; (k1,k5), (k3,k7) as 64 + u (nibble in place,
+          // one fp16 mantissa unit = 1/16 at 64); subtracting 1024 + z / 64 + z is exact
+          uint32_t v0 = (a & 0x000F000Fu) | 0x64006400u, v1 = (a & 0x00F000F0u) | 0x54005400u;
+          uint32_t v2 = (b & 0x000F000Fu) | 0x64006400u, v3 = (b & 0x00F000F0u) | 0x54005400u;
+          v0 = f16x2_sub(v0, z_lo); v2 = f16x2_sub(v2, z_lo);
+          v1 = f16x2_sub(v1, z_hi); v3 = f16x2_sub(v3, z_hi);
+          if (!p.perch) {                                          // (u - z) s, one rounding
+            v0 = f16x2_mul(v0, s2); v1 = f16x2_mul(v1, s2); v2 = f16x2_mul(v2, s2); v3 = f16x2_mul(v3, s2);
           }
-          const uint32_t s2 = p.perch ? 0x3C003C00u     // fp16 1.0: the scale is applied in the epilogue
-                                      : (uint32_t)__half_as_ushort(p.scales[(size_t)n * p.ng + gi]) * 0x00010001u;
-          const uint32_t zb2 = f16x2_bias((uint32_t)z);
-          const uint4 r0 = *reinterpret_cast<const uint4*>(raw + row * 32);
-          const uint4 r1 = *reinterpret_cast<const uint4*>(raw + row * 32 + 16);
-          const uint32_t words[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
-#pragma unroll
-          for (int w = 0; w < 8; ++w) {
-            uint32_t v[4];
-            nibbles_to_f16x2_biased(words[w], v);            // (k_i, k_{i+4}) as 1024 + u
-#pragma unroll
-            for (int i = 0; i < 4; ++i) v[i] = f16x2_mul(f16x2_sub(v[i], zb2), s2);   // (u - z) s, one rounding
-            out[w] = make_uint4(__byte_perm(v[0], v[1], 0x5410), __byte_perm(v[2], v[3], 0x5410),
-                                __byte_perm(v[0], v[1], 0x7632), __byte_perm(v[2], v[3], 0x7632));
-          }
-        } else {
-#pragma unroll
-          for (int w = 0; w < 8; ++w) out[w] = make_uint4(0, 0, 0, 0);
+          // 128-byte swizzle: 16-byte chunk c of row r lives at chunk c ^ (r & 7)
+          *reinterpret_cast<uint4*>(wrow + ((w ^ (ct & 7)) << 4)) = make_uint4(v0, v1, v2, v3);
         }
-        // 128-byte swizzle: 16-byte chunk c of row r lives at chunk c ^ (r & 7)
-#pragma unroll
-        for (int w = 0; w < 8; ++w)
-          *reinterpret_cast<uint4*>(wdst + row * 128 + ((w ^ (row & 7)) << 4)) = out[w];
+      } else {
+        give_up();
       }
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&bar_cvt[slot]));
+    };
+    // zero points and scales travel 4 groups ahead of their use in named
+    // registers (slot = group mod 4, never indexed at run time)
+    uint32_t z0 = load_z(0), z1 = load_z(1), z2 = load_z(2), z3 = load_z(3);
+    uint32_t c0 = load_s(0), c1 = load_s(1), c2 = load_s(2), c3 = load_s(3);
+    auto group = [&](int gi, uint32_t& zs, uint32_t& cs) {
+      const int s0 = gi * stages_per_group, s1 = std::min(s0 + stages_per_group, k_stages);
+      for (int s = s0; s < s1; ++s) convert(s, zs, cs);
+      zs = load_z(gi + 4);
+      cs = load_s(gi + 4);
+    };
+    for (int g0 = 0; g0 < ngroups; g0 += 4) {
+      if (g0 + 0 < ngroups) group(g0 + 0, z0, c0);
+      if (g0 + 1 < ngroups) group(g0 + 1, z1, c1);
+      if (g0 + 2 < ngroups) group(g0 + 2, z2, c2);
+      if (g0 + 3 < ngroups) group(g0 + 3, z3, c3);
     }
 
-    // epilogue: TMEM lanes 32*(warp%4) .. +31 are this warp's rows (tokens)
-    if (ok && !mbar_wait(smem_u32(&bar_acc), 0, kWaitNs)) give_up();
+    // epilogue: TMEM lanes 32*(warp%4) .. +31 are this warp's rows (tokens);
+    // warps 2-5 take output columns [0, 128), warps 6-9 columns [128, 256)
+    ok = ok && mbar_wait(smem_u32(&bar_acc), 0, kWaitNs);
+    ok = __all_sync(0xffffffffu, ok);
+    if (!ok) give_up();
     tc_fence_after();
     if (!s_abort) {
       const int q = warp & 3;
       const int tok = m0 + 32 * q + lane;
-      for (int cch = 0; cch < kBN / 32; ++cch) {
+      const int c_begin = ((warp - 2) >> 2) * (kBN / 2);
+      for (int cch = c_begin / 32; cch < (c_begin + kBN / 2) / 32; ++cch) {
         uint32_t r[32], rc[32];
         tmem_ld_32cols(tmem + ((uint32_t)(32 * q) << 16) + cch * 32, r);
         if (p.comp_stages) tmem_ld_32cols(tmem + ((uint32_t)(32 * q) << 16) + kBN + cch * 32, rc);
@@ -321,18 +349,20 @@ struct CompDownParams {
   __half* x16;          // optional [M][K] fp16 copy of x for the GEMM (NULL: not written)
 };
 
-// 8 bf16 -> 8 fp16 (exact inside the fp16 range); flags values beyond it.
+// 8 consecutive bf16 (k0..k7) -> 8 fp16 in the GEMM's operand order within an
+// 8-k chunk: (k0,k4) (k1,k5) (k2,k6) (k3,k7).  Exact inside the fp16 range;
+// flags values beyond it.
 __device__ __forceinline__ uint4 bf16x8_to_f16x8(uint4 v, bool& out_of_range) {
-  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-  uint32_t o[4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const float lo = bf16x2_lo(w[i]), hi = bf16x2_hi(w[i]);
-    out_of_range |= !(fabsf(lo) < 65504.0f) || !(fabsf(hi) < 65504.0f);
+  const float x0 = bf16x2_lo(v.x), x1 = bf16x2_hi(v.x), x2 = bf16x2_lo(v.y), x3 = bf16x2_hi(v.y);
+  const float x4 = bf16x2_lo(v.z), x5 = bf16x2_hi(v.z), x6 = bf16x2_lo(v.w), x7 = bf16x2_hi(v.w);
+  const float m = fmaxf(fmaxf(fmaxf(fabsf(x0), fabsf(x1)), fmaxf(fabsf(x2), fabsf(x3))),
+                        fmaxf(fmaxf(fabsf(x4), fabsf(x5)), fmaxf(fabsf(x6), fabsf(x7))));
+  out_of_range |= !(m < 65504.0f);
+  auto h2 = [](float lo, float hi) {
     const __half2 h = __floats2half2_rn(lo, hi);
-    o[i] = *reinterpret_cast<const uint32_t*>(&h);
-  }
-  return make_uint4(o[0], o[1], o[2], o[3]);
+    return *reinterpret_cast<const uint32_t*>(&h);
+  };
+  return make_uint4(h2(x0, x4), h2(x1, x5), h2(x2, x6), h2(x3, x7));
 }
 
 template <int RT>
@@ -515,8 +545,7 @@ int launch_gemm(const spear_w4_layer& L, const __half* x16, int M, void* y, int 
     tm_b = tm_x;
   }
   const size_t smem = (size_t)kStages * kStageBytes + 1024;
-  if (int rc = cuda_check(cudaFuncSetAttribute(w4_gemm_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem),
-                          "prefill: smem attribute")) return rc;
+  if (int rc = ensure_smem_limit(reinterpret_cast<const void*>(w4_gemm_tc), smem)) return rc;
   dim3 grid((L.N + kBN - 1) / kBN, (M + kBM - 1) / kBM);
   if (grid.y > 65535) return fail(SPEAR_ERR_UNSUPPORTED, "prefill: M=%d too large", M);
   w4_gemm_tc<<<grid, kGemmThreads, smem, st>>>(tm_x, tm_wq, tm_t, tm_b, p);
