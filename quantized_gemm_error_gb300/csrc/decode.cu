@@ -218,10 +218,15 @@ __device__ void streamer_block(const DecodeParams& p, float* smem) {
   float* red = smem + kWarps * kStages * 2 * 32 * 4;                  // [kWarps][MT][4][32]
   float* ybuf = red + kWarps * MT * 4 * 32;                           // [max_tiles][MT][4][32]
   uint32_t* Ts = reinterpret_cast<uint32_t*>(ybuf + p.max_tiles * MT * 4 * 32);  // [Mpad][r/2] hi, then lo
-  __half* sc_s = reinterpret_cast<__half*>(Ts + (COMP ? Mpad * kMaxRank : 0));   // [max_tiles][16][ng]
-  uint8_t* z_s = reinterpret_cast<uint8_t*>(sc_s + p.max_tiles * 16 * p.ng);     // [max_tiles][16][ng]
-  uint4* xs = reinterpret_cast<uint4*>((reinterpret_cast<uintptr_t>(z_s + p.max_tiles * 16 * p.ng) + 15) &
-                                       ~uintptr_t(15));                           // [M][xrow] (XS)
+  // the block's rows of scales, zero-point bytes and factor B, as laid out
+  // in global memory (each a contiguous range: whole 16-row tiles)
+  __half* sc_s = reinterpret_cast<__half*>(Ts + (COMP ? Mpad * kMaxRank : 0));   // [max_tiles * 16][ng]
+  uint8_t* z_s = reinterpret_cast<uint8_t*>(sc_s + p.max_tiles * 16 * p.ng);     // [max_tiles * 16][zrow]
+  const int zrow = (p.ng + 1) / 2;
+  __nv_bfloat16* B_s = reinterpret_cast<__nv_bfloat16*>(
+      (reinterpret_cast<uintptr_t>(z_s + p.max_tiles * 16 * zrow) + 15) & ~uintptr_t(15));  // [max_tiles * 16][r]
+  uint4* xs = reinterpret_cast<uint4*>((reinterpret_cast<uintptr_t>(B_s + (COMP ? p.max_tiles * 16 * p.r : 0)) +
+                                        15) & ~uintptr_t(15));            // [M][xrow] (XS)
   float* Ps = reinterpret_cast<float*>(xs + (XS ? p.M * xrow : 0));  // [M][nchunks] 1024 E + 64 O (XS)
   float* Xs = Ps + (XS ? p.M * p.nchunks : 0);                       // [M][nchunks] E + O (XS)
   __shared__ int s_flag;
@@ -246,7 +251,10 @@ __device__ void streamer_block(const DecodeParams& p, float* smem) {
     cp_async_commit();
   };
 
-  // 1. tokens (XS) and scales first -- they gate the first MMA -- then the weight stream
+  // 1. tokens (XS) into registers (they come from L2); then, as one cp.async
+  // group ahead of the weight stream, the block's scales, zero points and
+  // factor-B rows, so the only wait before the main loop is for bytes that
+  // travel together with the first weights
   const int xunits = XS ? p.M * k8 : 0;
   constexpr int kXBatch = XS ? 4 : 1;
   uint4 xr[kXBatch];
@@ -257,37 +265,31 @@ __device__ void streamer_block(const DecodeParams& p, float* smem) {
       xr[j] = e < xunits ? ldg16(p.x + (size_t)e * 8) : make_uint4(0, 0, 0, 0);
     }
   }
-  const int total_sc = ntl * 16 * p.ng;
-  const int zrow = (p.ng + 1) / 2;
-  auto load_sc = [&](int e, __half& sv, uint8_t& zv) {
-    const int tl = e / (16 * p.ng), rem = e % (16 * p.ng), row = rem / p.ng, gi = rem % p.ng;
-    const int n = (t0 + tl) * 16 + row;
-    sv = p.scales[(size_t)n * p.ng + gi];
-    zv = 8;
-    if (!p.sym) {
-      const uint8_t zb = p.zeros[(size_t)n * zrow + gi / 2];
-      zv = (gi & 1) ? (zb >> 4) : (zb & 15);
+  {
+    auto stage = [&](void* dst, const void* src_base, size_t bytes) {
+      for (size_t e = threadIdx.x; e < bytes / 16; e += kThreads)
+        cp_async16(reinterpret_cast<uint4*>(dst) + e, reinterpret_cast<const uint4*>(src_base) + e);
+    };
+    const size_t row0 = (size_t)t0 * 16, rows = (size_t)ntl * 16;
+    stage(sc_s, p.scales + row0 * p.ng, rows * p.ng * 2);
+    if (!p.sym) stage(z_s, p.zeros + row0 * zrow, rows * zrow);
+    if (COMP) stage(B_s, p.B + row0 * p.r, rows * p.r * 2);
+    cp_async_commit();
+  }
+#pragma unroll
+  for (int st = 0; st < kStages - 1; ++st) issue(st);
+  if (!XS) {
+    // token rows of this warp's first two chunks into L1 (16 tokens x 256 B per chunk)
+    for (int jj = 0; jj < 2 && jj < per_tile; ++jj) {
+      const int ch = warp + kWarps * jj;
+      for (int q = lane; q < Mpad * 2; q += 32) {
+        const int tok = q >> 1;
+        if (tok < p.M) prefetch_l1(p.x + (size_t)tok * p.K + ch * kChunkK + (q & 1) * 64);
+      }
     }
-  };
-  __half sv[8];
-  uint8_t zv[8];
-#pragma unroll
-  for (int u = 0; u < 8; ++u) {
-    const int e = threadIdx.x + u * kThreads;
-    sv[u] = __ushort_as_half(0);
-    zv[u] = 8;
-    if (e < total_sc) load_sc(e, sv[u], zv[u]);
   }
-#pragma unroll
-  for (int s = 0; s < kStages - 1; ++s) issue(s);
 
-  // 2. stage scales / zero points (and the tokens for XS)
-#pragma unroll
-  for (int u = 0; u < 8; ++u) {
-    const int e = threadIdx.x + u * kThreads;
-    if (e < total_sc) { sc_s[e] = sv[u]; z_s[e] = zv[u]; }
-  }
-  for (int e = threadIdx.x + 8 * kThreads; e < total_sc; e += kThreads) load_sc(e, sc_s[e], z_s[e]);
+  // 2. tokens for XS: fp16 in B-fragment order plus per-chunk even/odd sums
   if (XS) {
     bool bad = false;
     // 16 consecutive units (128 k) of one token are 16 consecutive lanes: their
@@ -329,6 +331,7 @@ __device__ void streamer_block(const DecodeParams& p, float* smem) {
     }
     if (bad) record_status(&g_decode_status, DEV_ERR_INVALID);
   }
+  cp_async_wait<kStages - 1>();                            // the staged scales, zeros and B
   __syncthreads();
 
   // 3. main loop
@@ -345,8 +348,11 @@ __device__ void streamer_block(const DecodeParams& p, float* smem) {
     const int srow = tl * 16 * p.ng;
     const __half* sc_lo = sc_s + srow + g * p.ng;
     const __half* sc_hi = sc_lo + 8 * p.ng;
-    const uint8_t* z_lo = z_s + srow + g * p.ng;
-    const uint8_t* z_hi = z_lo + 8 * p.ng;
+    const uint8_t* z_lo = z_s + (tl * 16 + g) * zrow;
+    const uint8_t* z_hi = z_lo + 8 * zrow;
+    auto zero_at = [&](const uint8_t* zr, int gi) -> int {
+      return p.sym ? 8 : (gi & 1) ? (zr[gi >> 1] >> 4) : (zr[gi >> 1] & 15);
+    };
     for (int j = 0; j < per_tile; ++j) {
       issue((slot + kStages - 1) % kStages);
       cp_async_wait<kStages - 1>();
@@ -356,12 +362,22 @@ __device__ void streamer_block(const DecodeParams& p, float* smem) {
       const uint4 whi = my_ring[(slot * 2 + 1) * 32 + lane];
       const uint32_t wl[4] = {wlo.x, wlo.y, wlo.z, wlo.w};
       const uint32_t wh[4] = {whi.x, whi.y, whi.z, whi.w};
-      const int zl = z_lo[gi], zh = z_hi[gi];
-      float part[MT][4];
+      const int zl = zero_at(z_lo, gi), zh = zero_at(z_hi, gi);
+      // two accumulators per token tile (the two k-steps of each 32-k piece)
+      // halve the dependent MMA chain
+      float part[MT][4], part2[MT][4];
 #pragma unroll
       for (int t = 0; t < MT; ++t)
 #pragma unroll
-        for (int i = 0; i < 4; ++i) part[t][i] = 0.0f;
+        for (int i = 0; i < 4; ++i) part[t][i] = part2[t][i] = 0.0f;
+      if (!XS && j + 2 < per_tile) {
+        // token rows of the chunk after next into L1 (16 tokens x 256 B)
+        const int chn = warp + kWarps * (j + 2);
+        for (int q = lane; q < Mpad * 2; q += 32) {
+          const int tok = q >> 1;
+          if (tok < p.M) prefetch_l1(p.x + (size_t)tok * p.K + chn * kChunkK + (q & 1) * 64);
+        }
+      }
       if constexpr (XS) {
         const uint4* xrowp = xs + g * xrow + ch * 16 + 4 * c;
 #pragma unroll
@@ -374,8 +390,10 @@ __device__ void streamer_block(const DecodeParams& p, float* smem) {
           const uint32_t e2 = (l8 & 0x00F000F0u) | 0x54005400u, e3 = (h8 & 0x00F000F0u) | 0x54005400u;
           const uint4 xv = tok_ok ? xrowp[w] : make_uint4(0, 0, 0, 0);
           mma_f16_16816(part[0], a0, a1, a2, a3, xv.x, xv.y);
-          mma_f16_16816(part[0], e0, e1, e2, e3, xv.z, xv.w);
+          mma_f16_16816(part2[0], e0, e1, e2, e3, xv.z, xv.w);
         }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) part[0][i] += part2[0][i];
         const float P0 = ok0 ? Ps[u0 * p.nchunks + ch] : 0.0f, X0 = ok0 ? Xs[u0 * p.nchunks + ch] : 0.0f;
         const float P1 = ok1 ? Ps[u1 * p.nchunks + ch] : 0.0f, X1 = ok1 ? Xs[u1 * p.nchunks + ch] : 0.0f;
         part[0][0] -= fmaf((float)zl, X0, P0);
@@ -403,9 +421,13 @@ __device__ void streamer_block(const DecodeParams& p, float* smem) {
             const uint32_t b00 = __byte_perm(xv.x, xv.z, 0x5410), b01 = __byte_perm(xv.x, xv.z, 0x7632);
             const uint32_t b10 = __byte_perm(xv.y, xv.w, 0x5410), b11 = __byte_perm(xv.y, xv.w, 0x7632);
             mma_bf16_16816(part[t], va[0], vb[0], va[1], vb[1], b00, b01);
-            mma_bf16_16816(part[t], va[2], vb[2], va[3], vb[3], b10, b11);
+            mma_bf16_16816(part2[t], va[2], vb[2], va[3], vb[3], b10, b11);
           }
         }
+#pragma unroll
+        for (int t = 0; t < MT; ++t)
+#pragma unroll
+          for (int i = 0; i < 4; ++i) part[t][i] += part2[t][i];
       }
       if (PERCH) {
 #pragma unroll
@@ -485,9 +507,9 @@ __device__ void streamer_block(const DecodeParams& p, float* smem) {
     if (COMP) {
       const int rh = p.r / 2;
       for (int j0 = 0; j0 < p.r; j0 += 16) {
-        const uint32_t* Blo = reinterpret_cast<const uint32_t*>(p.B + (size_t)n_lo * p.r + j0);
-        const uint32_t* Bhi = reinterpret_cast<const uint32_t*>(p.B + (size_t)n_hi * p.r + j0);
-        const uint32_t a0 = __ldg(Blo + c), a1 = __ldg(Bhi + c), a2 = __ldg(Blo + c + 4), a3 = __ldg(Bhi + c + 4);
+        const uint32_t* Blo = reinterpret_cast<const uint32_t*>(B_s + (size_t)(tl * 16 + g) * p.r + j0);
+        const uint32_t* Bhi = reinterpret_cast<const uint32_t*>(B_s + (size_t)(tl * 16 + g + 8) * p.r + j0);
+        const uint32_t a0 = Blo[c], a1 = Bhi[c], a2 = Blo[c + 4], a3 = Bhi[c + 4];
         const int tok = t * 8 + g;
         const uint32_t* th = Ts + tok * rh + j0 / 2;
         const uint32_t* tlo = Ts + Mpad * rh + tok * rh + j0 / 2;
@@ -565,12 +587,14 @@ size_t xs_smem(int M, int K) {
   return 16 + (size_t)M * (K / 8 + 1) * 16 + 2 * (size_t)M * (K / kChunkK) * 4;
 }
 
-size_t streamer_smem(int MT, bool comp, int max_tiles, int ng, size_t extra = 0) {
+size_t streamer_smem(int MT, bool comp, int max_tiles, int ng, int rank, size_t extra = 0) {
   size_t s = extra + (size_t)kWarps * kStages * 2 * 32 * 16; // ring (+ staged tokens)
   s += (size_t)kWarps * MT * 128 * 4;                        // red
   s += (size_t)max_tiles * MT * 128 * 4;                     // ybuf
   if (comp) s += (size_t)MT * 8 * kMaxRank * 4;              // T hi/lo
-  s += (size_t)max_tiles * 16 * ng * 3;                      // scales + zeros
+  s += (size_t)max_tiles * 16 * ng * 2;                      // scales
+  s += (size_t)max_tiles * 16 * ((ng + 1) / 2) + 16;         // zero-point bytes (+ alignment)
+  if (comp) s += (size_t)max_tiles * 16 * rank * 2 + 16;     // factor-B rows
   return s;
 }
 
@@ -603,7 +627,7 @@ int build_plan(const spear_w4_layer& L, int MT, int M, bool comp, bool try_xs, c
     pl->P = std::max(1, std::min(blocks - pl->Q, pl->tiles));
     pl->max_tiles = (pl->tiles + pl->P - 1) / pl->P;
     if (pl->max_tiles > 64) return fail(SPEAR_ERR_UNSUPPORTED, "decode: too many tiles per block");
-    pl->smem = std::max(streamer_smem(pl->MT, has_rank, pl->max_tiles, pl->ng, extra),
+    pl->smem = std::max(streamer_smem(pl->MT, has_rank, pl->max_tiles, pl->ng, L.rank, extra),
                         (size_t)kWarps * pl->MT * 128 * 4);
     if (pl->smem > di.smem_optin)
       return fail(SPEAR_ERR_UNSUPPORTED, "decode: shape needs %zu B of shared memory", pl->smem);
