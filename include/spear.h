@@ -119,12 +119,16 @@ spear_status spear_pack_w4(const float* W, int N, int K, int group_size, int sym
  * streams the int4 weights, computes g(x) and A x for every token in the same
  * launch and adds alpha*g*B(Ax) in the epilogue.  1 <= M <= 64.
  *   x : device bf16 [M][K];  y : device [M][N], bf16 or fp32 (out_dtype).
+ * M <= 32 runs on warp-level MMAs; M >= 33 on the tcgen05 tensor cores.
  * The thread blocks of the launch exchange the M x (rank+1) down-projection
- * and the partial sums of weight tiles they share through `workspace`
- * (device, at least spear_decode_workspace_bytes()).  The workspace must be
- * zeroed once before its first use (spear_workspace_init) and is left ready
- * for the next call; two calls that run at the same time must not share one.
- * After a SPEAR_ERR_TIMEOUT device status, zero it again.
+ * through `workspace` (device, at least spear_decode_workspace_bytes()).
+ * The workspace must be zeroed once before its first use
+ * (spear_workspace_init) and is left ready for the next call; two calls that
+ * run at the same time must not share one.  After a SPEAR_ERR_TIMEOUT device
+ * status, zero it again.
+ * Some launches carry the activations in fp16 (M <= 8 with M*K*2 <= 48 KB,
+ * and M >= 33): there |x| must stay below 65504; a larger value is reported
+ * as SPEAR_ERR_INVALID_ARG through spear_get_device_status.
  */
 spear_status spear_decode_workspace_bytes(const spear_w4_layer* L, int M, size_t* bytes);
 spear_status spear_linear_decode(const spear_w4_layer* L, const uint16_t* x, int M,
@@ -179,6 +183,20 @@ spear_status spear_linear_prefill(const spear_w4_layer* L, const uint16_t* x, in
 
 /* Zero a decode workspace (device) on `stream`. */
 spear_status spear_workspace_init(void* workspace, size_t bytes, void* stream);
+
+/*
+ * Launch overlap for chains of decode calls (process-wide, default off).
+ * With enable != 0, decode launches (spear_linear_decode and _noalloc) use
+ * programmatic dependent launch: a decode kernel may start while the kernel
+ * before it on the same stream is still finishing, and streams its weights
+ * meanwhile; it waits for that kernel to complete (with its memory visible)
+ * before it reads x, touches the workspace or writes y.  The caller
+ * guarantees that the kernel immediately before a decode call on the stream
+ * does not write that layer's qweight, scales, zeros, A, B or w_g.
+ * Host only; takes effect for launches issued afterwards (also inside stream
+ * capture, where it becomes a programmatic graph edge).
+ */
+spear_status spear_set_launch_overlap(int enable);
 
 /*
  * Module selection (Technical Summary 2.1 B), host only.  damage[L] >= 0 is a

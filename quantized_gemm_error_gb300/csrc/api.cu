@@ -1,6 +1,7 @@
 // api.cu -- the library's C ABI (include/spear.h): argument checks, error
 // reporting, phase dispatch and the host-side module selection.
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -60,6 +61,13 @@ int cuda_check(cudaError_t e, const char* what) {
   if (e == cudaSuccess) return SPEAR_OK;
   return fail(SPEAR_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
 }
+
+namespace {
+std::atomic<bool> g_launch_overlap{false};
+}  // namespace
+
+void set_launch_overlap(bool on) { g_launch_overlap.store(on); }
+bool launch_overlap() { return g_launch_overlap.load(); }
 
 bool log_plans() {
   static const bool on = [] {
@@ -158,7 +166,7 @@ spear_status spear_linear_decode(const spear_w4_layer* L, const uint16_t* x, int
   if (out_dtype != SPEAR_OUT_BF16 && out_dtype != SPEAR_OUT_F32)
     return fail(SPEAR_ERR_INVALID_ARG, "out_dtype=%d", out_dtype);
   return launch_decode(*L, x, M, y, out_dtype == SPEAR_OUT_F32, workspace, ws_bytes,
-                       static_cast<cudaStream_t>(stream));
+                       static_cast<cudaStream_t>(stream), launch_overlap());
 }
 
 spear_status spear_linear_decode_noalloc(const spear_w4_layer* L, const uint16_t* x, int M, void* y,
@@ -243,6 +251,11 @@ spear_status spear_layer_select_mask(const float* damage, const float* cost, int
       return SPEAR_OK;
     }
   }
+  return SPEAR_OK;
+}
+
+spear_status spear_set_launch_overlap(int enable) {
+  spear::set_launch_overlap(enable != 0);
   return SPEAR_OK;
 }
 

@@ -81,10 +81,11 @@ struct DecodeParams {
 // Lane (g, c) of a warp loads 16 B (8 consecutive k) per row; within a 32-k
 // piece the MMA's k positions {2c, 2c+1, 2c+8, 2c+9} of k-step h map to the
 // lane's k = 8c + 4h + {0, 1, 2, 3}, identically for both operands.
-constexpr int kMaxSlices = 8;
+constexpr int kMaxSlices = 16;
 
 template <int MT>
 __device__ void producer_block(const DecodeParams& p, float* smem) {
+  pdl_wait();                                              // x and the workspace come from earlier work
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, c = lane & 3;
   const int RT = (p.r + 1 + 15) / 16;
@@ -106,11 +107,13 @@ __device__ void producer_block(const DecodeParams& p, float* smem) {
   for (int t = 0; t < MT; ++t)
 #pragma unroll
     for (int i = 0; i < 4; ++i) acc[t][i] = 0.0f;
-  for (int pc0 = warp; pc0 < npieces; pc0 += 2 * kWarps) {
-    // two pieces per pass: all of their loads are in flight together
-    uint4 va[2], vb[2], xv[2][MT];
+  // U pieces per pass: all of their loads are in flight together (the plan
+  // sizes the slices so that one pass covers a warp's share)
+  constexpr int U = MT == 1 ? 4 : MT == 2 ? 2 : 1;
+  for (int pc0 = warp; pc0 < npieces; pc0 += U * kWarps) {
+    uint4 va[U], vb[U], xv[U][MT];
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
+    for (int h = 0; h < U; ++h) {
       const int pc = pc0 + h * kWarps;
       const bool ok = pc < npieces;
       const int kb = c0 * kChunkK + pc * 32 + 8 * c;
@@ -123,7 +126,7 @@ __device__ void producer_block(const DecodeParams& p, float* smem) {
       }
     }
 #pragma unroll
-    for (int h = 0; h < 2; ++h)
+    for (int h = 0; h < U; ++h)
 #pragma unroll
       for (int t = 0; t < MT; ++t) {
         mma_bf16_16816(acc[t], va[h].x, vb[h].x, va[h].y, vb[h].y, xv[h][t].x, xv[h][t].y);
@@ -258,13 +261,6 @@ __device__ void streamer_block(const DecodeParams& p, float* smem) {
   const int xunits = XS ? p.M * k8 : 0;
   constexpr int kXBatch = XS ? 4 : 1;
   uint4 xr[kXBatch];
-  if (XS) {
-#pragma unroll
-    for (int j = 0; j < kXBatch; ++j) {
-      const int e = threadIdx.x + j * kThreads;
-      xr[j] = e < xunits ? ldg16(p.x + (size_t)e * 8) : make_uint4(0, 0, 0, 0);
-    }
-  }
   {
     auto stage = [&](void* dst, const void* src_base, size_t bytes) {
       for (size_t e = threadIdx.x; e < bytes / 16; e += kThreads)
@@ -278,6 +274,16 @@ __device__ void streamer_block(const DecodeParams& p, float* smem) {
   }
 #pragma unroll
   for (int st = 0; st < kStages - 1; ++st) issue(st);
+  // everything above reads only the layer's weights; x, the workspace and y
+  // may belong to the kernel before this one (overlapped launches)
+  pdl_wait();
+  if (XS) {
+#pragma unroll
+    for (int j = 0; j < kXBatch; ++j) {
+      const int e = threadIdx.x + j * kThreads;
+      xr[j] = e < xunits ? ldg16(p.x + (size_t)e * 8) : make_uint4(0, 0, 0, 0);
+    }
+  }
   if (!XS) {
     // token rows of this warp's first two chunks into L1 (16 tokens x 256 B per chunk)
     for (int jj = 0; jj < 2 && jj < per_tile; ++jj) {
@@ -543,6 +549,7 @@ __device__ void streamer_block(const DecodeParams& p, float* smem) {
 template <int MT, bool COMP, bool PERCH, bool XS>
 __global__ void __launch_bounds__(kThreads, (MT <= 2 ? 2 : 1)) decode_kernel(const DecodeParams p) {
   extern __shared__ __align__(16) float smem[];
+  pdl_launch_dependents();                                 // every block is resident: let the next kernel queue
   if ((int)blockIdx.x < p.Q) {
     // The plain layer keeps the same block split as the compensated one (its
     // producer blocks idle), so forcing the gate to zero reproduces it bit for bit.
@@ -616,10 +623,11 @@ int build_plan(const spear_w4_layer& L, int MT, int M, bool comp, bool try_xs, c
   bool settled = false;
   for (int iter = 0; iter < 8 && !settled; ++iter) {
     if (has_rank) {
-      // RT row tiles x S K-slices; one slice's A bytes ~ one streamer's weight bytes
+      // RT row tiles x S K-slices, enough slices that each producer warp
+      // loads its share of A and x in one pass (U 32-k pieces)
       const int RT = (L.rank + 1 + 15) / 16;
-      const double w_per_block = (double)L.N * L.K / 2.0 / std::max(1, blocks - RT);
-      const int S = (int)std::lround(32.0 * L.K / w_per_block);
+      const int U = MT == 1 ? 4 : MT == 2 ? 2 : 1;
+      const int S = (4 * pl->nchunks + U * kWarps - 1) / (U * kWarps);
       pl->Q = RT * std::max(1, std::min(S, std::min(kMaxSlices, pl->nchunks)));
     } else {
       pl->Q = 0;
@@ -668,8 +676,10 @@ int get_plan(const spear_w4_layer& L, int M, Plan* out) {
       return SPEAR_OK;
     }
   Plan p{};
-  // staged tokens when they fit (M <= 8), else tokens from L1
-  if (build_plan(L, MT, M, comp != 0, MT == 1, di, &p) != SPEAR_OK) {
+  // staged tokens when they are small enough to keep two blocks per SM
+  // (M <= 8, M K 2 <= 48 KB), else tokens from L1
+  const bool try_xs = MT == 1 && xs_smem(M, L.K) <= 48 * 1024;
+  if (build_plan(L, MT, M, comp != 0, try_xs, di, &p) != SPEAR_OK) {
     if (MT != 1) return SPEAR_ERR_UNSUPPORTED;
     if (int rc = build_plan(L, MT, M, comp != 0, false, di, &p)) return rc;
   }
@@ -703,8 +713,8 @@ int decode_workspace_bytes(const spear_w4_layer& L, int M, size_t* bytes) {
 }
 
 int launch_decode(const spear_w4_layer& L, const uint16_t* x, int M, void* y, int out_f32, void* ws,
-                  size_t ws_bytes, cudaStream_t st) {
-  if (use_tc(M)) return launch_decode_tc(L, x, M, y, out_f32, ws, ws_bytes, st);
+                  size_t ws_bytes, cudaStream_t st, bool overlap) {
+  if (use_tc(M)) return launch_decode_tc(L, x, M, y, out_f32, ws, ws_bytes, st, overlap);
   Plan pl;
   if (int rc = get_plan(L, M, &pl)) return rc;
   if (!ws || ws_bytes < pl.total)
@@ -736,6 +746,11 @@ int launch_decode(const spear_w4_layer& L, const uint16_t* x, int M, void* y, in
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = pl.smem;
   cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = overlap ? 1 : 0;
   return cuda_check(cudaLaunchKernelEx(&cfg, pl.fn, p), "decode launch");
 }
 
@@ -793,7 +808,8 @@ int launch_decode_noalloc(const spear_w4_layer& L, const uint16_t* x, int M, voi
   if (int rc = noalloc_scratch(&ws)) return rc;
   // the synchronisation words must start at zero
   if (int rc = cuda_check(cudaMemsetAsync(ws, 0, sync_bytes, st), "decode scratch clear")) return rc;
-  return launch_decode(L, x, M, y, out_f32, ws, kNoallocScratchBytes, st);
+  // (after a memset, so no launch overlap)
+  return launch_decode(L, x, M, y, out_f32, ws, kNoallocScratchBytes, st, false);
 }
 
 int read_and_clear_status_decode(unsigned* out, cudaStream_t st) {

@@ -108,6 +108,7 @@ __device__ __forceinline__ void give_up(int* abort_flag) {
 // same k permutation, so the mma.sync sums are the plain dot products.
 template <int NP>
 __device__ void tc_producer(const TcParams& p, uint8_t* smem, int pc, int rank) {
+  pdl_wait();                                              // x and the workspace come from earlier work
   constexpr int MT = NP / 8;
   constexpr int NW = kThreads / 32;
   constexpr int U = MT <= 2 ? 2 : 1;                       // 32-k pieces per pass
@@ -307,6 +308,14 @@ __device__ void tc_tile(const CUtensorMap* tm_w, const CUtensorMap* tm_x, const 
       prefetch_tmap(tm_w);
       prefetch_tmap(tm_x);
       int ri = 0, xi = 0;
+      // the first weight units need no slot wait and read only the layer's
+      // weights: issue them before waiting for the kernel ahead (overlapped launches)
+      for (const int pre = nunits < kRawStages ? nunits : kRawStages; ri < pre; ++ri) {
+        const uint32_t full = smem_u32(&raw_full[ri]);
+        mbar_arrive_expect_tx(full, kRawBytes);
+        tma_load_2d(smem_u32(raw_ring + ri * kRawBytes), tm_w, unit_of(ri) * (kUnitK / 2), n0, full);
+      }
+      pdl_wait();
       bool ok = true;
       uint64_t t0 = globaltimer_ns();
       uint32_t idle = 0;
@@ -463,6 +472,7 @@ __device__ void tc_tile(const CUtensorMap* tm_w, const CUtensorMap* tm_x, const 
   } else {
     // --------------------------- token converters + epilogue (warps 0-3)
     const int tid = threadIdx.x;                           // 0..127
+    pdl_wait();                                            // they read the workspace
     bool ok = true, bad = false;
     for (int s = 0; s < nsteps; ++s) {
       const int rs = s % kXrStages, xs = s % kX16Stages;
@@ -556,6 +566,7 @@ __device__ void tc_tile(const CUtensorMap* tm_w, const CUtensorMap* tm_x, const 
   }
 
   // ---------------------------------------------- epilogue (whole cluster)
+  pdl_wait();                                              // y may be read by the kernel ahead
   cluster_sync();                                          // every partial is in place
   if (warp < kTmaWarp && !s_abort) {
     const int tid = threadIdx.x;
@@ -601,6 +612,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
                  const TcParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  pdl_launch_dependents();                                 // every CTA is resident: let the next kernel queue
   const int rank = (int)cluster_ctarank();
   const int cid = (int)blockIdx.x / p.S;
   const int npc = p.RT * p.Kp;
@@ -780,7 +792,7 @@ int decode_tc_workspace_bytes(const spear_w4_layer& L, int M, size_t* bytes) {
 size_t decode_tc_sync_bytes() { return 256; }
 
 int launch_decode_tc(const spear_w4_layer& L, const uint16_t* x, int M, void* y, int out_f32, void* ws,
-                     size_t ws_bytes, cudaStream_t st) {
+                     size_t ws_bytes, cudaStream_t st, bool overlap) {
   TcPlan pl;
   if (int rc = get_tc_plan(L, M, &pl)) return rc;
   if (!ws || ws_bytes < pl.total)
@@ -818,13 +830,15 @@ int launch_decode_tc(const spear_w4_layer& L, const uint16_t* x, int M, void* y,
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = pl.smem;
   cfg.stream = st;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = pl.S;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = overlap ? 2 : 1;
   return cuda_check(cudaLaunchKernelEx(&cfg, pl.fn, tm_w, tm_x, p), "decode launch");
 }
 

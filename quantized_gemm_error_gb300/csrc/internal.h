@@ -28,6 +28,10 @@ int device_info(DeviceInfo* out);
 // value other than "0": launch plans are then printed to stderr once each.
 bool log_plans();
 
+// Programmatic dependent launch for decode kernels (spear_set_launch_overlap).
+void set_launch_overlap(bool on);
+bool launch_overlap();
+
 // Raises (never lowers) the dynamic shared-memory limit of kernel `fn` on the
 // current device to at least `bytes`.  Launches captured in CUDA graphs keep
 // the size they were captured with, so a limit that a later plan lowered
@@ -42,7 +46,7 @@ int read_and_clear_status_pack(unsigned* out, cudaStream_t st);
 // ---- decode.cu
 int decode_workspace_bytes(const spear_w4_layer& L, int M, size_t* bytes);
 int launch_decode(const spear_w4_layer& L, const uint16_t* x, int M, void* y, int out_f32,
-                  void* ws, size_t ws_bytes, cudaStream_t st);
+                  void* ws, size_t ws_bytes, cudaStream_t st, bool overlap);
 int launch_decode_noalloc(const spear_w4_layer& L, const uint16_t* x, int M, void* y, int out_f32,
                           cudaStream_t st);
 int read_and_clear_status_decode(unsigned* out, cudaStream_t st);
@@ -51,7 +55,7 @@ int read_and_clear_status_decode(unsigned* out, cudaStream_t st);
 int decode_tc_workspace_bytes(const spear_w4_layer& L, int M, size_t* bytes);
 size_t decode_tc_sync_bytes();
 int launch_decode_tc(const spear_w4_layer& L, const uint16_t* x, int M, void* y, int out_f32, void* ws,
-                     size_t ws_bytes, cudaStream_t st);
+                     size_t ws_bytes, cudaStream_t st, bool overlap);
 int read_and_clear_status_decode_tc(unsigned* out, cudaStream_t st);
 
 // ---- prefill.cu

@@ -31,8 +31,8 @@ OUT_BF16, OUT_F32 = 0, 1
 # every symbol include/spear.h declares
 EXPORTS = ["spear_pack_w4_sizes", "spear_pack_w4", "spear_decode_workspace_bytes",
            "spear_linear_decode", "spear_linear_decode_noalloc", "spear_prefill_workspace_bytes", "spear_linear_prefill",
-           "spear_workspace_init", "spear_layer_select_mask", "spear_get_device_status",
-           "spear_status_string", "spear_last_error", "spear_version"]
+           "spear_workspace_init", "spear_set_launch_overlap", "spear_layer_select_mask",
+           "spear_get_device_status", "spear_status_string", "spear_last_error", "spear_version"]
 
 
 class SpearError(RuntimeError):
@@ -76,6 +76,7 @@ def load(path: str = LIB_PATH):
             "spear_workspace_init": [P, S, P],
             "spear_layer_select_mask": [P, P, I, ctypes.c_double, I, I, P, P],
             "spear_get_device_status": [ctypes.POINTER(I), P],
+            "spear_set_launch_overlap": [I],
         }
         for name, args in sig.items():
             fn = getattr(lib, name)
@@ -265,6 +266,14 @@ def spear_get_device_status(stream=None) -> int:
     out = ctypes.c_int()
     _check(load().spear_get_device_status(ctypes.byref(out), _stream(stream)), "spear_get_device_status")
     return out.value
+
+
+def spear_set_launch_overlap(enable: bool) -> None:
+    """Process-wide: decode launches may start while the previous kernel on
+    their stream finishes (programmatic dependent launch).  The caller
+    guarantees that the kernel right before a decode call does not write that
+    layer's weights; see include/spear.h."""
+    _check(load().spear_set_launch_overlap(1 if enable else 0), "spear_set_launch_overlap")
 
 
 def version() -> str:
