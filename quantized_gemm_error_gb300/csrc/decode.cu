@@ -85,7 +85,6 @@ constexpr int kMaxSlices = 16;
 
 template <int MT>
 __device__ void producer_block(const DecodeParams& p, float* smem) {
-  pdl_wait();                                              // x and the workspace come from earlier work
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, c = lane & 3;
   const int RT = (p.r + 1 + 15) / 16;
@@ -110,6 +109,9 @@ __device__ void producer_block(const DecodeParams& p, float* smem) {
   // U pieces per pass: all of their loads are in flight together (the plan
   // sizes the slices so that one pass covers a warp's share)
   constexpr int U = MT == 1 ? 4 : MT == 2 ? 2 : 1;
+  // the rows of A and w_g are weights: the first pass loads them before
+  // waiting for the kernel ahead (overlapped launches), then the tokens
+  bool waited = false;
   for (int pc0 = warp; pc0 < npieces; pc0 += U * kWarps) {
     uint4 va[U], vb[U], xv[U][MT];
 #pragma unroll
@@ -119,6 +121,16 @@ __device__ void producer_block(const DecodeParams& p, float* smem) {
       const int kb = c0 * kChunkK + pc * 32 + 8 * c;
       va[h] = (ok && wlo) ? ldg16(wlo + kb) : make_uint4(0, 0, 0, 0);
       vb[h] = (ok && whi) ? ldg16(whi + kb) : make_uint4(0, 0, 0, 0);
+    }
+    if (!waited) {
+      pdl_wait();
+      waited = true;
+    }
+#pragma unroll
+    for (int h = 0; h < U; ++h) {
+      const int pc = pc0 + h * kWarps;
+      const bool ok = pc < npieces;
+      const int kb = c0 * kChunkK + pc * 32 + 8 * c;
 #pragma unroll
       for (int t = 0; t < MT; ++t) {
         const int tok = t * 8 + g;
@@ -133,6 +145,7 @@ __device__ void producer_block(const DecodeParams& p, float* smem) {
         mma_bf16_16816(acc[t], va[h].z, vb[h].z, va[h].w, vb[h].w, xv[h][t].z, xv[h][t].w);
       }
   }
+  if (!waited) pdl_wait();                                 // before the workspace
   // cross-warp sum in a fixed order; this block's partial for its 16 rows
 #pragma unroll
   for (int t = 0; t < MT; ++t)

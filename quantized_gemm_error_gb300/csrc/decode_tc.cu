@@ -108,7 +108,6 @@ __device__ __forceinline__ void give_up(int* abort_flag) {
 // same k permutation, so the mma.sync sums are the plain dot products.
 template <int NP>
 __device__ void tc_producer(const TcParams& p, uint8_t* smem, int pc, int rank) {
-  pdl_wait();                                              // x and the workspace come from earlier work
   constexpr int MT = NP / 8;
   constexpr int NW = kThreads / 32;
   constexpr int U = MT <= 2 ? 2 : 1;                       // 32-k pieces per pass
@@ -134,6 +133,9 @@ __device__ void tc_producer(const TcParams& p, uint8_t* smem, int pc, int rank) 
   for (int t = 0; t < MT; ++t)
 #pragma unroll
     for (int i = 0; i < 4; ++i) acc[t][i] = 0.0f;
+  // the rows of A and w_g are weights: the first pass loads them before
+  // waiting for the kernel ahead (overlapped launches), then the tokens
+  bool waited = false;
   for (int pc0 = warp; pc0 < npieces; pc0 += U * NW) {
     uint4 va[U], vb[U], xv[U][MT];
 #pragma unroll
@@ -143,6 +145,16 @@ __device__ void tc_producer(const TcParams& p, uint8_t* smem, int pc, int rank) 
       const int kb = c0 * 128 + pcs * 32 + 8 * c;
       va[h] = (ok && wlo) ? ldg16(wlo + kb) : make_uint4(0, 0, 0, 0);
       vb[h] = (ok && whi) ? ldg16(whi + kb) : make_uint4(0, 0, 0, 0);
+    }
+    if (!waited) {
+      pdl_wait();
+      waited = true;
+    }
+#pragma unroll
+    for (int h = 0; h < U; ++h) {
+      const int pcs = pc0 + h * NW;
+      const bool ok = pcs < npieces;
+      const int kb = c0 * 128 + pcs * 32 + 8 * c;
 #pragma unroll
       for (int t = 0; t < MT; ++t) {
         const int tok = t * 8 + g;
@@ -157,6 +169,7 @@ __device__ void tc_producer(const TcParams& p, uint8_t* smem, int pc, int rank) 
         mma_bf16_16816(acc[t], va[h].z, vb[h].z, va[h].w, vb[h].w, xv[h][t].z, xv[h][t].w);
       }
   }
+  if (!waited) pdl_wait();                                 // before the workspace
   // fixed-order sum over the warps: this CTA's partial [16 rows][NP tokens]
 #pragma unroll
   for (int t = 0; t < MT; ++t)
@@ -256,8 +269,12 @@ __device__ void tc_tile(const CUtensorMap* tm_w, const CUtensorMap* tm_x, const 
   // after the main loop: the partial [64 tokens][257] over the raw ring and
   // the start of the weight ring, T and the gates further into the weight ring
   float* red = reinterpret_cast<float*>(smem);
-  float* T_s = reinterpret_cast<float*>(bf_ring + kBfBytes);       // [NP][r]
-  float* gate_s = T_s + NP * kMaxRank;                              // [NP]
+  // the gates and T split into bf16 hi + lo (T = hi + lo to ~2^-16 relative),
+  // the B operand of the epilogue's B T on warp-level MMAs; in the second
+  // fp16 step of the idle ring (16.25 KB)
+  float* gate_s = reinterpret_cast<float*>(bf_ring + kBfBytes);    // [NP]
+  uint32_t* th_s = reinterpret_cast<uint32_t*>(gate_s + NP);        // [NP][r/2] bf16 pairs, hi
+  uint32_t* tl_s = th_s + NP * kMaxRank / 2;                        // [NP][r/2] bf16 pairs, lo
   const int b_stride = 2 * p.r + 16;
 
   if (threadIdx.x == 0) {
@@ -550,9 +567,16 @@ __device__ void tc_tile(const CUtensorMap* tm_w, const CUtensorMap* tm_x, const 
         gate_s[t] = gt;
       }
       named_sync(1, kXWarps * 32);
-      for (int e = tid; e < NP * p.r; e += kXWarps * 32) {
-        const int t = e / p.r, jj = e % p.r;
-        T_s[e] = s_pok ? gate_s[t] * __ldcg(p.ws_P + (size_t)t * rp + jj) : 0.0f;
+      for (int e = tid; e < NP * p.r / 2; e += kXWarps * 32) {
+        const int t = e / (p.r / 2), jj = 2 * (e % (p.r / 2));
+        float ta = 0.0f, tb = 0.0f;
+        if (s_pok) {
+          ta = gate_s[t] * __ldcg(p.ws_P + (size_t)t * rp + jj);
+          tb = gate_s[t] * __ldcg(p.ws_P + (size_t)t * rp + jj + 1);
+        }
+        const float ha = __bfloat162float(__float2bfloat16_rn(ta)), hb = __bfloat162float(__float2bfloat16_rn(tb));
+        th_s[e] = pack_bf16x2(ha, hb);
+        tl_s[e] = pack_bf16x2(ta - ha, tb - hb);
       }
       named_sync(1, kXWarps * 32);
       if (tid == 0) {
@@ -569,32 +593,41 @@ __device__ void tc_tile(const CUtensorMap* tm_w, const CUtensorMap* tm_x, const 
   pdl_wait();                                              // y may be read by the kernel ahead
   cluster_sync();                                          // every partial is in place
   if (warp < kTmaWarp && !s_abort) {
-    const int tid = threadIdx.x;
+    // one (16-row, 8-token) output tile per warp at a time: B T on mma.sync
+    // (B rows as A, T hi/lo as B), then the S partials through DSMEM, then y
     const uint32_t red_base = smem_u32(red);
-    for (int e = tid; e < nr * p.M; e += kTmaWarp * 32) {
-      const int rl = e % nr, t = e / nr;
-      const int rowt = e_r0 + rl, nn = n0 + rowt;
-      const uint32_t la = red_base + (uint32_t)(t * kRedStride + rowt) * 4u;
-      float v = 0.0f;
-      for (int qq = 0; qq < S; ++qq) v += dsmem_ld_f32(dsmem_addr(la, (uint32_t)qq));
+    const int g = lane >> 2, c = lane & 3;
+    const int rtiles = (nr + 15) / 16, ttiles = (p.M + 7) / 8;
+    for (int item = warp; item < rtiles * ttiles; item += kTmaWarp) {
+      const int rt = item % rtiles, tt = item / rtiles;
+      float bt[4] = {0.0f, 0.0f, 0.0f, 0.0f};
       if (COMP) {
-        const uint8_t* br = B_s + rl * b_stride;
-        const float* tr = T_s + t * p.r;
-        float bt = 0.0f;
-        for (int jj = 0; jj < p.r; jj += 8) {
-          const uint4 b8 = *reinterpret_cast<const uint4*>(br + jj * 2);
-          const uint32_t bw[4] = {b8.x, b8.y, b8.z, b8.w};
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            bt = fmaf(bf16x2_lo(bw[i]), tr[jj + 2 * i], bt);
-            bt = fmaf(bf16x2_hi(bw[i]), tr[jj + 2 * i + 1], bt);
-          }
+        const uint8_t* blo = B_s + (rt * 16 + g) * b_stride;
+        const uint8_t* bhi = blo + 8 * b_stride;
+        const int tok = tt * 8 + g;
+        const uint32_t* th = th_s + tok * (p.r / 2);
+        const uint32_t* tl = tl_s + tok * (p.r / 2);
+        for (int j0 = 0; j0 < p.r; j0 += 16) {
+          const uint32_t a0 = *reinterpret_cast<const uint32_t*>(blo + (j0 + 2 * c) * 2);
+          const uint32_t a1 = *reinterpret_cast<const uint32_t*>(bhi + (j0 + 2 * c) * 2);
+          const uint32_t a2 = *reinterpret_cast<const uint32_t*>(blo + (j0 + 2 * c + 8) * 2);
+          const uint32_t a3 = *reinterpret_cast<const uint32_t*>(bhi + (j0 + 2 * c + 8) * 2);
+          mma_bf16_16816(bt, a0, a1, a2, a3, th[j0 / 2 + c], th[j0 / 2 + c + 4]);
+          mma_bf16_16816(bt, a0, a1, a2, a3, tl[j0 / 2 + c], tl[j0 / 2 + c + 4]);
         }
-        v += bt;
       }
-      if (nn < p.N) {
-        if (p.out_f32) reinterpret_cast<float*>(p.y)[(size_t)t * p.N + nn] = v;
-        else reinterpret_cast<__nv_bfloat16*>(p.y)[(size_t)t * p.N + nn] = __float2bfloat16_rn(v);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int rl = rt * 16 + g + 8 * (i >> 1), t = tt * 8 + 2 * c + (i & 1);
+        if (rl >= nr || t >= p.M) continue;
+        const int rowt = e_r0 + rl, nn = n0 + rowt;
+        const uint32_t la = red_base + (uint32_t)(t * kRedStride + rowt) * 4u;
+        float v = bt[i];
+        for (int qq = 0; qq < S; ++qq) v += dsmem_ld_f32(dsmem_addr(la, (uint32_t)qq));
+        if (nn < p.N) {
+          if (p.out_f32) reinterpret_cast<float*>(p.y)[(size_t)t * p.N + nn] = v;
+          else reinterpret_cast<__nv_bfloat16*>(p.y)[(size_t)t * p.N + nn] = __float2bfloat16_rn(v);
+        }
       }
     }
   }
@@ -665,7 +698,7 @@ size_t tile_smem(int NP, int BF, int nr_max, int rank, TcPlan* c) {
   c->off_xr = (uint32_t)off;
   off += (size_t)kXrStages * NP * 128;
   c->off_B = (uint32_t)off;
-  off += (size_t)nr_max * (2 * std::max(rank, 8) + 16);
+  off += (size_t)align_up(nr_max, 16) * (2 * std::max(rank, 8) + 16);   // whole 16-row MMA tiles
   return align_up(off, 1024) + 1024;            // + alignment slack of the dynamic base
 }
 
