@@ -325,6 +325,7 @@ def run_ours(args, world, rank, local):
             calls.append((K, N, M))
     ws_bytes = max(spear.spear_decode_workspace_bytes(L, M) for _, _, L, _ in copies[0] for M in DECODE_M)
     ws = spear.new_workspace(ws_bytes, device)
+    torch.cuda.synchronize()              # inputs made on the default stream; calls run on `stream`
     step_bytes = sum(decode_bytes(K, N, M) for K, N, M in calls)
 
     def step(cp, comp=True):
@@ -508,6 +509,7 @@ def run_prefill(torch, spear, device, stream, peaks):
             y = torch.empty(M, N, dtype=torch.bfloat16, device=device)
             ws = spear.new_workspace(max(spear.spear_prefill_workspace_bytes(L, M, m)
                                          for m in (spear.PREFILL_FUSED, spear.PREFILL_STREAM)), device, zero=False)
+            torch.cuda.synchronize()          # inputs made on the default stream; calls run on `stream`
             res = {}
             for name, Lc, mode in (("fused", L, spear.PREFILL_FUSED), ("stream", L, spear.PREFILL_STREAM),
                                    ("plain", L.with_comp(False), spear.PREFILL_FUSED)):
