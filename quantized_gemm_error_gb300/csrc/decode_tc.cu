@@ -62,13 +62,13 @@ constexpr int kRawBytes = kTileRows * kUnitK / 2;   // 32 KB
 constexpr int kBfBytes = kTileRows * kStepK * 2;    // 32 KB of fp16 weights per step
 constexpr int kX16Bytes = 64 * kStepK * 2;          // 8 KB: 64 token rows (MMA M = 64)
 constexpr int kRawStages = 2, kXrStages = 2, kX16Stages = 3, kMaxBfStages = 3;
-constexpr int kRedStride = kTileRows + 1;       // floats per token row of the partial
+constexpr int kRedStride = kTileRows + 4;       // floats per token row of the partial (16-byte rows)
 constexpr int kXWarps = 4;                      // warps 0-3: token conversion, TMEM drain
 constexpr int kConvWarp0 = 4, kConvWarps = 16;  // warps 4-19: weight conversion (two threads per row)
 constexpr int kTmaWarp = 20, kMmaWarp = 21;
 constexpr int kThreads = 704;
-constexpr int kMaxRank = 64;
 constexpr int kMaxS = 8;
+constexpr int kMaxKp = 8;                        // K ranges of the producer clusters
 constexpr uint64_t kPipeWaitNs = 2000ull * 1000 * 1000;   // 2 s: far beyond any legitimate wait
 constexpr uint64_t kTWaitNs = 200ull * 1000 * 1000;       // 200 ms for the published P
 
@@ -192,8 +192,14 @@ __device__ void tc_producer(const TcParams& p, uint8_t* smem, int pc, int rank) 
     float* dst = p.Kp == 1 ? nullptr : p.ws_part + ((size_t)kp * p.RT + rt) * 16 * NP;
     for (int e = threadIdx.x; e < 16 * NP; e += kThreads) {
       const uint32_t la = smem_u32(part + e);
+      float pv[kMaxS];
+#pragma unroll
+      for (int q = 0; q < kMaxS; ++q)                        // every load in flight, then the sum
+        if (q < p.S) pv[q] = dsmem_ld_f32(dsmem_addr(la, (uint32_t)q));
       float v = 0.0f;
-      for (int q = 0; q < p.S; ++q) v += dsmem_ld_f32(dsmem_addr(la, (uint32_t)q));
+#pragma unroll
+      for (int q = 0; q < kMaxS; ++q)
+        if (q < p.S) v += pv[q];
       if (dst) {
         dst[e] = v;
       } else {
@@ -211,8 +217,14 @@ __device__ void tc_producer(const TcParams& p, uint8_t* smem, int pc, int rank) 
       // the last of the Kp clusters of this row tile sums them in K order
       __threadfence();
       for (int e = threadIdx.x; e < 16 * NP; e += kThreads) {
+        float pv[kMaxKp];
+#pragma unroll
+        for (int q = 0; q < kMaxKp; ++q)
+          if (q < p.Kp) pv[q] = __ldcg(p.ws_part + ((size_t)q * p.RT + rt) * 16 * NP + e);
         float v = 0.0f;
-        for (int q = 0; q < p.Kp; ++q) v += __ldcg(p.ws_part + ((size_t)q * p.RT + rt) * 16 * NP + e);
+#pragma unroll
+        for (int q = 0; q < kMaxKp; ++q)
+          if (q < p.Kp) v += pv[q];
         const int row = e / NP, tok = e % NP, i = rt * 16 + row;
         if (i <= p.r) p.ws_P[(size_t)tok * (p.r + 1) + i] = v;
       }
@@ -258,7 +270,9 @@ __device__ void tc_tile(const CUtensorMap* tm_w, const CUtensorMap* tm_x, const 
   const int nsteps = 4 * nunits - (half_tail ? 2 : 0);     // 64-k steps (even)
   const int ngroups = nsteps / 2;                          // 128-k groups
   auto unit_of = [&](int i) { return rank + i * S; };      // global unit of local unit i
-  const int e_r0 = rank * kTileRows / S, e_r1 = (rank + 1) * kTileRows / S;   // rows finished here
+  // rows finished here: whole 16-row tiles, so every owner range starts on a
+  // 16-byte boundary of the partial and of y
+  const int e_r0 = 16 * (rank * (kTileRows / 16) / S), e_r1 = 16 * ((rank + 1) * (kTileRows / 16) / S);
   const int nr = e_r1 - e_r0;
 
   uint8_t* raw_ring = smem;                                // [2][256 rows][128 B] int4
@@ -269,12 +283,11 @@ __device__ void tc_tile(const CUtensorMap* tm_w, const CUtensorMap* tm_x, const 
   // after the main loop: the partial [64 tokens][257] over the raw ring and
   // the start of the weight ring, T and the gates further into the weight ring
   float* red = reinterpret_cast<float*>(smem);
-  // the gates and T split into bf16 hi + lo (T = hi + lo to ~2^-16 relative),
-  // the B operand of the epilogue's B T on warp-level MMAs; in the second
-  // fp16 step of the idle ring (16.25 KB)
-  float* gate_s = reinterpret_cast<float*>(bf_ring + kBfBytes);    // [NP]
-  uint32_t* th_s = reinterpret_cast<uint32_t*>(gate_s + NP);        // [NP][r/2] bf16 pairs, hi
-  uint32_t* tl_s = th_s + NP * kMaxRank / 2;                        // [NP][r/2] bf16 pairs, lo
+  // T = alpha g t split into bf16 hi + lo (T = hi + lo to ~2^-16 relative),
+  // the B operand of the epilogue's B T on warp-level MMAs: in the bf16 token
+  // ring once the last token tile is converted (NP r 4 <= 2 NP 128 bytes)
+  uint32_t* th_s = reinterpret_cast<uint32_t*>(xr_ring);            // [NP][r/2] bf16 pairs, hi
+  uint32_t* tl_s = th_s + NP * p.r / 2;                             // [NP][r/2] bf16 pairs, lo
   const int b_stride = 2 * p.r + 16;
 
   if (threadIdx.x == 0) {
@@ -411,29 +424,29 @@ __device__ void tc_tile(const CUtensorMap* tm_w, const CUtensorMap* tm_x, const 
     const bool row_ok = n < p.N;
     const int zrow = (p.ng + 1) / 2;
     auto gidx = [&](int gl) { return PERCH ? 0 : 2 * unit_of(gl >> 1) + (gl & 1); };
+    // The prefetched registers hold the loaded zero-point byte and scale bits
+    // as they are; the nibble is picked and the scale doubled where they are
+    // used, so no instruction waits for the load before then.
     auto load_z = [&](int gl) -> uint32_t {
-      if (p.sym || !row_ok || gl >= ngroups) return 8u;
-      const int gi = gidx(gl);
-      const uint32_t b = __ldg(p.zeros + (size_t)n * zrow + gi / 2);
-      return (gi & 1) ? (b >> 4) : (b & 15u);
+      if (p.sym || !row_ok || gl >= ngroups) return 0x88u;
+      return __ldg(p.zeros + (size_t)n * zrow + gidx(gl) / 2);
     };
-    // fp16x2 of the group scale (per-channel: 1.0, the scale is applied in the epilogue)
     auto load_s = [&](int gl) -> uint32_t {
-      if (PERCH) return 0x3C003C00u;
-      if (!row_ok || gl >= ngroups) return 0u;
-      return (uint32_t)__half_as_ushort(__ldg(p.scales + (size_t)n * p.ng + gidx(gl))) * 0x00010001u;
+      if (PERCH || !row_ok || gl >= ngroups) return 0u;
+      return __half_as_ushort(__ldg(p.scales + (size_t)n * p.ng + gidx(gl)));
     };
     bool ok = true;
     auto wait_all = [&](uint64_t* bar, uint32_t parity) {
-      ok = ok && mbar_wait(smem_u32(bar), parity, kPipeWaitNs) && !s_abort;
-      ok = __all_sync(0xffffffffu, ok);
+      ok = __all_sync(0xffffffffu, ok && mbar_wait(smem_u32(bar), parity, kPipeWaitNs) && !s_abort);
     };
     // one 64-k step: this thread's 32 k of its row, as (u - z) * s in fp16
-    auto convert = [&](int s, uint32_t z, uint32_t s2) {
+    auto convert = [&](int s, uint32_t zb, uint32_t sb) {
       const int u = s >> 2, j = s & 3, slot = u % kRawStages;
       if (j == 0) wait_all(&raw_full[slot], (u / kRawStages) & 1);
       wait_all(&bf_empty[s % BF], ((s / BF) & 1) ^ 1);
       if (ok) {
+        const uint32_t z = (gidx(s >> 1) & 1) ? (zb >> 4) : (zb & 15u);
+        const uint32_t s2 = sb * 0x00010001u;                      // fp16x2 of the group scale
         const uint4 rv = *reinterpret_cast<const uint4*>(raw_ring + slot * kRawBytes + row * 128 +
                                                           (((2 * j + half) ^ (row & 7)) << 4));
         uint8_t* brow = bf_ring + (s % BF) * kBfBytes + row * 128;
@@ -460,6 +473,16 @@ __device__ void tc_tile(const CUtensorMap* tm_w, const CUtensorMap* tm_x, const 
         if (j == 3 || s == nsteps - 1) mbar_arrive(smem_u32(&raw_empty[slot]));
       }
     };
+    // the factor-B rows of the rows finished here, for the epilogue: in
+    // flight during the conversions
+    if (COMP) {
+      const int per = p.r / 8;                             // 16-byte pieces per row
+      for (int e = threadIdx.x - kConvWarp0 * 32; e < nr * per; e += kConvWarps * 32) {
+        const int rr = e / per, cc = e % per, nn = n0 + e_r0 + rr;
+        if (nn < p.N) cp_async16(B_s + rr * b_stride + cc * 16, p.B + (size_t)nn * p.r + cc * 8);
+      }
+      cp_async_commit();
+    }
     // zero points and scales travel 4 groups ahead of their use in named
     // registers (slot = group mod 4, never indexed at run time)
     uint32_t z0 = load_z(0), z1 = load_z(1), z2 = load_z(2), z3 = load_z(3);
@@ -476,15 +499,34 @@ __device__ void tc_tile(const CUtensorMap* tm_w, const CUtensorMap* tm_x, const 
       if (gl0 + 2 < ngroups) group(gl0 + 2, z2, c2);
       if (gl0 + 3 < ngroups) group(gl0 + 3, z3, c3);
     }
-    // the factor-B rows of the rows finished here, for the epilogue
-    if (COMP) {
-      const int per = p.r / 8;                             // 16-byte pieces per row
-      for (int e = threadIdx.x - kConvWarp0 * 32; e < nr * per; e += kConvWarps * 32) {
-        const int rr = e / per, cc = e % per, nn = n0 + e_r0 + rr;
-        if (nn < p.N) cp_async16(B_s + rr * b_stride + cc * 16, p.B + (size_t)nn * p.r + cc * 8);
+    if (COMP) cp_async_wait<0>();
+
+    // accumulator [64 tokens][256 rows] -> this CTA's partial, token-major (row
+    // stride 257).  Each converter warp drains 64 columns of the TMEM lane
+    // quarter it may access (warp mod 4); tokens 16 q .. 16 q + 15 sit in its
+    // lanes 0-15.
+    ok = __all_sync(0xffffffffu, ok && mbar_wait(smem_u32(&acc_full), 0, kPipeWaitNs) && !s_abort);
+    if (ok) {
+      tc_fence_after();
+      const int q = warp & 3, cb = 64 * ((warp - kConvWarp0) >> 2);
+      const int t = 16 * q + lane;
+      const bool t_ok = lane < 16 && t < NP;
+#pragma unroll 1
+      for (int c0 = cb; c0 < cb + 64; c0 += 32) {
+        uint32_t v[32];
+        tmem_ld_32cols(tmem + ((uint32_t)(32 * q) << 16) + c0, v);
+        tmem_ld_wait();
+        if (t_ok) {
+#pragma unroll
+          for (int i = 0; i < 32; i += 4)
+            *reinterpret_cast<float4*>(red + t * kRedStride + c0 + i) =
+                make_float4(s_scale[c0 + i] * __uint_as_float(v[i]), s_scale[c0 + i + 1] * __uint_as_float(v[i + 1]),
+                            s_scale[c0 + i + 2] * __uint_as_float(v[i + 2]),
+                            s_scale[c0 + i + 3] * __uint_as_float(v[i + 3]));
+        }
       }
-      cp_async_commit();
-      cp_async_wait<0>();
+    } else {
+      give_up(&s_abort);
     }
   } else {
     // --------------------------- token converters + epilogue (warps 0-3)
@@ -494,8 +536,8 @@ __device__ void tc_tile(const CUtensorMap* tm_w, const CUtensorMap* tm_x, const 
     for (int s = 0; s < nsteps; ++s) {
       const int rs = s % kXrStages, xs = s % kX16Stages;
       ok = ok && mbar_wait(smem_u32(&xr_full[rs]), (s / kXrStages) & 1, kPipeWaitNs) &&
-           mbar_wait(smem_u32(&x16_empty[xs]), ((s / kX16Stages) & 1) ^ 1, kPipeWaitNs) && !s_abort;
-      ok = __all_sync(0xffffffffu, ok);
+           mbar_wait(smem_u32(&x16_empty[xs]), ((s / kX16Stages) & 1) ^ 1, kPipeWaitNs);
+      ok = __all_sync(0xffffffffu, ok && !s_abort);
       if (ok) {
         const uint8_t* src = xr_ring + rs * NP * 128;
         uint8_t* dst = x16_ring + xs * kX16Bytes;
@@ -525,29 +567,9 @@ __device__ void tc_tile(const CUtensorMap* tm_w, const CUtensorMap* tm_x, const 
     }
     if (bad) record_status(&g_dtc_status, DEV_ERR_INVALID);
 
-    // accumulator [64 tokens][256 rows] -> this CTA's partial, token-major (row stride 257)
-    ok = ok && mbar_wait(smem_u32(&acc_full), 0, kPipeWaitNs) && !s_abort;
-    ok = __all_sync(0xffffffffu, ok);
-    if (ok) {
-      tc_fence_after();
-      const int t = 16 * warp + lane;                      // token of this lane (lanes 0-15)
-      const bool t_ok = lane < 16 && t < NP;
-#pragma unroll 1
-      for (int c0 = 0; c0 < kTileRows; c0 += 32) {
-        uint32_t v[32];
-        tmem_ld_32cols(tmem + ((uint32_t)(32 * warp) << 16) + c0, v);
-        tmem_ld_wait();
-        if (t_ok) {
-#pragma unroll
-          for (int i = 0; i < 32; ++i) red[t * kRedStride + c0 + i] = s_scale[c0 + i] * __uint_as_float(v[i]);
-        }
-      }
-    } else {
-      give_up(&s_abort);
-    }
-
     if (COMP) {
-      // the published P: gate per token, then T = alpha g P
+      // the published P: gate per token, then T = alpha g P (P read straight
+      // from the workspace, every load of a thread in flight together)
       if (tid == 0) {
         const uint64_t tw = globaltimer_ns();
         int pok = 0;
@@ -560,23 +582,38 @@ __device__ void tc_tile(const CUtensorMap* tm_w, const CUtensorMap* tm_x, const 
         s_pok = pok;
       }
       named_sync(1, kXWarps * 32);
-      const int rp = p.r + 1;
-      for (int t = tid; t < NP; t += kXWarps * 32) {
-        float gt = 0.0f;
-        if (s_pok && t < p.M) gt = p.alpha / (1.0f + expf(-(__ldcg(p.ws_P + (size_t)t * rp + p.r) + p.b_g)));
-        gate_s[t] = gt;
-      }
-      named_sync(1, kXWarps * 32);
-      for (int e = tid; e < NP * p.r / 2; e += kXWarps * 32) {
-        const int t = e / (p.r / 2), jj = 2 * (e % (p.r / 2));
-        float ta = 0.0f, tb = 0.0f;
-        if (s_pok) {
-          ta = gate_s[t] * __ldcg(p.ws_P + (size_t)t * rp + jj);
-          tb = gate_s[t] * __ldcg(p.ws_P + (size_t)t * rp + jj + 1);
+      // one round trip: every thread loads its pairs of P and, for the token of
+      // each pair, the gate row, all in flight together; the gate is formed
+      // per pair (the same value for every pair of a token)
+      const int rp = p.r + 1, half_r = p.r / 2;
+      const bool pok = s_pok != 0;
+      constexpr int kPer = 8;                              // pairs per thread and pass (r <= 32: one pass)
+      for (int e0 = 0; e0 < NP * half_r; e0 += kPer * kXWarps * 32) {
+        float pa[kPer], pb[kPer], pg[kPer];
+#pragma unroll
+        for (int i = 0; i < kPer; ++i) {
+          const int e = e0 + tid + i * kXWarps * 32;
+          pa[i] = pb[i] = pg[i] = 0.0f;
+          if (pok && e < NP * half_r) {
+            const int t = e / half_r, jj = 2 * (e % half_r);
+            const float* row = p.ws_P + (size_t)t * rp;
+            pa[i] = __ldcg(row + jj);
+            pb[i] = __ldcg(row + jj + 1);
+            pg[i] = __ldcg(row + p.r);
+          }
         }
-        const float ha = __bfloat162float(__float2bfloat16_rn(ta)), hb = __bfloat162float(__float2bfloat16_rn(tb));
-        th_s[e] = pack_bf16x2(ha, hb);
-        tl_s[e] = pack_bf16x2(ta - ha, tb - hb);
+#pragma unroll
+        for (int i = 0; i < kPer; ++i) {
+          const int e = e0 + tid + i * kXWarps * 32;
+          if (e < NP * half_r) {
+            const int t = e / half_r;
+            const float gt = (pok && t < p.M) ? p.alpha / (1.0f + expf(-(pg[i] + p.b_g))) : 0.0f;
+            const float ta = gt * pa[i], tb = gt * pb[i];
+            const float ha = __bfloat162float(__float2bfloat16_rn(ta)), hb = __bfloat162float(__float2bfloat16_rn(tb));
+            th_s[e] = pack_bf16x2(ha, hb);
+            tl_s[e] = pack_bf16x2(ta - ha, tb - hb);
+          }
+        }
       }
       named_sync(1, kXWarps * 32);
       if (tid == 0) {
@@ -590,18 +627,18 @@ __device__ void tc_tile(const CUtensorMap* tm_w, const CUtensorMap* tm_x, const 
   }
 
   // ---------------------------------------------- epilogue (whole cluster)
-  pdl_wait();                                              // y may be read by the kernel ahead
-  cluster_sync();                                          // every partial is in place
-  if (warp < kTmaWarp && !s_abort) {
-    // one (16-row, 8-token) output tile per warp at a time: B T on mma.sync
-    // (B rows as A, T hi/lo as B), then the S partials through DSMEM, then y
-    const uint32_t red_base = smem_u32(red);
-    const int g = lane >> 2, c = lane & 3;
-    const int rtiles = (nr + 15) / 16, ttiles = (p.M + 7) / 8;
-    for (int item = warp; item < rtiles * ttiles; item += kTmaWarp) {
-      const int rt = item % rtiles, tt = item / rtiles;
-      float bt[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-      if (COMP) {
+  if (COMP && warp < kTmaWarp) {
+    // B T for the rows finished here, added into this CTA's own partial
+    // before the cluster reads it: one (16-row, 8-token) tile per warp at a
+    // time on mma.sync (B rows as A, T hi/lo as B).  Warps 0-19 only: the
+    // TMA and MMA warps never reach this barrier.
+    named_sync(2, kTmaWarp * 32);                          // drained partial, T and B rows in place
+    if (!s_abort) {
+      const int g = lane >> 2, c = lane & 3;
+      const int rtiles = nr / 16, ttiles = (p.M + 7) / 8;
+      for (int item = warp; item < rtiles * ttiles; item += kTmaWarp) {
+        const int rt = item % rtiles, tt = item / rtiles;
+        float bt[4] = {0.0f, 0.0f, 0.0f, 0.0f};
         const uint8_t* blo = B_s + (rt * 16 + g) * b_stride;
         const uint8_t* bhi = blo + 8 * b_stride;
         const int tok = tt * 8 + g;
@@ -615,18 +652,53 @@ __device__ void tc_tile(const CUtensorMap* tm_w, const CUtensorMap* tm_x, const 
           mma_bf16_16816(bt, a0, a1, a2, a3, th[j0 / 2 + c], th[j0 / 2 + c + 4]);
           mma_bf16_16816(bt, a0, a1, a2, a3, tl[j0 / 2 + c], tl[j0 / 2 + c + 4]);
         }
-      }
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int rl = rt * 16 + g + 8 * (i >> 1), t = tt * 8 + 2 * c + (i & 1);
-        if (rl >= nr || t >= p.M) continue;
-        const int rowt = e_r0 + rl, nn = n0 + rowt;
-        const uint32_t la = red_base + (uint32_t)(t * kRedStride + rowt) * 4u;
-        float v = bt[i];
-        for (int qq = 0; qq < S; ++qq) v += dsmem_ld_f32(dsmem_addr(la, (uint32_t)qq));
-        if (nn < p.N) {
-          if (p.out_f32) reinterpret_cast<float*>(p.y)[(size_t)t * p.N + nn] = v;
-          else reinterpret_cast<__nv_bfloat16*>(p.y)[(size_t)t * p.N + nn] = __float2bfloat16_rn(v);
+        for (int i = 0; i < 4; ++i) {
+          const int rl = rt * 16 + g + 8 * (i >> 1), t = tt * 8 + 2 * c + (i & 1);
+          if (t < p.M) red[t * kRedStride + e_r0 + rl] += bt[i];
+        }
+      }
+    }
+  }
+  pdl_wait();                                              // y may be read by the kernel ahead
+  cluster_sync();                                          // every partial is in place
+  if (!s_abort) {
+    // y for the rows finished here: four consecutive rows of one token per
+    // thread, the S partials read 16 bytes at a time (all in flight), summed
+    // in rank order
+    const uint32_t red_base = smem_u32(red);
+    const int nq = nr / 4;
+    const bool vec = (p.N & 3) == 0;
+    for (int idx = threadIdx.x; idx < p.M * nq; idx += kThreads) {
+      const int t = idx / nq, row = e_r0 + 4 * (idx % nq), nn = n0 + row;
+      const uint32_t la = red_base + (uint32_t)(t * kRedStride + row) * 4u;
+      float4 pv[kMaxS];
+#pragma unroll
+      for (int qq = 0; qq < kMaxS; ++qq)
+        if (qq < S) pv[qq] = dsmem_ld_f32x4(dsmem_addr(la, (uint32_t)qq));
+      float4 v = pv[0];
+#pragma unroll
+      for (int qq = 1; qq < kMaxS; ++qq)
+        if (qq < S) { v.x += pv[qq].x; v.y += pv[qq].y; v.z += pv[qq].z; v.w += pv[qq].w; }
+      if (nn >= p.N) continue;
+      const size_t o = (size_t)t * p.N + nn;
+      if (vec) {                                           // nn + 3 < N as N and nn are multiples of 4
+        if (p.out_f32) {
+          *reinterpret_cast<float4*>(reinterpret_cast<float*>(p.y) + o) = v;
+        } else {
+          const __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y), hi = __floats2bfloat162_rn(v.z, v.w);
+          uint2 pk;
+          pk.x = *reinterpret_cast<const uint32_t*>(&lo);
+          pk.y = *reinterpret_cast<const uint32_t*>(&hi);
+          *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(p.y) + o) = pk;
+        }
+      } else {
+        const float vv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          if (nn + j >= p.N) break;
+          if (p.out_f32) reinterpret_cast<float*>(p.y)[o + j] = vv[j];
+          else reinterpret_cast<__nv_bfloat16*>(p.y)[o + j] = __float2bfloat16_rn(vv[j]);
         }
       }
     }
@@ -721,7 +793,7 @@ int build_tc_plan(const spear_w4_layer& L, int NP, bool comp, const DeviceInfo& 
     TcPlan c = *pl;
     c.S = S;
     const int units_per = (pl->units + S - 1) / S;      // most units one CTA takes
-    c.Kp = has_rank ? std::max(1, std::min(8, (int)std::ceil((double)L.K / (S * 512.0)))) : 1;
+    c.Kp = has_rank ? std::max(1, std::min(kMaxKp, (int)std::ceil((double)L.K / (S * 512.0)))) : 1;
     const int nr_max = (kTileRows + S - 1) / S;
     // three fp16 weight steps in flight when they fit, else two
     c.BF = kMaxBfStages;

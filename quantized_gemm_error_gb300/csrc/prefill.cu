@@ -203,23 +203,27 @@ w4_gemm_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
     const int zrow = (p.ng + 1) / 2;
     const int stages_per_group = p.perch ? k_stages : p.G / kBK;
     const int ngroups = (k_stages + stages_per_group - 1) / stages_per_group;
+    // The prefetched registers hold the loaded zero-point byte and scale bits
+    // as they are; the nibble is picked and the scale doubled where they are
+    // used, so no instruction waits for the load before then.  Per-channel
+    // scales are applied in the epilogue.
     auto load_z = [&](int gi) -> uint32_t {
-      if (p.sym || !row_ok || gi >= ngroups) return 8u;
-      const uint32_t zb = __ldg(p.zeros + (size_t)n * zrow + gi / 2);
-      return (gi & 1) ? (zb >> 4) : (zb & 15u);
+      if (p.sym || !row_ok || gi >= ngroups) return 0x88u;
+      return __ldg(p.zeros + (size_t)n * zrow + gi / 2);
     };
-    // fp16x2 of the group scale; per-channel: 1.0 (the scale is applied in the epilogue)
     auto load_s = [&](int gi) -> uint32_t {
-      if (p.perch) return 0x3C003C00u;
-      if (!row_ok || gi >= ngroups) return 0u;
-      return (uint32_t)__half_as_ushort(__ldg(p.scales + (size_t)n * p.ng + gi)) * 0x00010001u;
+      if (p.perch || !row_ok || gi >= ngroups) return 0u;
+      return __half_as_ushort(__ldg(p.scales + (size_t)n * p.ng + gi));
     };
     bool ok = true;
-    auto convert = [&](int s, uint32_t z, uint32_t s2) {
+    auto convert = [&](int s, uint32_t zb, uint32_t sb) {
       const int slot = s % kStages;
-      ok = ok && mbar_wait(smem_u32(&bar_full[slot]), (s / kStages) & 1, kWaitNs) && !s_abort;
-      ok = __all_sync(0xffffffffu, ok);
+      ok = __all_sync(0xffffffffu, ok && mbar_wait(smem_u32(&bar_full[slot]), (s / kStages) & 1, kWaitNs) &&
+                                       !s_abort);
       if (ok) {
+        const int gi = s / stages_per_group;
+        const uint32_t z = (gi & 1) ? (zb >> 4) : (zb & 15u);
+        const uint32_t s2 = sb * 0x00010001u;                      // fp16x2 of the group scale
         const uint8_t* raw = raw_slot(slot) + ct * 32;
         uint8_t* wrow = w_slot(slot) + ct * 128;
         const uint32_t z_lo = f16x2_bias(z);                       // 1024 + z
@@ -268,8 +272,7 @@ w4_gemm_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
 
     // epilogue: TMEM lanes 32*(warp%4) .. +31 are this warp's rows (tokens);
     // warps 2-5 take output columns [0, 128), warps 6-9 columns [128, 256)
-    ok = ok && mbar_wait(smem_u32(&bar_acc), 0, kWaitNs);
-    ok = __all_sync(0xffffffffu, ok);
+    ok = __all_sync(0xffffffffu, ok && mbar_wait(smem_u32(&bar_acc), 0, kWaitNs));
     if (!ok) give_up();
     tc_fence_after();
     if (!s_abort) {
