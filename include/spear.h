@@ -58,7 +58,8 @@ enum {
 
 /* Prefill modes (Technical Summary 2.2 A, "semi-fused" prefill). */
 enum {
-  SPEAR_PREFILL_AUTO = 0,    /* pick by measured time for the shape            */
+  SPEAR_PREFILL_AUTO = 0,    /* FUSED: the faster mode at every measured shape
+                                (Llama-7B projections, M = 512 .. 8192)        */
   SPEAR_PREFILL_FUSED = 1,   /* gate/down-projection pass, then one GEMM whose
                                 K loop is extended by the rank-r up-projection */
   SPEAR_PREFILL_STREAM = 2   /* W4 GEMM on `stream` while the compensator's

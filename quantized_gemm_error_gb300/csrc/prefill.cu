@@ -338,11 +338,14 @@ w4_gemm_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
 // split K in 128-k chunks and are summed in a fixed order.  Same operand
 // mapping as the decode producer: lane (g, c) owns 8 consecutive k per row.
 constexpr int kCdThreads = 256;
-constexpr int kCdTok = 32;
+constexpr int kCdWarps = kCdThreads / 32;
+constexpr int kCdTok = 16;                    // tokens per cluster
 constexpr int kCdMT = kCdTok / 8;
+constexpr int kCdMaxCK = 8;                   // CTAs per cluster (K ranges)
 
 struct CompDownParams {
   int M, K, r;
+  int CK;               // cluster size: CTAs splitting K for one token tile
   const __nv_bfloat16* x;
   const __nv_bfloat16* A;
   const __nv_bfloat16* w_g;
@@ -368,13 +371,24 @@ __device__ __forceinline__ uint4 bf16x8_to_f16x8(uint4 v, bool& out_of_range) {
   return make_uint4(h2(x0, x4), h2(x1, x5), h2(x2, x6), h2(x3, x7));
 }
 
+// One cluster of CK CTAs per 16-token tile; CTA `rank` covers the 32-k pieces
+// [rank n / CK, (rank + 1) n / CK) of K (and writes the fp16 token copy of
+// that range).  Its 8 warps take interleaved pieces, U at a time with every
+// load in flight; the warp partials are summed in warp order, the CK partials
+// in rank order through distributed shared memory, then rank 0 forms the gate
+// and T = alpha g (A x) as bf16 hi + lo.
 template <int RT>
 __global__ void __launch_bounds__(kCdThreads) comp_down_kernel(const CompDownParams p) {
-  __shared__ float red[8][kCdMT][4][32];
-  __shared__ float res[RT * 16][kCdTok];      // [projection row][token]
+  constexpr int U = RT <= 3 ? 2 : 1;                       // pieces in flight per warp
+  __shared__ float red[kCdWarps][kCdMT][4][32];
+  __shared__ float part[RT * 16][kCdTok];                  // [projection row][token]
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, c = lane & 3;
-  const int tok0 = blockIdx.x * kCdTok;
+  const int CK = p.CK;
+  const int rank = (int)cluster_ctarank();
+  const int tok0 = (int)(blockIdx.x / CK) * kCdTok;
+  const int npieces = p.K / 32;
+  const int pc0 = rank * npieces / CK, pc1 = (rank + 1) * npieces / CK;
   float acc[RT][kCdMT][4];
 #pragma unroll
   for (int rt = 0; rt < RT; ++rt)
@@ -382,38 +396,52 @@ __global__ void __launch_bounds__(kCdThreads) comp_down_kernel(const CompDownPar
     for (int t = 0; t < kCdMT; ++t)
 #pragma unroll
       for (int i = 0; i < 4; ++i) acc[rt][t][i] = 0.0f;
-  const int nchunks = p.K / 128;
-  for (int ch = warp; ch < nchunks; ch += 8) {
+  bool bad = false;
+  for (int pb = pc0 + warp; pb < pc1; pb += U * kCdWarps) {
+    uint4 xv[U][kCdMT], va[U][RT], vb[U][RT];
 #pragma unroll
-    for (int piece = 0; piece < 4; ++piece) {
-      const int kb = ch * 128 + piece * 32 + 8 * c;
-      uint4 xv[kCdMT];
+    for (int u = 0; u < U; ++u) {
+      const int pc = pb + u * kCdWarps;
+      const bool ok = pc < pc1;
+      const int kb = pc * 32 + 8 * c;
 #pragma unroll
       for (int t = 0; t < kCdMT; ++t) {
         const int tok = tok0 + t * 8 + g;
-        xv[t] = tok < p.M ? ldg16(p.x + (size_t)tok * p.K + kb) : make_uint4(0, 0, 0, 0);
-        if (p.x16 && tok < p.M) {
-          bool bad = false;
-          *reinterpret_cast<uint4*>(p.x16 + (size_t)tok * p.K + kb) = bf16x8_to_f16x8(xv[t], bad);
-          if (bad) record_status(&g_prefill_status, DEV_ERR_INVALID);
-        }
+        xv[u][t] = (ok && tok < p.M) ? ldg16(p.x + (size_t)tok * p.K + kb) : make_uint4(0, 0, 0, 0);
       }
 #pragma unroll
       for (int rt = 0; rt < RT; ++rt) {
         const int rlo = rt * 16 + g, rhi = rlo + 8;
-        const uint4 va = rlo < p.r ? ldg16(p.A + (size_t)rlo * p.K + kb)
-                                   : rlo == p.r ? ldg16(p.w_g + kb) : make_uint4(0, 0, 0, 0);
-        const uint4 vb = rhi < p.r ? ldg16(p.A + (size_t)rhi * p.K + kb)
-                                   : rhi == p.r ? ldg16(p.w_g + kb) : make_uint4(0, 0, 0, 0);
-#pragma unroll
-        for (int t = 0; t < kCdMT; ++t) {
-          mma_bf16_16816(acc[rt][t], va.x, vb.x, va.y, vb.y, xv[t].x, xv[t].y);
-          mma_bf16_16816(acc[rt][t], va.z, vb.z, va.w, vb.w, xv[t].z, xv[t].w);
-        }
+        va[u][rt] = !ok ? make_uint4(0, 0, 0, 0)
+                        : rlo < p.r ? ldg16(p.A + (size_t)rlo * p.K + kb)
+                                    : rlo == p.r ? ldg16(p.w_g + kb) : make_uint4(0, 0, 0, 0);
+        vb[u][rt] = !ok ? make_uint4(0, 0, 0, 0)
+                        : rhi < p.r ? ldg16(p.A + (size_t)rhi * p.K + kb)
+                                    : rhi == p.r ? ldg16(p.w_g + kb) : make_uint4(0, 0, 0, 0);
       }
     }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int pc = pb + u * kCdWarps;
+      if (p.x16 && pc < pc1) {
+        const int kb = pc * 32 + 8 * c;
+#pragma unroll
+        for (int t = 0; t < kCdMT; ++t) {
+          const int tok = tok0 + t * 8 + g;
+          if (tok < p.M) *reinterpret_cast<uint4*>(p.x16 + (size_t)tok * p.K + kb) = bf16x8_to_f16x8(xv[u][t], bad);
+        }
+      }
+#pragma unroll
+      for (int rt = 0; rt < RT; ++rt)
+#pragma unroll
+        for (int t = 0; t < kCdMT; ++t) {
+          mma_bf16_16816(acc[rt][t], va[u][rt].x, vb[u][rt].x, va[u][rt].y, vb[u][rt].y, xv[u][t].x, xv[u][t].y);
+          mma_bf16_16816(acc[rt][t], va[u][rt].z, vb[u][rt].z, va[u][rt].w, vb[u][rt].w, xv[u][t].z, xv[u][t].w);
+        }
+    }
   }
-  // fixed-order sum over warps, one projection-row tile at a time
+  if (bad) record_status(&g_prefill_status, DEV_ERR_INVALID);
+  // fixed-order sum over the warps, one projection-row tile at a time
 #pragma unroll
   for (int rt = 0; rt < RT; ++rt) {
 #pragma unroll
@@ -424,23 +452,43 @@ __global__ void __launch_bounds__(kCdThreads) comp_down_kernel(const CompDownPar
     for (int e = threadIdx.x; e < kCdMT * 4 * 32; e += kCdThreads) {
       const int t = e / 128, i = (e / 32) & 3, ln = e & 31;
       float s = 0.0f;
-      for (int w = 0; w < 8; ++w) s += red[w][t][i][ln];
+#pragma unroll
+      for (int w = 0; w < kCdWarps; ++w) s += red[w][t][i][ln];
       // C fragment element i of lane ln: row (ln/4) + 8 (i/2), token 2 (ln%4) + (i%2)
-      res[rt * 16 + (ln >> 2) + 8 * (i >> 1)][t * 8 + 2 * (ln & 3) + (i & 1)] = s;
+      part[rt * 16 + (ln >> 2) + 8 * (i >> 1)][t * 8 + 2 * (ln & 3) + (i & 1)] = s;
     }
     __syncthreads();
   }
-  // row r is the gate logit; rows 0..r-1 the down-projection
-  for (int e = threadIdx.x; e < kCdTok * p.r; e += kCdThreads) {
-    const int m = e / p.r, j = e % p.r;
-    const int tok = tok0 + m;
-    const float gate = 1.0f / (1.0f + expf(-(res[p.r][m] + p.b_g)));
-    const float tv = p.alpha * gate * res[j][m];
-    const __nv_bfloat16 hi = __float2bfloat16_rn(tv);
-    const __nv_bfloat16 lo = __float2bfloat16_rn(tv - __bfloat162float(hi));
-    if (tok < p.M) {
-      p.T2[(size_t)tok * p.t2_cols + j] = hi;
-      p.T2[(size_t)tok * p.t2_cols + p.r + j] = lo;
+  cluster_sync();                                          // every CTA's partial is in place
+  if (rank == 0) {
+    // the CK partials in rank order (all loads in flight), into this CTA's own
+    // partial; then row r is the gate logit, rows 0..r-1 the down-projection
+    for (int e = threadIdx.x; e < (p.r + 1) * kCdTok; e += kCdThreads) {
+      const uint32_t la = smem_u32(&part[0][0] + e);
+      float pv[kCdMaxCK];
+#pragma unroll
+      for (int q = 0; q < kCdMaxCK; ++q)
+        if (q < CK) pv[q] = dsmem_ld_f32(dsmem_addr(la, (uint32_t)q));
+      float v = 0.0f;
+#pragma unroll
+      for (int q = 0; q < kCdMaxCK; ++q)
+        if (q < CK) v += pv[q];
+      (&part[0][0])[e] = v;
+    }
+  }
+  cluster_sync();                                          // peers are done reading; rank 0's sums in place
+  if (rank == 0) {
+    for (int e = threadIdx.x; e < kCdTok * p.r; e += kCdThreads) {
+      const int m = e / p.r, j = e % p.r;
+      const int tok = tok0 + m;
+      const float gate = 1.0f / (1.0f + expf(-(part[p.r][m] + p.b_g)));
+      const float tv = p.alpha * gate * part[j][m];
+      const __nv_bfloat16 hi = __float2bfloat16_rn(tv);
+      const __nv_bfloat16 lo = __float2bfloat16_rn(tv - __bfloat162float(hi));
+      if (tok < p.M) {
+        p.T2[(size_t)tok * p.t2_cols + j] = hi;
+        p.T2[(size_t)tok * p.t2_cols + p.r + j] = lo;
+      }
     }
   }
 }
@@ -516,6 +564,8 @@ __global__ void __launch_bounds__(256) comp_up_add_kernel(const CompUpParams p) 
 int t2_cols_for(int r) { return 2 * r; }
 size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
 
+// AUTO takes the fused mode: with the clustered down-projection it is the
+// faster one at every measured shape (4-14 % over the plain W4 GEMM).
 int resolve_mode(int mode) { return mode == SPEAR_PREFILL_AUTO ? SPEAR_PREFILL_FUSED : mode; }
 
 // x16: fp16 copy of the activations [M][K].
@@ -557,6 +607,8 @@ int launch_gemm(const spear_w4_layer& L, const __half* x16, int M, void* y, int 
 
 int launch_comp_down(const spear_w4_layer& L, const uint16_t* x, int M, __nv_bfloat16* T2, __half* x16,
                      cudaStream_t st) {
+  DeviceInfo di;
+  if (int rc = device_info(&di)) return rc;
   CompDownParams p{};
   p.x16 = x16;
   p.M = M; p.K = L.K; p.r = L.rank;
@@ -565,13 +617,28 @@ int launch_comp_down(const spear_w4_layer& L, const uint16_t* x, int M, __nv_bfl
   p.w_g = reinterpret_cast<const __nv_bfloat16*>(L.w_g);
   p.b_g = L.b_g; p.alpha = L.alpha;
   p.T2 = T2; p.t2_cols = t2_cols_for(L.rank);
-  const unsigned blocks = (unsigned)((M + kCdTok - 1) / kCdTok);
+  // enough K ranges per token tile for about two CTAs per SM
+  const int tiles = (M + kCdTok - 1) / kCdTok;
+  p.CK = std::max(1, std::min(kCdMaxCK, (2 * di.num_sms + tiles - 1) / tiles));
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3((unsigned)(tiles * p.CK));
+  cfg.blockDim = dim3(kCdThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = st;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = (unsigned)p.CK;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  cudaError_t e;
   switch ((L.rank + 1 + 15) / 16) {
-    case 2: comp_down_kernel<2><<<blocks, kCdThreads, 0, st>>>(p); break;
-    case 3: comp_down_kernel<3><<<blocks, kCdThreads, 0, st>>>(p); break;
-    default: comp_down_kernel<5><<<blocks, kCdThreads, 0, st>>>(p); break;
+    case 2: e = cudaLaunchKernelEx(&cfg, comp_down_kernel<2>, p); break;
+    case 3: e = cudaLaunchKernelEx(&cfg, comp_down_kernel<3>, p); break;
+    default: e = cudaLaunchKernelEx(&cfg, comp_down_kernel<5>, p); break;
   }
-  return cuda_check(cudaGetLastError(), "comp_down launch");
+  return cuda_check(e, "comp_down launch");
 }
 
 int launch_to_fp16(const uint16_t* x, __half* x16, size_t n, cudaStream_t st) {
