@@ -48,16 +48,25 @@ __device__ unsigned g_prefill_status;
 
 using namespace sm100;
 
-constexpr int kBM = 128;                  // tokens per tile (MMA M)
 constexpr int kBN = 256;                  // outputs per tile (MMA N)
 constexpr int kBK = 64;                   // k per stage (one 128-byte swizzle row of bf16)
-constexpr int kStages = 4;
-constexpr int kXBytes = kBM * kBK * 2;    // 16 KB
 constexpr int kWBytes = kBN * kBK * 2;    // 32 KB
 constexpr int kRawBytes = kBN * kBK / 2;  // 8 KB
-constexpr int kStageBytes = kXBytes + kWBytes + kRawBytes;
 constexpr int kGemmThreads = 320;         // warp 0: TMA, warp 1: MMA, warps 2-9: convert + epilogue
-constexpr uint32_t kTmemCols = 512;       // main accumulator in [0, 256), correction in [256, 512)
+constexpr uint32_t kTmemCols = 512;
+
+// BM tokens per tile: 128 (one M = 128 MMA per 16 k; accumulator in TMEM
+// columns [0, 256), the fused correction in [256, 512)) or 256 (two M = 128
+// MMAs per 16 k on the same converted weight tile, accumulators in [0, 256)
+// and [256, 512), the fused correction added into them), which halves the
+// dequantisation work and the int4 traffic per output.
+template <int BM>
+struct TileCfg {
+  static constexpr int kStages = BM == 256 ? 3 : 4;
+  static constexpr int kXBytes = BM * kBK * 2;          // 16 or 32 KB
+  static constexpr int kStageBytes = kXBytes + kWBytes + kRawBytes;
+  static constexpr int kMH = BM / 128;                  // M = 128 MMAs per 16 k
+};
 constexpr uint64_t kWaitNs = 2000ull * 1000 * 1000;   // 2 s: far beyond any legitimate wait
 
 struct GemmParams {
@@ -76,10 +85,13 @@ __device__ __forceinline__ uint32_t sw_layout(int row_bytes) {
   return row_bytes >= 128 ? LAYOUT_SW128 : row_bytes == 64 ? LAYOUT_SW64 : LAYOUT_SW32;
 }
 
+template <int BM>
 __global__ void __launch_bounds__(kGemmThreads, 1)
 w4_gemm_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_wq,
            const __grid_constant__ CUtensorMap tm_t, const __grid_constant__ CUtensorMap tm_b,
            const GemmParams p) {
+  using C = TileCfg<BM>;
+  constexpr int kStages = C::kStages, kXBytes = C::kXBytes, kStageBytes = C::kStageBytes, kMH = C::kMH;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   __shared__ __align__(8) uint64_t bar_full[kStages], bar_cvt[kStages], bar_empty[kStages], bar_acc;
@@ -87,7 +99,7 @@ w4_gemm_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
   __shared__ int s_abort;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int n0 = blockIdx.x * kBN, m0 = blockIdx.y * kBM;
+  const int n0 = blockIdx.x * kBN, m0 = blockIdx.y * BM;
   const int k_stages = p.K / kBK;
   const int total_stages = k_stages + p.comp_stages;
 
@@ -140,7 +152,7 @@ w4_gemm_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
           tma_load_2d(smem_u32(raw_slot(slot)), &tm_wq, s * (kBK / 2), n0, full);
         } else {
           const int j = s - k_stages;   // compensator step: T box j and the factor B
-          mbar_arrive_expect_tx(full, kBM * p.t_row_bytes + kBN * p.b_row_bytes);
+          mbar_arrive_expect_tx(full, BM * p.t_row_bytes + kBN * p.b_row_bytes);
           tma_load_2d(smem_u32(x_slot(slot)), &tm_t, j * 64, m0, full);
           tma_load_2d(smem_u32(w_slot(slot)), &tm_b, 0, n0, full);
         }
@@ -155,8 +167,8 @@ w4_gemm_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
   } else if (warp == 1) {
     // ------------------------------------------------------------- MMA issuer
     if (lane == 0) {
-      const uint32_t idesc = idesc_f16_f32(kBM, kBN);            // fp16 X x fp16 W
-      const uint32_t idesc_comp = idesc_bf16_f32(kBM, kBN);      // bf16 T x bf16 B
+      const uint32_t idesc = idesc_f16_f32(128, kBN);            // fp16 X x fp16 W (M = 128 per MMA)
+      const uint32_t idesc_comp = idesc_bf16_f32(128, kBN);      // bf16 T x bf16 B
       bool ok = true;
       for (int s = 0; s < total_stages && ok; ++s) {
         const int slot = s % kStages;
@@ -169,22 +181,30 @@ w4_gemm_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
         if (s < k_stages) {
 #pragma unroll
           for (int k = 0; k < kBK / 16; ++k) {
-            const uint64_t ad = smem_desc(xa + 32 * k, 1024, LAYOUT_SW128);
             const uint64_t bd = smem_desc(wa + 32 * k, 1024, LAYOUT_SW128);
-            mma_bf16_ss(tmem, ad, bd, idesc, (s > 0 || k > 0) ? 1u : 0u);
+#pragma unroll
+            for (int mh = 0; mh < kMH; ++mh) {                 // token rows 128 mh .. (16 KB apart)
+              const uint64_t ad = smem_desc(xa + mh * 16384 + 32 * k, 1024, LAYOUT_SW128);
+              mma_bf16_ss(tmem + mh * kBN, ad, bd, idesc, (s > 0 || k > 0) ? 1u : 0u);
+            }
           }
         } else {
-          // A = T box j (columns 64j.. of [T_hi | T_lo]); B = the factor B (k = rank);
-          // accumulated into the second accumulator (columns 256..511).
+          // A = T box j (columns 64j.. of [T_hi | T_lo]); B = the factor B (k = rank).
+          // BM = 128: accumulated into the second accumulator (columns 256..511);
+          // BM = 256 (group scales only): added into the main accumulators.
           const int j = s - k_stages;
           const uint32_t a_layout = sw_layout(p.t_row_bytes), b_layout = sw_layout(p.b_row_bytes);
           for (int i = 0; i < p.t_row_bytes / 32; ++i) {
             const int col = 64 * j + 16 * i;                 // column of [T_hi | T_lo]
             if (col >= 2 * p.r) break;
             const int bstep = (col % p.r) / 16;
-            const uint64_t ad = smem_desc(xa + 32 * i, 8 * p.t_row_bytes, a_layout);
             const uint64_t bd = smem_desc(wa + 32 * bstep, 8 * p.b_row_bytes, b_layout);
-            mma_bf16_ss(tmem + kBN, ad, bd, idesc_comp, (j > 0 || i > 0) ? 1u : 0u);
+#pragma unroll
+            for (int mh = 0; mh < kMH; ++mh) {
+              const uint64_t ad = smem_desc(xa + mh * 128 * p.t_row_bytes + 32 * i, 8 * p.t_row_bytes, a_layout);
+              if (kMH == 1) mma_bf16_ss(tmem + kBN, ad, bd, idesc_comp, (j > 0 || i > 0) ? 1u : 0u);
+              else mma_bf16_ss(tmem + mh * kBN, ad, bd, idesc_comp, 1u);
+            }
           }
         }
         mma_commit(smem_u32(&bar_empty[slot]));             // frees the stage when these MMAs finish
@@ -277,12 +297,17 @@ w4_gemm_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
     tc_fence_after();
     if (!s_abort) {
       const int q = warp & 3;
-      const int tok = m0 + 32 * q + lane;
       const int c_begin = ((warp - 2) >> 2) * (kBN / 2);
-      for (int cch = c_begin / 32; cch < (c_begin + kBN / 2) / 32; ++cch) {
+      // BM = 256: the second accumulator (columns 256..) holds tokens 128..255
+      // and the correction is already in both
+      const bool sep_comp = kMH == 1 && p.comp_stages;
+#pragma unroll 1
+      for (int it = 0; it < kMH * (kBN / 2 / 32); ++it) {
+        const int mh = it / (kBN / 2 / 32), cch = c_begin / 32 + it % (kBN / 2 / 32);
+        const int tok = m0 + 128 * mh + 32 * q + lane;
         uint32_t r[32], rc[32];
-        tmem_ld_32cols(tmem + ((uint32_t)(32 * q) << 16) + cch * 32, r);
-        if (p.comp_stages) tmem_ld_32cols(tmem + ((uint32_t)(32 * q) << 16) + kBN + cch * 32, rc);
+        tmem_ld_32cols(tmem + ((uint32_t)(32 * q) << 16) + mh * kBN + cch * 32, r);
+        if (sep_comp) tmem_ld_32cols(tmem + ((uint32_t)(32 * q) << 16) + kBN + cch * 32, rc);
         tmem_ld_wait();
         const int n = n0 + cch * 32;
         if (n >= p.N) continue;
@@ -304,7 +329,7 @@ w4_gemm_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
 #pragma unroll
           for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
         }
-        if (p.comp_stages) {
+        if (sep_comp) {
 #pragma unroll
           for (int i = 0; i < 32; ++i) v[i] += __uint_as_float(rc[i]);
         }
@@ -569,10 +594,20 @@ size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
 int resolve_mode(int mode) { return mode == SPEAR_PREFILL_AUTO ? SPEAR_PREFILL_FUSED : mode; }
 
 // x16: fp16 copy of the activations [M][K].
+// Token count from which a tile takes 256 tokens (two M = 128 MMAs on each
+// converted weight tile); below it the 128-token tiles keep more SMs busy.
+#ifndef SPEAR_PREFILL_BM256_MIN_M
+#define SPEAR_PREFILL_BM256_MIN_M 1024
+#endif
+
 int launch_gemm(const spear_w4_layer& L, const __half* x16, int M, void* y, int out_f32, const __nv_bfloat16* T2,
                 int r_fused, cudaStream_t st) {
+  const bool perch = L.group_size == L.K;
+  // per-channel scales multiply the accumulator in the epilogue, so a fused
+  // correction needs its own accumulator: 128-token tiles
+  const int BM = (M >= SPEAR_PREFILL_BM256_MIN_M && !(perch && r_fused > 0)) ? 256 : 128;
   CUtensorMap tm_x, tm_wq, tm_t, tm_b;
-  if (int rc = make_tmap(&tm_x, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, x16, L.K, M, kBK, kBM,
+  if (int rc = make_tmap(&tm_x, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, x16, L.K, M, kBK, BM,
                          CU_TENSOR_MAP_SWIZZLE_128B)) return rc;
   if (int rc = make_tmap(&tm_wq, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, L.qweight, L.K / 2, L.N, kBK / 2, kBN,
                          CU_TENSOR_MAP_SWIZZLE_NONE)) return rc;
@@ -589,7 +624,7 @@ int launch_gemm(const spear_w4_layer& L, const __half* x16, int M, void* y, int 
     p.t_row_bytes = tbox * 2;
     p.b_row_bytes = r_fused * 2;
     p.comp_stages = (2 * r_fused + 63) / 64;
-    if (int rc = make_tmap(&tm_t, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, T2, tcols, M, tbox, kBM,
+    if (int rc = make_tmap(&tm_t, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, T2, tcols, M, tbox, BM,
                            swizzle_for(p.t_row_bytes))) return rc;
     if (int rc = make_tmap(&tm_b, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, L.B, r_fused, L.N, r_fused, kBN,
                            swizzle_for(p.b_row_bytes))) return rc;
@@ -597,11 +632,13 @@ int launch_gemm(const spear_w4_layer& L, const __half* x16, int M, void* y, int 
     tm_t = tm_x;
     tm_b = tm_x;
   }
-  const size_t smem = (size_t)kStages * kStageBytes + 1024;
-  if (int rc = ensure_smem_limit(reinterpret_cast<const void*>(w4_gemm_tc), smem)) return rc;
-  dim3 grid((L.N + kBN - 1) / kBN, (M + kBM - 1) / kBM);
+  auto fn = BM == 256 ? w4_gemm_tc<256> : w4_gemm_tc<128>;
+  const size_t smem = BM == 256 ? (size_t)TileCfg<256>::kStages * TileCfg<256>::kStageBytes + 1024
+                                : (size_t)TileCfg<128>::kStages * TileCfg<128>::kStageBytes + 1024;
+  if (int rc = ensure_smem_limit(reinterpret_cast<const void*>(fn), smem)) return rc;
+  dim3 grid((L.N + kBN - 1) / kBN, (M + BM - 1) / BM);
   if (grid.y > 65535) return fail(SPEAR_ERR_UNSUPPORTED, "prefill: M=%d too large", M);
-  w4_gemm_tc<<<grid, kGemmThreads, smem, st>>>(tm_x, tm_wq, tm_t, tm_b, p);
+  fn<<<grid, kGemmThreads, smem, st>>>(tm_x, tm_wq, tm_t, tm_b, p);
   return cuda_check(cudaGetLastError(), "prefill gemm launch");
 }
 

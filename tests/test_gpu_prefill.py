@@ -44,6 +44,12 @@ def test_prefill_single_tile_plain(G, sym):
     (768, 1024, 128, False, 32, 300),
     (320, 2048, 128, False, 64, 257),       # ragged N tile (320 = 256 + 64) and ragged M
     (1024, 1024, 1024, True, 32, 512),
+    # 256-token tiles (M >= 1024): ragged last tile, rank 16 / 32 / 64 (64-, 128-byte T rows)
+    (512, 1024, 128, False, 32, 1100),
+    (320, 1024, 128, False, 64, 1280),
+    (256, 1024, 128, True, 16, 1030),
+    (512, 1024, 1024, False, 0, 1300),      # per-channel scales, no compensator: 256-token tiles
+    (256, 1024, 1024, False, 32, 1100),     # per-channel scales with the compensator: 128-token tiles
 ])
 @pytest.mark.parametrize("mode", [FUSED, STREAM])
 def test_prefill_matches_oracle(N, K, G, sym, r, M, mode):
@@ -95,14 +101,16 @@ def test_decode_and_prefill_agree(M):
     assert (yp - yd).abs().max().item() <= 2e-2 * rms
 
 
-def test_prefill_gate_zero_equals_plain():
-    N, K, r, M = 512, 1024, 32, 200
+@pytest.mark.parametrize("M", [200, 1100])
+def test_prefill_gate_zero_equals_plain(M):
+    N, K, r = 512, 1024, 32
     lay, rng = make_layer(N, K, r, seed=46)
     x = make_tokens(rng, M, K)
     L_on = gpu_layer(lay, 128, False, b_g=-1e30)
     y_on = _run(L_on, x, FUSED, 1)
     y_off = _run(L_on.with_comp(False), x, FUSED, 1)
-    # the fused correction adds exact zeros into its own accumulator
+    # the fused correction adds exact zeros (its own accumulator for 128-token
+    # tiles, the main one for 256-token tiles)
     assert torch.equal(y_on, y_off)
 
 
