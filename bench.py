@@ -549,6 +549,31 @@ def run_prefill(torch, spear, device, stream, peaks):
             "cases": out}
 
 
+def profile_prefill_case(spec: str):
+    """One prefill call, repeated, for a profiler to capture (no timing, no JSON):
+    --profile-prefill K,N,M,mode,iters with mode 0 auto, 1 fused, 2 stream, 3 plain."""
+    import torch
+    from quantized_gemm_error_gb300 import spear
+    from quantized_gemm_error_gb300.inputs import make_layer, make_tokens
+    K, N, M, mode, iters = (int(v) for v in spec.split(","))
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(device)
+    spear.load()
+
+    def dev16(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(device)
+
+    lay, rng = make_layer(N, K, RANK, seed=K + N + 1)
+    q, s, z = spear.spear_pack_w4(torch.from_numpy(lay.W).to(device), G, SYM)
+    L = spear.W4Layer(N, K, G, SYM, q, s, z, RANK, dev16(lay.A), dev16(lay.B), dev16(lay.w_g), 0.0, 1.0, mode != 3)
+    x = dev16(make_tokens(rng, M, K, outlier_frac=OUTLIERS))
+    torch.cuda.synchronize()
+    for _ in range(iters):
+        spear.spear_linear_prefill(L, x, mode=spear.PREFILL_FUSED if mode == 3 else mode)
+    torch.cuda.synchronize()
+    print(f"prefill K={K} N={N} M={M} mode={mode} x{iters}: status {spear.spear_get_device_status()}")
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -557,7 +582,12 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile-prefill", metavar="K,N,M,MODE,ITERS", default=None,
+                    help="run one prefill case ITERS times for a profiler and exit")
     args = ap.parse_args()
+    if args.profile_prefill:
+        profile_prefill_case(args.profile_prefill)
+        return
     args.warmup = max(3, args.warmup)
     world, rank, local = dist_setup(args)
     if args.impl == "reference":

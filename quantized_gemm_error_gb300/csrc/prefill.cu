@@ -34,6 +34,7 @@
 #include <cuda.h>
 
 #include <algorithm>
+#include <cstdio>
 #include <mutex>
 
 #include "common.cuh"
@@ -594,18 +595,29 @@ size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
 int resolve_mode(int mode) { return mode == SPEAR_PREFILL_AUTO ? SPEAR_PREFILL_FUSED : mode; }
 
 // x16: fp16 copy of the activations [M][K].
-// Token count from which a tile takes 256 tokens (two M = 128 MMAs on each
-// converted weight tile); below it the 128-token tiles keep more SMs busy.
-#ifndef SPEAR_PREFILL_BM256_MIN_M
-#define SPEAR_PREFILL_BM256_MIN_M 1024
-#endif
+// Tile height: 256 tokens (two M = 128 MMAs on each converted weight tile)
+// where it takes fewer time units than 128-token tiles.  One CTA per SM; a
+// 256-token tile's K loop takes ~1.35x as long as a 128-token one's (measured
+// stage times on GB300), so cost = waves x (1 or 1.35).  Per-channel scales
+// multiply the accumulator in the epilogue, so with a fused correction (its
+// own accumulator) tiles stay at 128 tokens.
+int pick_bm(int M, int N, bool perch_fused, int num_sms) {
+  if (perch_fused) return 128;
+  const long long ntiles = (N + kBN - 1) / kBN;
+  const long long w128 = (ntiles * ((M + 127) / 128) + num_sms - 1) / num_sms;
+  const long long w256 = (ntiles * ((M + 255) / 256) + num_sms - 1) / num_sms;
+  return 135 * w256 < 100 * w128 ? 256 : 128;
+}
 
 int launch_gemm(const spear_w4_layer& L, const __half* x16, int M, void* y, int out_f32, const __nv_bfloat16* T2,
                 int r_fused, cudaStream_t st) {
+  DeviceInfo di;
+  if (int rc = device_info(&di)) return rc;
   const bool perch = L.group_size == L.K;
-  // per-channel scales multiply the accumulator in the epilogue, so a fused
-  // correction needs its own accumulator: 128-token tiles
-  const int BM = (M >= SPEAR_PREFILL_BM256_MIN_M && !(perch && r_fused > 0)) ? 256 : 128;
+  const int BM = pick_bm(M, L.N, perch && r_fused > 0, di.num_sms);
+  if (log_plans())
+    fprintf(stderr, "[spear] prefill gemm N=%d K=%d M=%d G=%d fused_rank=%d: %d-token tiles\n", L.N, L.K, M,
+            L.group_size, r_fused, BM);
   CUtensorMap tm_x, tm_wq, tm_t, tm_b;
   if (int rc = make_tmap(&tm_x, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, x16, L.K, M, kBK, BM,
                          CU_TENSOR_MAP_SWIZZLE_128B)) return rc;

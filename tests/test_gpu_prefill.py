@@ -44,12 +44,15 @@ def test_prefill_single_tile_plain(G, sym):
     (768, 1024, 128, False, 32, 300),
     (320, 2048, 128, False, 64, 257),       # ragged N tile (320 = 256 + 64) and ragged M
     (1024, 1024, 1024, True, 32, 512),
-    # 256-token tiles (M >= 1024): ragged last tile, rank 16 / 32 / 64 (64-, 128-byte T rows)
     (512, 1024, 128, False, 32, 1100),
-    (320, 1024, 128, False, 64, 1280),
-    (256, 1024, 128, True, 16, 1030),
-    (512, 1024, 1024, False, 0, 1300),      # per-channel scales, no compensator: 256-token tiles
-    (256, 1024, 1024, False, 32, 1100),     # per-channel scales with the compensator: 128-token tiles
+    # 256-token tiles (10 column tiles, M ~ 2000: one wave of 256-token tiles
+    # against two of 128-token ones on 152 SMs): ragged last tile, rank 16 /
+    # 32 / 64 (64- and 128-byte T rows)
+    (2560, 512, 128, False, 32, 2000),
+    (2560, 512, 128, False, 64, 1950),
+    (2560, 512, 128, True, 16, 2048),
+    (2560, 512, 512, False, 0, 2000),       # per-channel scales, no compensator: 256-token tiles
+    (2560, 512, 512, False, 32, 2000),      # per-channel scales with the compensator: 128-token tiles
 ])
 @pytest.mark.parametrize("mode", [FUSED, STREAM])
 def test_prefill_matches_oracle(N, K, G, sym, r, M, mode):
@@ -101,9 +104,9 @@ def test_decode_and_prefill_agree(M):
     assert (yp - yd).abs().max().item() <= 2e-2 * rms
 
 
-@pytest.mark.parametrize("M", [200, 1100])
-def test_prefill_gate_zero_equals_plain(M):
-    N, K, r = 512, 1024, 32
+@pytest.mark.parametrize("N,K,M", [(512, 1024, 200), (2560, 512, 2000)])
+def test_prefill_gate_zero_equals_plain(N, K, M):
+    r = 32
     lay, rng = make_layer(N, K, r, seed=46)
     x = make_tokens(rng, M, K)
     L_on = gpu_layer(lay, 128, False, b_g=-1e30)
