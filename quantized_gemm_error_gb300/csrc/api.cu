@@ -49,6 +49,8 @@ int check_layer(const spear_w4_layer* L) {
 }
 }  // namespace
 
+void set_last_error(const char* msg) { snprintf(t_last_error, sizeof(t_last_error), "%s", msg ? msg : ""); }
+
 int fail(int status, const char* fmt, ...) {
   va_list ap;
   va_start(ap, fmt);

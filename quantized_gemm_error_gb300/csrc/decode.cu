@@ -599,6 +599,7 @@ struct Plan {
   size_t smem;
   size_t off_prod, off_T, off_sync, total;
   KernelFn fn;
+  int unsupported;                          // no warp-level plan for this shape (cached)
 };
 
 size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
@@ -685,6 +686,9 @@ int get_plan(const spear_w4_layer& L, int M, Plan* out) {
   for (const Plan& p : cache)
     if (p.device == di.device && p.N == L.N && p.K == L.K && p.G == L.group_size && p.rank == L.rank &&
         p.comp == comp && p.MT == MT && (MT > 1 || p.M == M)) {
+      if (p.unsupported)
+        return fail(SPEAR_ERR_UNSUPPORTED, "decode: N=%d K=%d M=%d needs more shared memory than an SM has",
+                    L.N, L.K, M);
       *out = p;
       return SPEAR_OK;
     }
@@ -692,11 +696,17 @@ int get_plan(const spear_w4_layer& L, int M, Plan* out) {
   // staged tokens when they are small enough to keep two blocks per SM
   // (M <= 8, M K 2 <= 48 KB), else tokens from L1
   const bool try_xs = MT == 1 && xs_smem(M, L.K) <= 48 * 1024;
-  if (build_plan(L, MT, M, comp != 0, try_xs, di, &p) != SPEAR_OK) {
-    if (MT != 1) return SPEAR_ERR_UNSUPPORTED;
-    if (int rc = build_plan(L, MT, M, comp != 0, false, di, &p)) return rc;
-  }
+  int rc = build_plan(L, MT, M, comp != 0, try_xs, di, &p);
+  if (rc != SPEAR_OK && MT == 1) rc = build_plan(L, MT, M, comp != 0, false, di, &p);
   p.device = di.device; p.N = L.N; p.K = L.K; p.G = L.group_size; p.rank = L.rank; p.comp = comp; p.M = M;
+  p.MT = MT;
+  if (rc != SPEAR_OK) {
+    if (rc != SPEAR_ERR_UNSUPPORTED) return rc;
+    p.unsupported = 1;                     // remembered: later calls take the other kernel at once
+    if (cache.size() > 4096) cache.clear();
+    cache.push_back(p);
+    return rc;
+  }
   if (log_plans())
     fprintf(stderr, "[spear] decode plan N=%d K=%d G=%d rank=%d comp=%d M=%d: MT=%d xs=%d Q=%d P=%d max_tiles=%d "
             "smem=%zu\n", L.N, L.K, L.group_size, L.rank, comp, M, p.MT, p.xs, p.Q, p.P, p.max_tiles, p.smem);
@@ -715,10 +725,26 @@ int get_plan(const spear_w4_layer& L, int M, Plan* out) {
 #define SPEAR_TC_MIN_M 33
 #endif
 constexpr int kTcMinM = SPEAR_TC_MIN_M;
-bool use_tc(int M) { return M >= kTcMinM; }
+
+// The warp-level kernel stages the scales, zero points and factor-B rows of
+// all its tiles at once; where that does not fit in shared memory (very wide
+// layers at 17-32 tokens, e.g. 28672 rows at M = 32, one block per SM) the
+// tensor-core kernel, which takes any M <= 64, serves the call.
+bool use_tc(const spear_w4_layer& L, int M) {
+  if (M >= kTcMinM) return true;
+  char saved[512];
+  snprintf(saved, sizeof(saved), "%s", spear_last_error());
+  Plan pl;
+  const int rc = get_plan(L, M, &pl);
+  if (rc == SPEAR_ERR_UNSUPPORTED) {
+    set_last_error(saved);                 // the probe is not this call's failure
+    return true;
+  }
+  return false;
+}
 
 int decode_workspace_bytes(const spear_w4_layer& L, int M, size_t* bytes) {
-  if (use_tc(M)) return decode_tc_workspace_bytes(L, M, bytes);
+  if (use_tc(L, M)) return decode_tc_workspace_bytes(L, M, bytes);
   Plan pl;
   if (int rc = get_plan(L, M, &pl)) return rc;
   *bytes = pl.total;
@@ -727,7 +753,7 @@ int decode_workspace_bytes(const spear_w4_layer& L, int M, size_t* bytes) {
 
 int launch_decode(const spear_w4_layer& L, const uint16_t* x, int M, void* y, int out_f32, void* ws,
                   size_t ws_bytes, cudaStream_t st, bool overlap) {
-  if (use_tc(M)) return launch_decode_tc(L, x, M, y, out_f32, ws, ws_bytes, st, overlap);
+  if (use_tc(L, M)) return launch_decode_tc(L, x, M, y, out_f32, ws, ws_bytes, st, overlap);
   Plan pl;
   if (int rc = get_plan(L, M, &pl)) return rc;
   if (!ws || ws_bytes < pl.total)
@@ -804,7 +830,7 @@ int noalloc_scratch(void** out) {
 int launch_decode_noalloc(const spear_w4_layer& L, const uint16_t* x, int M, void* y, int out_f32,
                           cudaStream_t st) {
   size_t total = 0, sync_bytes = 0;
-  if (use_tc(M)) {
+  if (use_tc(L, M)) {
     if (int rc = decode_tc_workspace_bytes(L, M, &total)) return rc;
     sync_bytes = decode_tc_sync_bytes();
   } else {

@@ -12,6 +12,9 @@ namespace spear {
 
 // Records a thread-local error message and returns `status`.
 int fail(int status, const char* fmt, ...);
+// Puts back a thread-local error message saved earlier (after an internal
+// probe that failed on purpose).
+void set_last_error(const char* msg);
 // Maps a CUDA error to SPEAR_ERR_CUDA with a message (SPEAR_OK if e == cudaSuccess).
 int cuda_check(cudaError_t e, const char* what);
 

@@ -96,6 +96,14 @@ WORKLOADS = {
     "llama7b_prefill_g128_r32": dict(shapes=[(4096, 4096), (4096, 11008), (11008, 4096)], G=128,
                                      sym=False, r=32, decode_M=[], prefill_M=[512, 2048, 8192],
                                      outlier_frac=0.01),
+    # Llama-7B 32-block decoder stack: per block q, k, v, o (4096x4096), gate, up
+    # (4096x11008), down (11008x4096); per-output-channel symmetric int4;
+    # compensators (rank 64) on a layer mask of 4 of the 32 blocks, the other
+    # blocks plain W4; one mixed step = a 1024-token prefill chunk plus 32
+    # decode tokens (1056 tokens on the prefill path, 32 on the decode path)
+    "llama7b_stack_sym_r64": dict(shapes=[(4096, 4096)] * 4 + [(4096, 11008)] * 2 + [(11008, 4096)],
+                                  G=None, sym=True, r=64, blocks=32, masked_blocks=4,
+                                  decode_M=[32], prefill_M=[1056], outlier_frac=0.0),
     # Llama-70B linears, group 128 asymmetric, rank 64
     "llama70b_g128_r64": dict(shapes=[(8192, 8192), (8192, 28672), (28672, 8192)], G=128, sym=False,
                               r=64, decode_M=[1, 8, 32], prefill_M=[256, 512, 1024, 2048, 4096],

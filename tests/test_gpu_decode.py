@@ -35,6 +35,8 @@ def _run(layer, x_bits, out_dtype=0, ws=None):
     (1024, 1024, 1024, True, 16, 1),        # 1024^2 per-channel symmetric, rank 16
     (1024, 1024, 1024, True, 16, 16),
     (512, 2048, 128, False, 32, 9),
+    (512, 1024, 128, False, 32, 24),        # 17-32 tokens: four token tiles per warp
+    (256, 2048, 2048, True, 64, 32),
     (320, 1152, 128, False, 64, 33),
     (256, 1024, 1024, False, 32, 64),
     (1024, 1024, 128, True, 0, 5),          # rank 0: plain W4
