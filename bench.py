@@ -34,9 +34,9 @@ DECODE_M = [1, 4, 16, 64]
 PREFILL_M = [512, 2048, 8192]
 G, SYM, RANK, OUTLIERS = 128, False, 32, 0.01
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-# the library serves decode calls of M >= 33 tokens with its tensor-core kernel
+# the library serves decode calls of M >= 17 tokens with its tensor-core kernel
 # (decode_tc.cu), smaller ones with the warp-level kernel (decode.cu)
-TC_MIN_M = 33
+TC_MIN_M = 17
 DRAM_SUMMARY = os.path.join(ROOT, "profiles", "decode_dram_bytes.json")
 
 
@@ -574,6 +574,59 @@ def profile_prefill_case(spec: str):
     print(f"prefill K={K} N={N} M={M} mode={mode} x{iters}: status {spear.spear_get_device_status()}")
 
 
+def run_stack(args):
+    """The Llama-7B 32-block decoder stack (per-channel symmetric int4; rank-64
+    compensators on the 4 blocks the selection rule picks): one mixed step of
+    chunked prefill (a 1024-token chunk and 32 decode tokens, 1056 tokens
+    through all 224 linears on the prefill path) and the 32 decode tokens
+    alone on the decode path, each one CUDA graph.  Weights (3.2 GB of int4)
+    exceed L2, so every replay streams them from HBM."""
+    import torch
+    from quantized_gemm_error_gb300 import spear
+    from quantized_gemm_error_gb300.stack import StackStep, build_stack, select_blocks
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(device)
+    spear.load()
+    spear.spear_set_launch_overlap(True)
+    wl = __import__("quantized_gemm_error_gb300.inputs", fromlist=["workload"]).workload("llama7b_stack_sym_r64")
+    mask, ranks = select_blocks(wl["blocks"], wl["masked_blocks"], wl["r"], seed=0)
+    layers = build_stack(ranks, device, seed=0, recipe="device")
+    step = StackStep(layers, wl["prefill_M"][0], wl["decode_M"][0], device, seed=0)
+    step.capture()
+    peaks, _ = load_peaks()
+    out = {}
+    for name in ("prefill", "decode"):
+        for _ in range(args.warmup):
+            step.replay(name)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(step.stream)
+        for _ in range(args.steps):
+            step.replay(name)
+        e1.record(step.stream)
+        torch.cuda.synchronize()
+        out[name] = e0.elapsed_time(e1) / args.steps            # ms per pass
+    status = spear.spear_get_device_status()
+    tp, td = out["prefill"] / 1e3, out["decode"] / 1e3
+    line = {
+        "metric": "decoder-stack mixed step tokens/s (1056 tokens x 224 linears, prefill path)",
+        "value": round(step.Mp / tp, 1), "unit": "tokens/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(out["prefill"], 4), "higher_is_better": True,
+        "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "llama7b_stack_sym_r64", "blocks": wl["blocks"], "linears": len(layers),
+                   "compensated_blocks": [int(b) for b in np.flatnonzero(mask)], "rank": wl["r"],
+                   "prefill_M": step.Mp, "decode_M": step.Md, "launch": "cuda-graph",
+                   "l2": "3.2 GB of int4 weights stream from HBM every pass"},
+        "prefill_path": {"TFLOP_s": round(step.prefill_flops() / tp / 1e12, 1),
+                         "frac_bf16_burst": round(step.prefill_flops() / tp / 1e12 / peaks["bf16_tflops"], 4)},
+        "decode_path": {"ms": round(out["decode"], 4), "tokens_s": round(step.Md / td, 1),
+                        "GB_s": round(step.decode_bytes() / td / 1e9, 1),
+                        "frac_hbm": round(step.decode_bytes() / td / 1e9 / peaks["hbm_gbs"], 4)},
+        "gpu_launches": None, "status": status,
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -584,9 +637,16 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--profile-prefill", metavar="K,N,M,MODE,ITERS", default=None,
                     help="run one prefill case ITERS times for a profiler and exit")
+    ap.add_argument("--stack", action="store_true",
+                    help="time the 32-block decoder stack (mixed prefill step and decode step) instead")
     args = ap.parse_args()
     if args.profile_prefill:
         profile_prefill_case(args.profile_prefill)
+        return
+    if args.stack:
+        args.warmup = max(3, min(args.warmup, 10))
+        args.steps = min(args.steps, 50)
+        run_stack(args)
         return
     args.warmup = max(3, args.warmup)
     world, rank, local = dist_setup(args)

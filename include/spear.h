@@ -120,15 +120,17 @@ spear_status spear_pack_w4(const float* W, int N, int K, int group_size, int sym
  * streams the int4 weights, computes g(x) and A x for every token in the same
  * launch and adds alpha*g*B(Ax) in the epilogue.  1 <= M <= 64.
  *   x : device bf16 [M][K];  y : device [M][N], bf16 or fp32 (out_dtype).
- * M <= 32 runs on warp-level MMAs; M >= 33 on the tcgen05 tensor cores.
+ * M <= 16 runs on warp-level MMAs; M >= 17 on the tcgen05 tensor cores.
  * The thread blocks of the launch exchange the M x (rank+1) down-projection
  * through `workspace` (device, at least spear_decode_workspace_bytes()).
  * The workspace must be zeroed once before its first use
  * (spear_workspace_init) and is left ready for the next call; two calls that
  * run at the same time must not share one.  After a SPEAR_ERR_TIMEOUT device
  * status, zero it again.
+ * Every block of a launch stays resident at once; a shape too wide for that
+ * (e.g. N = 131072 at 12 tokens) returns SPEAR_ERR_UNSUPPORTED.
  * Some launches carry the activations in fp16 (M <= 8 with M*K*2 <= 48 KB,
- * and M >= 33): there |x| must stay below 65504; a larger value is reported
+ * and M >= 17): there |x| must stay below 65504; a larger value is reported
  * as SPEAR_ERR_INVALID_ARG through spear_get_device_status.
  */
 spear_status spear_decode_workspace_bytes(const spear_w4_layer* L, int M, size_t* bytes);

@@ -584,12 +584,12 @@ KernelFn pick(int MT, bool comp, bool perch, bool xs) {
   switch (MT) {
     case 1: return xs ? pick_kernel<1, true>(comp, perch) : pick_kernel<1, false>(comp, perch);
     case 2: return pick_kernel<2, false>(comp, perch);
-    case 4: return pick_kernel<4, false>(comp, perch);
-    default: return pick_kernel<8, false>(comp, perch);
+    default: return pick_kernel<2, false>(comp, perch);
   }
 }
 
-int mt_for(int M) { return M <= 8 ? 1 : M <= 16 ? 2 : M <= 32 ? 4 : 8; }
+// (1-16 tokens: every larger count goes to the tensor-core kernel)
+int mt_for(int M) { return M <= 8 ? 1 : 2; }
 
 // Host-side plan: block counts, the tile split and the workspace layout.
 struct Plan {
@@ -720,16 +720,18 @@ int get_plan(const spear_w4_layer& L, int M, Plan* out) {
 
 // Token counts from which the tensor-core kernel (decode_tc.cu) serves the
 // call: from there on its MMA throughput beats the warp-level MMAs below,
-// whose token fragments are reloaded for every 16 weight rows.
+// whose token fragments are reloaded for every 16 weight rows (measured on
+// the Llama-7B shapes: at 24 and 32 tokens the tensor-core kernel takes
+// 0.6-0.8x the time, at 16 tokens the warp-level one wins).
 #ifndef SPEAR_TC_MIN_M
-#define SPEAR_TC_MIN_M 33
+#define SPEAR_TC_MIN_M 17
 #endif
 constexpr int kTcMinM = SPEAR_TC_MIN_M;
 
 // The warp-level kernel stages the scales, zero points and factor-B rows of
-// all its tiles at once; where that does not fit in shared memory (very wide
-// layers at 17-32 tokens, e.g. 28672 rows at M = 32, one block per SM) the
-// tensor-core kernel, which takes any M <= 64, serves the call.
+// all its tiles at once; where that does not fit in shared memory (layers so
+// wide that a block owns too many 16-row tiles) the tensor-core kernel, which
+// takes any M <= 64, serves the call.
 bool use_tc(const spear_w4_layer& L, int M) {
   if (M >= kTcMinM) return true;
   char saved[512];

@@ -2,8 +2,8 @@
 // the 5th-generation tensor cores, one launch per layer (SPEAR explainer,
 // Technical Summary 2.2 A: in the memory-bound decode phase the compensator
 // runs inside the low-bit GEMM's launch).  Serves the larger token counts
-// (33..64), where the per-weight arithmetic outgrows the warp-level MMAs of
-// decode.cu.
+// (17..64), where the per-weight arithmetic outgrows the warp-level MMAs of
+// decode.cu, and the wide layers whose warp-level plan does not fit.
 //
 //   y[m][n] = sum_k (u[n][k] - z[n][g]) s[n][g] x[m][k]  +  sum_j B[n][j] T[m][j]
 //   T[m][j] = alpha g_m (A x_m)[j],   g_m = sigmoid(w_g . x_m + b_g)
@@ -34,7 +34,7 @@
 // Shared memory carries every weight several times (int4 in, fp16 out, fp16
 // read by the tensor core: ~10 bytes per int4 byte), which bounds this kernel
 // near a quarter of what an SM draws from HBM; decode.cu's register path does
-// not have that cost and serves M <= 32.
+// not have that cost and serves M <= 16.
 #include <cuda.h>
 
 #include <algorithm>

@@ -35,7 +35,7 @@ def _run(layer, x_bits, out_dtype=0, ws=None):
     (1024, 1024, 1024, True, 16, 1),        # 1024^2 per-channel symmetric, rank 16
     (1024, 1024, 1024, True, 16, 16),
     (512, 2048, 128, False, 32, 9),
-    (512, 1024, 128, False, 32, 24),        # 17-32 tokens: four token tiles per warp
+    (512, 1024, 128, False, 32, 24),        # 17-32 tokens: tensor-core kernel, 32 token rows
     (256, 2048, 2048, True, 64, 32),
     (320, 1152, 128, False, 64, 33),
     (256, 1024, 1024, False, 32, 64),
@@ -61,6 +61,24 @@ def test_decode_llama7b_shapes_sampled(N, K, M):
     ref = oracle.linear(oracle_layer(lay, 128, False), x, n_idx=cols, nthreads=8)
     y = _run(L, x)
     check_close(y[:, torch.from_numpy(cols).cuda()], ref)
+
+
+def test_decode_very_wide_layer():
+    """131072 output rows x 128.  One token runs (a warp-level block owns ~56
+    16-row tiles, one block per SM).  At 12 tokens neither kernel can keep all
+    its blocks resident (the warp-level plan outgrows shared memory; the
+    tensor-core kernel would need 512 co-resident tile clusters), and the call
+    says so instead of launching."""
+    from quantized_gemm_error_gb300 import spear
+    N, K, r = 131072, 128, 64
+    lay, rng = make_layer(N, K, r, seed=24)
+    L = gpu_layer(lay, 128, False)
+    x = make_tokens(rng, 1, K, outlier_frac=0.01)
+    ref = oracle.linear(oracle_layer(lay, 128, False), x, nthreads=8)
+    check_close(_run(L, x), ref)
+    with pytest.raises(spear.SpearError) as e:
+        _run(L, make_tokens(rng, 12, K))
+    assert spear.STATUS_NAMES[e.value.status] == "SPEAR_ERR_UNSUPPORTED"
 
 
 def test_correction_term_alone():

@@ -1,7 +1,7 @@
 """Overlapped decode launches (spear_set_launch_overlap): a chain of decode
 calls in which every call reads the previous call's output must give the same
 bits with and without overlap, eagerly and inside a captured CUDA graph, on
-both decode kernels (M <= 32 and M >= 33)."""
+both decode kernels (M <= 16 and M >= 17)."""
 import pytest
 import torch
 
