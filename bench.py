@@ -382,15 +382,25 @@ def run_ours(args, world, rank, local):
     # per-call breakdown: for each call of the step, one graph holding that
     # call on every weight copy (consecutive launches overlap as in the step);
     # comp on vs off
+    # the pages' vector gate (hidden width 8 on the rank-32 code) on the same
+    # weights, against the task's scalar gate and the plain layer
+    import dataclasses
+    gen = torch.Generator(device=device)
+    gen.manual_seed(0)
+    vg = dict(gate_w1=torch.randn(8, RANK, generator=gen, device=device) * (3.0 / RANK ** 0.5),
+              gate_c1=torch.randn(8, generator=gen, device=device) * 0.1,
+              gate_w2=torch.randn(RANK, 8, generator=gen, device=device) / 8 ** 0.5,
+              gate_c2=torch.randn(RANK, generator=gen, device=device))
     cases = []
     for (K, N, M) in calls:
         res = {}
-        for comp in (True, False):
+        for comp in (True, False, "vector"):
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, stream=stream):
                 for cp in range(ncopy):
                     L = [l for (k, n, l, _) in copies[cp] if (k, n) == (K, N)][0]
-                    Lc = L if comp else L.with_comp(False)
+                    Lc = (L if comp is True else L.with_comp(False) if comp is False
+                          else dataclasses.replace(L, w_g=None, **vg))
                     spear.spear_linear_decode(Lc, xs_dev[(K, M)], y=ys[(N, M)], workspace=ws, stream=stream)
             reps = 20
             g.replay()
@@ -408,7 +418,9 @@ def run_ours(args, world, rank, local):
                       "GB_s": round(gbs, 1),
                       "frac_hbm_measured": round(gbs / peaks["hbm_gbs"], 4),
                       "frac_hbm_8000": round(gbs / 8000.0, 4),
-                      "plain_us": round(res[False], 3), "comp_overhead": round(res[True] / res[False] - 1, 4)})
+                      "plain_us": round(res[False], 3), "comp_overhead": round(res[True] / res[False] - 1, 4),
+                      "vector_gate_us": round(res["vector"], 3),
+                      "vector_gate_overhead": round(res["vector"] / res[False] - 1, 4)})
     tot_on = sum(c["us"] for c in cases)
     tot_off = sum(c["plain_us"] for c in cases)
 
@@ -481,6 +493,7 @@ def run_ours(args, world, rank, local):
             "gpu_launches": args.steps * len(calls),
             "clocks": clk.summary(),
             "comp_overhead_step": round(tot_on / tot_off - 1, 4),
+            "vector_gate_overhead_step": round(sum(c["vector_gate_us"] for c in cases) / tot_off - 1, 4),
             "decode_cases": cases,
             "prefill": prefill,
         }

@@ -92,6 +92,19 @@ typedef struct spear_w4_layer {
   const uint16_t* w_g;
   float b_g, alpha;
   int comp_enabled;
+  /* The pages' vector gate (Technical Summary 2.1 A: B diag(gamma(A x)) A,
+   * gamma a bottleneck MLP), used when gate_hidden > 0:
+   *   t = A x,  gamma(t) = sigmoid(gate_w2 relu(gate_w1 t + gate_c1) + gate_c2),
+   *   correction = alpha B (gamma(t) * t)   (elementwise product, per token);
+   * device fp32 arrays gate_w1 [gate_hidden][rank], gate_c1 [gate_hidden],
+   * gate_w2 [rank][gate_hidden], gate_c2 [rank]; 1 <= gate_hidden <= 32.
+   * w_g and b_g are then unused (w_g may be NULL).  gate_hidden = 0 selects
+   * the scalar gate g = sigmoid(w_g . x + b_g) and leaves these unread. */
+  int gate_hidden;
+  const float* gate_w1;
+  const float* gate_c1;
+  const float* gate_w2;
+  const float* gate_c2;
 } spear_w4_layer;
 
 /* Byte sizes of the three packed buffers for an N x K weight. */

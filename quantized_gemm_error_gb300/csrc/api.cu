@@ -38,11 +38,16 @@ int check_layer(const spear_w4_layer* L) {
   if (!aligned16(L->qweight) || !aligned16(L->scales) || (L->zeros && !aligned16(L->zeros)))
     return fail(SPEAR_ERR_INVALID_ARG, "layer buffers must be 16-byte aligned");
   if (!rank_ok(L->rank)) return fail(SPEAR_ERR_INVALID_ARG, "rank=%d must be 0, 16, 32 or 64", L->rank);
+  if (L->gate_hidden < 0 || L->gate_hidden > 32)
+    return fail(SPEAR_ERR_INVALID_ARG, "gate_hidden=%d must be in [0, 32]", L->gate_hidden);
   if (L->comp_enabled && L->rank > 0) {
-    if (!L->A || !L->B || !L->w_g) return fail(SPEAR_ERR_INVALID_ARG, "compensator buffers are NULL");
-    if (!aligned16(L->A) || !aligned16(L->B) || !aligned16(L->w_g))
+    const bool vec = L->gate_hidden > 0;
+    if (!L->A || !L->B || (!vec && !L->w_g)) return fail(SPEAR_ERR_INVALID_ARG, "compensator buffers are NULL");
+    if (!aligned16(L->A) || !aligned16(L->B) || (L->w_g && !aligned16(L->w_g)))
       return fail(SPEAR_ERR_INVALID_ARG, "compensator buffers must be 16-byte aligned");
-    if (!std::isfinite(L->alpha) || std::isnan(L->b_g))
+    if (vec && (!L->gate_w1 || !L->gate_c1 || !L->gate_w2 || !L->gate_c2))
+      return fail(SPEAR_ERR_INVALID_ARG, "vector-gate buffers are NULL");
+    if (!std::isfinite(L->alpha) || (!vec && std::isnan(L->b_g)))
       return fail(SPEAR_ERR_INVALID_ARG, "alpha must be finite and b_g not NaN");
   }
   return SPEAR_OK;

@@ -138,4 +138,56 @@ __device__ __forceinline__ void nibbles_to_bf16x2_biased(uint32_t w, uint32_t (&
   for (int i = 0; i < 4; ++i) out[i] = ((w >> (4 * i)) & 0x000F000Fu) | 0x43004300u;
 }
 
+// The vector gate (Technical Summary 2.1 A: gamma is a bottleneck MLP on the
+// rank-r code t = A x), for ntok tokens at once, in two phases with a barrier
+// of the calling threads [tid0, tid0 + nthreads) between and after them:
+//   vector_gate_hidden:  hid[m][i] = relu(c1[i] + sum_j W1s[i][j] t[m][j])   [ntok][h]
+//   vector_gate_apply:   t[m][j] *= sigmoid(c2[j] + sum_i W2s[j][i] hid[m][i])
+// t[m][j] sits at t[m * tm + j * tj] (shared memory); W1s [h][r] and W2s
+// [r][h] are staged in shared memory (stage_gate_weights); c1 [h], c2 [r] are
+// fp32 in global memory.  fp32 accumulation in index order; every (token,
+// unit) pair belongs to one thread, so apply may overwrite t in place.
+__device__ __forceinline__ void vector_gate_hidden(const float* t, int tm, int tj, int ntok, int r, int h,
+                                                   const float* W1s, const float* c1, float* hid, int tid,
+                                                   int nthreads) {
+  for (int e = tid; e < ntok * h; e += nthreads) {
+    const int m = e / h, i = e % h;
+    float acc = __ldg(c1 + i);
+    for (int j = 0; j < r; ++j) acc = fmaf(W1s[i * r + j], t[m * tm + j * tj], acc);
+    hid[e] = fmaxf(acc, 0.0f);
+  }
+}
+__device__ __forceinline__ void vector_gate_apply(float* t, int tm, int tj, int ntok, int r, int h,
+                                                  const float* W2s, const float* c2, const float* hid, int tid,
+                                                  int nthreads) {
+  for (int e = tid; e < ntok * r; e += nthreads) {
+    const int m = e / r, j = e % r;
+    float acc = __ldg(c2 + j);
+    for (int i = 0; i < h; ++i) acc = fmaf(W2s[j * h + i], hid[m * h + i], acc);
+    t[m * tm + j * tj] *= 1.0f / (1.0f + expf(-acc));
+  }
+}
+
+// Copies the gate's W1 [h][r] and W2 [r][h] (fp32, global) into shared memory
+// with threads [tid0, tid0 + nthreads) of the block, eight loads in flight per
+// thread; the caller synchronises those threads afterwards.
+__device__ __forceinline__ void stage_gate_weights(const float* W1, const float* W2, int r, int h, float* W1s,
+                                                   float* W2s, int tid, int nthreads) {
+  const int n = h * r;
+  for (int e0 = 0; e0 < 2 * n; e0 += 8 * nthreads) {
+    float v[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int e = e0 + tid + i * nthreads;
+      v[i] = e < n ? __ldg(W1 + e) : e < 2 * n ? __ldg(W2 + (e - n)) : 0.0f;
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int e = e0 + tid + i * nthreads;
+      if (e < n) W1s[e] = v[i];
+      else if (e < 2 * n) W2s[e - n] = v[i];
+    }
+  }
+}
+
 }  // namespace spear

@@ -62,6 +62,8 @@ struct DecodeParams {
   const __nv_bfloat16* B;
   const __nv_bfloat16* w_g;
   float b_g, alpha;
+  int gh;                   // vector-gate hidden width (0: the scalar gate)
+  const float *gw1, *gc1, *gw2, *gc2;
   // work split
   int Q, P;                 // producer / streamer blocks
   int tiles, nchunks;       // N/16, K/128
@@ -184,13 +186,32 @@ __device__ void producer_block(const DecodeParams& p, float* smem) {
     for (int ss = 0; ss < kMaxSlices; ++ss) v += part[ss];
     return v;
   };
-  float* gate = smem;                                   // [Mpad]
-  for (int m = threadIdx.x; m < Mpad; m += kThreads) gate[m] = 1.0f / (1.0f + expf(-(slice_sum(m, p.r) + p.b_g)));
-  __syncthreads();
-  for (int e = threadIdx.x; e < Mpad * p.r; e += kThreads) {
-    const int m = e / p.r, j = e % p.r;
-    const float v = slice_sum(m, j);
-    p.ws_T[e] = (m < p.M) ? p.alpha * gate[m] * v : 0.0f;
+  if (p.gh > 0) {
+    // vector gate: t [Mpad][r] into shared memory, then one warp per token
+    // forms gamma(t) and T = alpha gamma(t) t
+    float* ts = smem;                                   // [Mpad][r]
+    float* hs = ts + Mpad * p.r;                        // [Mpad][h] hidden units
+    float* w1s = hs + Mpad * p.gh;                      // [h][r]
+    float* w2s = w1s + p.gh * p.r;                      // [r][h]
+    stage_gate_weights(p.gw1, p.gw2, p.r, p.gh, w1s, w2s, threadIdx.x, kThreads);
+    for (int e = threadIdx.x; e < Mpad * p.r; e += kThreads) ts[e] = slice_sum(e / p.r, e % p.r);
+    __syncthreads();
+    vector_gate_hidden(ts, p.r, 1, Mpad, p.r, p.gh, w1s, p.gc1, hs, threadIdx.x, kThreads);
+    __syncthreads();
+    vector_gate_apply(ts, p.r, 1, Mpad, p.r, p.gh, w2s, p.gc2, hs, threadIdx.x, kThreads);
+    __syncthreads();
+    for (int e = threadIdx.x; e < Mpad * p.r; e += kThreads)
+      p.ws_T[e] = (e / p.r < p.M) ? p.alpha * ts[e] : 0.0f;
+  } else {
+    float* gate = smem;                                 // [Mpad]
+    for (int m = threadIdx.x; m < Mpad; m += kThreads)
+      gate[m] = 1.0f / (1.0f + expf(-(slice_sum(m, p.r) + p.b_g)));
+    __syncthreads();
+    for (int e = threadIdx.x; e < Mpad * p.r; e += kThreads) {
+      const int m = e / p.r, j = e % p.r;
+      const float v = slice_sum(m, j);
+      p.ws_T[e] = (m < p.M) ? p.alpha * gate[m] * v : 0.0f;
+    }
   }
   __threadfence();
   __syncthreads();
@@ -651,7 +672,9 @@ int build_plan(const spear_w4_layer& L, int MT, int M, bool comp, bool try_xs, c
     if (pl->max_tiles > 64) return fail(SPEAR_ERR_UNSUPPORTED, "decode: too many tiles per block");
     pl->smem = std::max(streamer_smem(pl->MT, has_rank, pl->max_tiles, pl->ng, L.rank, extra),
                         (size_t)kWarps * pl->MT * 128 * 4);
-    if (pl->smem > di.smem_optin)
+    cudaFuncAttributes fa{};
+    if (cudaFuncGetAttributes(&fa, pl->fn) != cudaSuccess) return fail(SPEAR_ERR_CUDA, "decode: cudaFuncGetAttributes failed");
+    if (pl->smem + fa.sharedSizeBytes > di.smem_optin)
       return fail(SPEAR_ERR_UNSUPPORTED, "decode: shape needs %zu B of shared memory", pl->smem);
     if (int rc = ensure_smem_limit(reinterpret_cast<const void*>(pl->fn), pl->smem)) return rc;
     int per_sm = 0;
@@ -774,6 +797,7 @@ int launch_decode(const spear_w4_layer& L, const uint16_t* x, int M, void* y, in
   p.B = reinterpret_cast<const __nv_bfloat16*>(L.B);
   p.w_g = reinterpret_cast<const __nv_bfloat16*>(L.w_g);
   p.b_g = L.b_g; p.alpha = L.alpha;
+  p.gh = L.gate_hidden; p.gw1 = L.gate_w1; p.gc1 = L.gate_c1; p.gw2 = L.gate_w2; p.gc2 = L.gate_c2;
   p.Q = pl.Q; p.P = pl.P; p.tiles = pl.tiles; p.nchunks = pl.nchunks;
   p.max_tiles = pl.max_tiles; p.ng = pl.ng;
   char* base = reinterpret_cast<char*>(ws);

@@ -90,6 +90,8 @@ struct TcParams {
   const __nv_bfloat16* B;
   const __nv_bfloat16* w_g;
   float b_g, alpha;
+  int gh;                   // vector-gate hidden width (0: the scalar gate)
+  const float *gw1, *gc1, *gw2, *gc2;
   float* ws_part;           // [Kp][RT][16][NP] producer-cluster partials
   float* ws_P;              // [NP][r + 1]: (A x)[j] for j < r, w_g . x at j = r
   unsigned* ws_sync;        // [0] producer row tiles published, [1] tile-CTA ticket, [2 + rt] Kp tickets
@@ -588,7 +590,49 @@ __device__ void tc_tile(const CUtensorMap* tm_w, const CUtensorMap* tm_x, const 
       const int rp = p.r + 1, half_r = p.r / 2;
       const bool pok = s_pok != 0;
       constexpr int kPer = 8;                              // pairs per thread and pass (r <= 32: one pass)
-      for (int e0 = 0; e0 < NP * half_r; e0 += kPer * kXWarps * 32) {
+      if (p.gh > 0) {
+        // vector gate: once the MMAs are done the second fp16 weight slot is
+        // scratch for t [NP][r]; one warp per token forms gamma(t), then
+        // T = alpha gamma(t) t as bf16 hi + lo
+        bool vok = mbar_wait(smem_u32(&acc_full), 0, kPipeWaitNs);
+        vok = __all_sync(0xffffffffu, vok && !s_abort);
+        if (!vok) give_up(&s_abort);
+        // slot 1 holds t [NP][r] and the staged W1 [h][r], W2 [r][h] (<= 32 KB
+        // for r <= 64, h <= 32); hidden units and the gate in static memory
+        float* ts = reinterpret_cast<float*>(bf_ring + kBfBytes);       // [NP][r]
+        float* w1s = ts + NP * p.r;
+        float* w2s = w1s + p.gh * p.r;
+        __shared__ float hs[NP * 32];                                    // [NP][h] hidden units
+        stage_gate_weights(p.gw1, p.gw2, p.r, p.gh, w1s, w2s, tid, kXWarps * 32);
+        for (int e0 = 0; e0 < NP * p.r; e0 += kPer * kXWarps * 32) {
+          float v[kPer];
+#pragma unroll
+          for (int i = 0; i < kPer; ++i) {
+            const int e = e0 + tid + i * kXWarps * 32;
+            v[i] = (pok && e < NP * p.r) ? __ldcg(p.ws_P + (size_t)(e / p.r) * rp + e % p.r) : 0.0f;
+          }
+#pragma unroll
+          for (int i = 0; i < kPer; ++i) {
+            const int e = e0 + tid + i * kXWarps * 32;
+            if (e < NP * p.r) ts[e] = v[i];
+          }
+        }
+        named_sync(1, kXWarps * 32);
+        vector_gate_hidden(ts, p.r, 1, NP, p.r, p.gh, w1s, p.gc1, hs, tid, kXWarps * 32);
+        named_sync(1, kXWarps * 32);
+        vector_gate_apply(ts, p.r, 1, NP, p.r, p.gh, w2s, p.gc2, hs, tid, kXWarps * 32);
+        named_sync(1, kXWarps * 32);
+        for (int e = tid; e < NP * half_r; e += kXWarps * 32) {
+          const int m = e / half_r, jj = e % half_r;
+          const bool on = pok && m < p.M;
+          const float ta = on ? p.alpha * ts[m * p.r + 2 * jj] : 0.0f;
+          const float tb = on ? p.alpha * ts[m * p.r + 2 * jj + 1] : 0.0f;
+          const float ha = __bfloat162float(__float2bfloat16_rn(ta)), hb = __bfloat162float(__float2bfloat16_rn(tb));
+          th_s[e] = pack_bf16x2(ha, hb);
+          tl_s[e] = pack_bf16x2(ta - ha, tb - hb);
+        }
+      }
+      for (int e0 = 0; p.gh == 0 && e0 < NP * half_r; e0 += kPer * kXWarps * 32) {
         float pa[kPer], pb[kPer], pg[kPer];
 #pragma unroll
         for (int i = 0; i < kPer; ++i) {
@@ -785,6 +829,10 @@ int build_tc_plan(const spear_w4_layer& L, int NP, bool comp, const DeviceInfo& 
 
   // Producer smem: [NW][MT][4][32] + [16][NP] floats
   const size_t prod_smem = ((size_t)(kThreads / 32) * (NP / 8) * 128 + 16 * NP) * 4 + 1024;
+  // the dynamic shared memory a CTA may take next to the kernel's static arrays
+  cudaFuncAttributes fa{};
+  if (cudaFuncGetAttributes(&fa, pl->fn) != cudaSuccess) return fail(SPEAR_ERR_CUDA, "decode: cudaFuncGetAttributes failed");
+  const size_t smem_limit = di.smem_optin > fa.sharedSizeBytes ? di.smem_optin - fa.sharedSizeBytes : 0;
 
   int best_cost = INT32_MAX;
   TcPlan best{};
@@ -798,12 +846,12 @@ int build_tc_plan(const spear_w4_layer& L, int NP, bool comp, const DeviceInfo& 
     // three fp16 weight steps in flight when they fit, else two
     c.BF = kMaxBfStages;
     size_t sm = tile_smem(NP, c.BF, nr_max, L.rank, &c);
-    if (sm > di.smem_optin) {
+    if (sm > smem_limit) {
       c.BF = 2;
       sm = tile_smem(NP, c.BF, nr_max, L.rank, &c);
     }
     c.smem = std::max(sm, prod_smem);
-    if (c.smem > di.smem_optin) continue;
+    if (c.smem > smem_limit) continue;
     // all of the unified L1 / shared-memory array as shared memory (one CTA
     // per SM holds up to ~220 KB of rings)
     if (int rc = ensure_smem_limit(reinterpret_cast<const void*>(c.fn), c.smem)) return rc;
@@ -923,6 +971,7 @@ int launch_decode_tc(const spear_w4_layer& L, const uint16_t* x, int M, void* y,
   p.B = reinterpret_cast<const __nv_bfloat16*>(L.B);
   p.w_g = reinterpret_cast<const __nv_bfloat16*>(L.w_g);
   p.b_g = L.b_g; p.alpha = L.alpha;
+  p.gh = L.gate_hidden; p.gw1 = L.gate_w1; p.gc1 = L.gate_c1; p.gw2 = L.gate_w2; p.gc2 = L.gate_c2;
   char* base = reinterpret_cast<char*>(ws);
   p.ws_sync = reinterpret_cast<unsigned*>(base + pl.off_sync);
   p.ws_part = reinterpret_cast<float*>(base + pl.off_part);

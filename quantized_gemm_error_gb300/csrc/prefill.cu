@@ -376,6 +376,8 @@ struct CompDownParams {
   const __nv_bfloat16* A;
   const __nv_bfloat16* w_g;
   float b_g, alpha;
+  int gh;               // vector-gate hidden width (0: the scalar gate)
+  const float *gw1, *gc1, *gw2, *gc2;
   __nv_bfloat16* T2;    // [M][t2_cols]: T_hi in [0, r), T_lo in [r, 2r)
   int t2_cols;
   __half* x16;          // optional [M][K] fp16 copy of x for the GEMM (NULL: not written)
@@ -438,12 +440,13 @@ __global__ void __launch_bounds__(kCdThreads) comp_down_kernel(const CompDownPar
 #pragma unroll
       for (int rt = 0; rt < RT; ++rt) {
         const int rlo = rt * 16 + g, rhi = rlo + 8;
+        // (row r is w_g . x for the scalar gate; with the vector gate w_g may be NULL)
         va[u][rt] = !ok ? make_uint4(0, 0, 0, 0)
                         : rlo < p.r ? ldg16(p.A + (size_t)rlo * p.K + kb)
-                                    : rlo == p.r ? ldg16(p.w_g + kb) : make_uint4(0, 0, 0, 0);
+                                    : (rlo == p.r && p.w_g) ? ldg16(p.w_g + kb) : make_uint4(0, 0, 0, 0);
         vb[u][rt] = !ok ? make_uint4(0, 0, 0, 0)
                         : rhi < p.r ? ldg16(p.A + (size_t)rhi * p.K + kb)
-                                    : rhi == p.r ? ldg16(p.w_g + kb) : make_uint4(0, 0, 0, 0);
+                                    : (rhi == p.r && p.w_g) ? ldg16(p.w_g + kb) : make_uint4(0, 0, 0, 0);
       }
     }
 #pragma unroll
@@ -503,11 +506,22 @@ __global__ void __launch_bounds__(kCdThreads) comp_down_kernel(const CompDownPar
     }
   }
   cluster_sync();                                          // peers are done reading; rank 0's sums in place
+  __shared__ float hid[kCdTok * 32];                       // [16 tokens][h]
+  __shared__ float gw1s[32 * 64], gw2s[64 * 32];           // the gate's W1, W2 (h <= 32, r <= 64)
+  if (rank == 0 && p.gh > 0) {
+    // vector gate on the summed partial (part[j][m]): t scaled in place by gamma(t)
+    stage_gate_weights(p.gw1, p.gw2, p.r, p.gh, gw1s, gw2s, threadIdx.x, kCdThreads);
+    __syncthreads();
+    vector_gate_hidden(&part[0][0], 1, kCdTok, kCdTok, p.r, p.gh, gw1s, p.gc1, hid, threadIdx.x, kCdThreads);
+    __syncthreads();
+    vector_gate_apply(&part[0][0], 1, kCdTok, kCdTok, p.r, p.gh, gw2s, p.gc2, hid, threadIdx.x, kCdThreads);
+    __syncthreads();
+  }
   if (rank == 0) {
     for (int e = threadIdx.x; e < kCdTok * p.r; e += kCdThreads) {
       const int m = e / p.r, j = e % p.r;
       const int tok = tok0 + m;
-      const float gate = 1.0f / (1.0f + expf(-(part[p.r][m] + p.b_g)));
+      const float gate = p.gh > 0 ? 1.0f : 1.0f / (1.0f + expf(-(part[p.r][m] + p.b_g)));
       const float tv = p.alpha * gate * part[j][m];
       const __nv_bfloat16 hi = __float2bfloat16_rn(tv);
       const __nv_bfloat16 lo = __float2bfloat16_rn(tv - __bfloat162float(hi));
@@ -665,6 +679,7 @@ int launch_comp_down(const spear_w4_layer& L, const uint16_t* x, int M, __nv_bfl
   p.A = reinterpret_cast<const __nv_bfloat16*>(L.A);
   p.w_g = reinterpret_cast<const __nv_bfloat16*>(L.w_g);
   p.b_g = L.b_g; p.alpha = L.alpha;
+  p.gh = L.gate_hidden; p.gw1 = L.gate_w1; p.gc1 = L.gate_c1; p.gw2 = L.gate_w2; p.gc2 = L.gate_c2;
   p.T2 = T2; p.t2_cols = t2_cols_for(L.rank);
   // enough K ranges per token tile for about two CTAs per SM
   const int tiles = (M + kCdTok - 1) / kCdTok;

@@ -46,7 +46,9 @@ class _Layer(ctypes.Structure):
                 ("symmetric", ctypes.c_int), ("qweight", ctypes.c_void_p), ("scales", ctypes.c_void_p),
                 ("zeros", ctypes.c_void_p), ("rank", ctypes.c_int), ("A", ctypes.c_void_p),
                 ("B", ctypes.c_void_p), ("w_g", ctypes.c_void_p), ("b_g", ctypes.c_float),
-                ("alpha", ctypes.c_float), ("comp_enabled", ctypes.c_int)]
+                ("alpha", ctypes.c_float), ("comp_enabled", ctypes.c_int), ("gate_hidden", ctypes.c_int),
+                ("gate_w1", ctypes.c_void_p), ("gate_c1", ctypes.c_void_p), ("gate_w2", ctypes.c_void_p),
+                ("gate_c2", ctypes.c_void_p)]
 
 
 _lock = threading.Lock()
@@ -131,11 +133,19 @@ class W4Layer:
     b_g: float = 0.0
     alpha: float = 1.0
     comp_enabled: bool = True
+    # the vector gate gamma(A x) = sigmoid(W2 relu(W1 (A x) + c1) + c2), fp32 device
+    # tensors W1 [h][rank], c1 [h], W2 [rank][h], c2 [rank]; None: the scalar gate
+    gate_w1: Optional[torch.Tensor] = None
+    gate_c1: Optional[torch.Tensor] = None
+    gate_w2: Optional[torch.Tensor] = None
+    gate_c2: Optional[torch.Tensor] = None
 
     def c_struct(self) -> _Layer:
+        h = int(self.gate_w1.shape[0]) if self.gate_w1 is not None else 0
         return _Layer(self.N, self.K, self.group_size, int(self.symmetric), _ptr(self.qweight),
                       _ptr(self.scales), _ptr(self.zeros), int(self.rank), _ptr(self.A), _ptr(self.B),
-                      _ptr(self.w_g), float(self.b_g), float(self.alpha), int(self.comp_enabled))
+                      _ptr(self.w_g), float(self.b_g), float(self.alpha), int(self.comp_enabled), h,
+                      _ptr(self.gate_w1), _ptr(self.gate_c1), _ptr(self.gate_w2), _ptr(self.gate_c2))
 
     def with_comp(self, enabled: bool) -> "W4Layer":
         d = dict(self.__dict__)

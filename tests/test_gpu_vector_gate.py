@@ -1,0 +1,79 @@
+"""GPU parity of the pages' vector gate (Technical Summary 2.1 A: effective
+weight W + alpha B diag(gamma(A x)) A, gamma a bottleneck MLP; read as
+gamma(t) = sigmoid(W2 relu(W1 t + c1) + c2)) against the oracle's
+linear_vector_gate: decode on the warp-level kernel (1, 5, 12 tokens) and the
+tensor-core kernel (24, 64 tokens), prefill on 128- and 256-token tiles in
+both modes; no w_g is given."""
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from spear_testutil import check_close, gpu_layer, make_layer, make_tokens, oracle_layer, to_dev_u16
+
+pytestmark = pytest.mark.gpu
+
+
+def _gate(rng, r, h):
+    W1 = (rng.standard_normal((h, r)) * (3.0 / np.sqrt(r))).astype(np.float32)
+    c1 = (rng.standard_normal(h) * 0.1).astype(np.float32)
+    W2 = (rng.standard_normal((r, h)) * (1.0 / np.sqrt(h))).astype(np.float32)
+    c2 = rng.standard_normal(r).astype(np.float32)
+    return W1, c1, W2, c2
+
+
+def _layers(N, K, G, sym, r, h, seed):
+    lay, rng = make_layer(N, K, r, seed=seed)
+    W1, c1, W2, c2 = _gate(np.random.default_rng(seed + 1), r, h)
+    L = gpu_layer(lay, G, sym)
+    dev = lambda a: torch.from_numpy(a).cuda()
+    L = dataclasses.replace(L, w_g=None, gate_w1=dev(W1), gate_c1=dev(c1), gate_w2=dev(W2), gate_c2=dev(c2))
+    return L, oracle_layer(lay, G, sym), (W1, c1, W2, c2), rng
+
+
+@pytest.mark.parametrize("N,K,G,sym,r,h,M", [
+    (512, 1024, 128, False, 32, 8, 1),
+    (512, 1024, 128, False, 32, 8, 5),       # tokens staged in shared memory
+    (256, 2048, 128, False, 16, 4, 12),      # two token tiles
+    (320, 1152, 128, False, 64, 16, 24),     # tensor-core kernel, 32 token rows
+    (256, 1024, 1024, True, 32, 32, 64),     # tensor-core kernel, per-channel scales
+])
+def test_decode_vector_gate_matches_oracle(N, K, G, sym, r, h, M):
+    from quantized_gemm_error_gb300 import spear
+    L, OL, g, rng = _layers(N, K, G, sym, r, h, seed=200 + N + M)
+    x = make_tokens(rng, M, K, outlier_frac=0.01)
+    ref, gam = oracle.linear_vector_gate(OL, x, *g, nthreads=8)
+    assert 0.02 < gam.mean() < 0.98 and gam.std() > 0.05           # the gate really varies
+    y = spear.spear_linear_decode(L, to_dev_u16(x, torch.bfloat16), out_dtype=1)
+    torch.cuda.synchronize()
+    assert spear.spear_get_device_status() == 0
+    check_close(y, ref)
+
+
+@pytest.mark.parametrize("N,K,G,sym,r,h,M", [
+    (512, 1024, 128, False, 32, 8, 300),     # 128-token tiles
+    (2560, 512, 128, False, 32, 8, 2000),    # 256-token tiles: the correction joins the main accumulators
+    (512, 1024, 1024, True, 64, 16, 200),    # per-channel scales
+])
+@pytest.mark.parametrize("mode", [1, 2])
+def test_prefill_vector_gate_matches_oracle(N, K, G, sym, r, h, M, mode):
+    from quantized_gemm_error_gb300 import spear
+    L, OL, g, rng = _layers(N, K, G, sym, r, h, seed=300 + N + M)
+    x = make_tokens(rng, M, K, outlier_frac=0.01)
+    ref, _ = oracle.linear_vector_gate(OL, x, *g, nthreads=8)
+    y = spear.spear_linear_prefill(L, to_dev_u16(x, torch.bfloat16), out_dtype=1, mode=mode,
+                                   stream_aux=torch.cuda.Stream())
+    torch.cuda.synchronize()
+    assert spear.spear_get_device_status() == 0
+    check_close(y, ref)
+
+
+def test_vector_gate_hidden_width_is_checked():
+    from quantized_gemm_error_gb300 import spear
+    L, _, g, rng = _layers(256, 512, 128, False, 16, 4, seed=7)
+    big = torch.zeros(33, 16, device="cuda")
+    with pytest.raises(spear.SpearError):
+        spear.spear_linear_decode(dataclasses.replace(L, gate_w1=big), to_dev_u16(make_tokens(rng, 1, 512),
+                                                                                     torch.bfloat16))
