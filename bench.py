@@ -640,6 +640,60 @@ def run_stack(args):
     print(json.dumps(line), flush=True)
 
 
+def run_schedule(args):
+    """SLO-constrained chunk selection on the 32-block decoder stack: latency
+    tables measured per layer kind, then for several compensator densities and
+    inter-token latency targets the chosen prefill chunk, its predicted mixed
+    step and the measured one (the stack step at that chunk, CUDA graph)."""
+    import torch
+    from quantized_gemm_error_gb300 import spear
+    from quantized_gemm_error_gb300.scheduler import choose_chunk, measure_curves
+    from quantized_gemm_error_gb300.stack import StackStep, build_stack, select_blocks
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(device)
+    spear.load()
+    spear.spear_set_launch_overlap(True)
+    D = 32
+    choices = [0, 128, 256, 384, 512, 768, 1024, 1536, 2048]
+    targets_ms = [8.0, 16.0, 22.0]
+    rows = []
+    table = None
+    for masked in (0, 4, 8):
+        ranks = select_blocks(32, masked, 64, seed=0)[1] if masked else [0] * 32
+        layers = build_stack(ranks, device, seed=0, recipe="device")
+        Ls = [sl.layer for sl in layers]
+        t = measure_curves(Ls, [128, 256, 512, 1024, 2048, 2560], [1, 8, 16, 32, 64], device)
+        table = t if table is None else {**table, **t}
+        for tgt in targets_ms:
+            C, pred = choose_chunk(Ls, table, D, choices, tgt * 1e3)
+            step = StackStep(layers, max(C + D, 1), D, device, seed=0)
+            step.capture()
+            name = "prefill" if C > 0 else "decode"
+            for _ in range(3):
+                step.replay(name)
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(step.stream)
+            for _ in range(10):
+                step.replay(name)
+            e1.record(step.stream)
+            torch.cuda.synchronize()
+            meas = e0.elapsed_time(e1) / 10
+            rows.append({"compensated_blocks": masked, "itl_target_ms": tgt, "chunk": C,
+                         "predicted_ms": round(pred / 1e3, 3), "measured_ms": round(meas, 3),
+                         "slo_met": bool(meas <= tgt)})
+            del step
+        del layers, Ls
+        torch.cuda.empty_cache()
+    met = sum(r["slo_met"] for r in rows)
+    print(json.dumps({
+        "metric": "SLO-constrained chunk selection on the 32-block stack (steps meeting the ITL target)",
+        "value": met, "unit": f"of {len(rows)}", "higher_is_better": True, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "llama7b_stack_sym_r64", "decode_tokens": D, "chunk_choices": choices,
+                   "launch": "cuda-graph"},
+        "decisions": rows, "status": spear.spear_get_device_status()}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -652,9 +706,15 @@ def main():
                     help="run one prefill case ITERS times for a profiler and exit")
     ap.add_argument("--stack", action="store_true",
                     help="time the 32-block decoder stack (mixed prefill step and decode step) instead")
+    ap.add_argument("--schedule", action="store_true",
+                    help="SLO-constrained chunk selection on the decoder stack: chosen chunks, predicted and "
+                         "measured step latencies")
     args = ap.parse_args()
     if args.profile_prefill:
         profile_prefill_case(args.profile_prefill)
+        return
+    if args.schedule:
+        run_schedule(args)
         return
     if args.stack:
         args.warmup = max(3, min(args.warmup, 10))

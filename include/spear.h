@@ -231,6 +231,30 @@ spear_status spear_layer_select_mask(const float* damage, const float* cost, int
                                      uint8_t* mask_out, int* rank_out);
 
 /*
+ * SLO-constrained chunk selection (Technical Summary 2.2 C), host only.
+ * A latency curve holds n >= 1 measured points (M[i], us[i]) of one layer
+ * (M strictly increasing, us >= 0); between points the latency is linear in
+ * M, outside them it continues the line through the two nearest points (one
+ * point: constant).  For a step with D = decode_tokens decode tokens and a
+ * prefill chunk of C tokens the predicted step latency is
+ *   C > 0:  sum over layers of prefill[l](C + D)   (one mixed pass, prefill path)
+ *   C = 0:  sum over layers of decode[l](D)        (decode path; 0 if D = 0)
+ * chunk_out receives the largest C in choices[nchoices] (C >= 0) whose step
+ * latency is <= itl_target_us; if none is, the smallest C.  step_us_out (may
+ * be NULL) receives that C's predicted latency.  A layer's curves reflect its
+ * compensator (or its absence), so the choice follows the EC density.
+ */
+typedef struct spear_latency_curve {
+  int n;
+  const int* M;
+  const float* us;
+} spear_latency_curve;
+
+spear_status spear_chunk_select(const spear_latency_curve* prefill, const spear_latency_curve* decode,
+                                int nlayers, int decode_tokens, const int* choices, int nchoices,
+                                double itl_target_us, int* chunk_out, double* step_us_out);
+
+/*
  * Reads and clears the device status word of the current device
  * (synchronises `stream`).  *out = SPEAR_OK, or the first kernel-side error
  * recorded since the last read.

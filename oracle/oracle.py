@@ -25,7 +25,7 @@ _lib = None
 __all__ = [
     "build_oracle", "f32_to_f16_ru", "f16_to_f32", "f32_to_bf16_rn", "bf16_to_f32",
     "quantize_pack", "unpack_codes", "unpack_zeros", "dequant", "linear",
-    "linear_vector_gate", "layer_select_mask", "packed_sizes",
+    "linear_vector_gate", "layer_select_mask", "chunk_select", "packed_sizes",
 ]
 
 
@@ -203,6 +203,35 @@ def linear_vector_gate(layer: dict, x_bf16, W1, c1, W2, c2, *, nthreads: int = 1
         _ptr(x), M, int(nthreads), _ptr(y), _ptr(gam))
     _check(rc, "linear_vector_gate")
     return y, gam
+
+
+# --------------------------------------------------------- chunk selection
+
+def chunk_select(prefill_curves, decode_curves, decode_tokens: int, choices, itl_target_us: float):
+    """SLO-constrained chunk choice (Technical Summary 2.2 C), written out
+    plainly: a curve is (M list, microseconds list); its latency at M is the
+    line through the two points bracketing M (the nearest two outside the
+    range; one point: constant).  A chunk C > 0 costs the sum of the prefill
+    curves at C + D; C = 0 the sum of the decode curves at D (0 without
+    decode tokens).  Returns (largest C within the target, else the smallest C;
+    that C's latency)."""
+    def at(curve, M):
+        Ms, us = [float(v) for v in curve[0]], [float(v) for v in curve[1]]
+        if len(Ms) == 1:
+            return us[0]
+        i = 0
+        while i + 2 < len(Ms) and M > Ms[i + 1]:
+            i += 1
+        return us[i] + (us[i + 1] - us[i]) * (M - Ms[i]) / (Ms[i + 1] - Ms[i])
+
+    def step(C):
+        if C > 0:
+            return sum(at(c, C + decode_tokens) for c in prefill_curves)
+        return sum(at(c, decode_tokens) for c in decode_curves) if decode_tokens > 0 else 0.0
+
+    ok = [C for C in choices if step(C) <= itl_target_us]
+    C = max(ok) if ok else min(choices)
+    return C, step(C)
 
 
 # --------------------------------------------------------- module selection

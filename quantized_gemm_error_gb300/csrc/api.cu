@@ -215,6 +215,57 @@ spear_status spear_workspace_init(void* workspace, size_t bytes, void* stream) {
 // Module selection, host only (see spear.h).  Ranks modules by damage share
 // per unit of relative cost, keeps round(exp(entropy)) of them and gives them
 // one common rank, a multiple of 16, that fits the byte budget.
+namespace {
+// Latency of one curve at M: piecewise linear through the points, continued
+// past either end along the two nearest points.
+bool curve_ok(const spear_latency_curve& c) {
+  if (c.n < 1 || !c.M || !c.us) return false;
+  for (int i = 0; i < c.n; ++i) {
+    if (!std::isfinite(c.us[i]) || c.us[i] < 0.0f) return false;
+    if (i > 0 && c.M[i] <= c.M[i - 1]) return false;
+  }
+  return true;
+}
+double curve_at(const spear_latency_curve& c, double M) {
+  if (c.n == 1) return c.us[0];
+  int i = 0;                                        // segment [i, i + 1]
+  while (i + 2 < c.n && M > c.M[i + 1]) ++i;
+  const double m0 = c.M[i], m1 = c.M[i + 1], u0 = c.us[i], u1 = c.us[i + 1];
+  return u0 + (u1 - u0) * (M - m0) / (m1 - m0);
+}
+}  // namespace
+
+spear_status spear_chunk_select(const spear_latency_curve* prefill, const spear_latency_curve* decode,
+                                int nlayers, int decode_tokens, const int* choices, int nchoices,
+                                double itl_target_us, int* chunk_out, double* step_us_out) {
+  if (!prefill || !decode || nlayers <= 0 || !choices || nchoices <= 0 || !chunk_out || decode_tokens < 0 ||
+      !(itl_target_us >= 0.0))
+    return spear::fail(SPEAR_ERR_INVALID_ARG, "chunk_select: bad arguments");
+  for (int l = 0; l < nlayers; ++l)
+    if (!curve_ok(prefill[l]) || !curve_ok(decode[l]))
+      return spear::fail(SPEAR_ERR_INVALID_ARG, "chunk_select: curve of layer %d invalid", l);
+  for (int i = 0; i < nchoices; ++i)
+    if (choices[i] < 0) return spear::fail(SPEAR_ERR_INVALID_ARG, "chunk_select: choices[%d] < 0", i);
+  auto step = [&](int C) {
+    double s = 0.0;
+    if (C > 0) {
+      for (int l = 0; l < nlayers; ++l) s += curve_at(prefill[l], (double)C + decode_tokens);
+    } else if (decode_tokens > 0) {
+      for (int l = 0; l < nlayers; ++l) s += curve_at(decode[l], (double)decode_tokens);
+    }
+    return s;
+  };
+  int best = -1, smallest = choices[0];
+  for (int i = 0; i < nchoices; ++i) {
+    smallest = std::min(smallest, choices[i]);
+    if (step(choices[i]) <= itl_target_us && choices[i] > best) best = choices[i];
+  }
+  const int C = best >= 0 ? best : smallest;
+  *chunk_out = C;
+  if (step_us_out) *step_us_out = step(C);
+  return SPEAR_OK;
+}
+
 spear_status spear_layer_select_mask(const float* damage, const float* cost, int L, double budget_bytes,
                                      int rank_min, int rank_max, uint8_t* mask_out, int* rank_out) {
   if (!damage || !cost || !mask_out || !rank_out || L <= 0) return fail(SPEAR_ERR_INVALID_ARG, "bad arguments");

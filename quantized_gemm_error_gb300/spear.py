@@ -31,7 +31,7 @@ OUT_BF16, OUT_F32 = 0, 1
 # every symbol include/spear.h declares
 EXPORTS = ["spear_pack_w4_sizes", "spear_pack_w4", "spear_decode_workspace_bytes",
            "spear_linear_decode", "spear_linear_decode_noalloc", "spear_prefill_workspace_bytes", "spear_linear_prefill",
-           "spear_workspace_init", "spear_set_launch_overlap", "spear_layer_select_mask",
+           "spear_workspace_init", "spear_set_launch_overlap", "spear_layer_select_mask", "spear_chunk_select",
            "spear_get_device_status", "spear_status_string", "spear_last_error", "spear_version"]
 
 
@@ -77,6 +77,7 @@ def load(path: str = LIB_PATH):
             "spear_linear_prefill": [LP, P, I, P, I, I, P, S, P, P],
             "spear_workspace_init": [P, S, P],
             "spear_layer_select_mask": [P, P, I, ctypes.c_double, I, I, P, P],
+            "spear_chunk_select": [P, P, I, I, P, I, ctypes.c_double, ctypes.POINTER(I), ctypes.POINTER(ctypes.c_double)],
             "spear_get_device_status": [ctypes.POINTER(I), P],
             "spear_set_launch_overlap": [I],
         }
@@ -268,6 +269,34 @@ def spear_layer_select_mask(damage, cost, budget_bytes: float, rank_min: int, ra
                                           mask.ctypes.data_as(ctypes.c_void_p),
                                           rank.ctypes.data_as(ctypes.c_void_p)), "spear_layer_select_mask")
     return mask, rank
+
+
+class _Curve(ctypes.Structure):
+    _fields_ = [("n", ctypes.c_int), ("M", ctypes.c_void_p), ("us", ctypes.c_void_p)]
+
+
+def spear_chunk_select(prefill_curves, decode_curves, decode_tokens: int, choices, itl_target_us: float):
+    """prefill_curves / decode_curves: per layer, a pair (M list, microseconds list).
+    Returns (chunk, predicted step microseconds)."""
+    keep = []
+
+    def curves(cs):
+        arr = (_Curve * len(cs))()
+        for i, (Ms, us) in enumerate(cs):
+            m = np.ascontiguousarray(Ms, dtype=np.int32)
+            u = np.ascontiguousarray(us, dtype=np.float32)
+            keep.extend([m, u])
+            arr[i] = _Curve(m.shape[0], m.ctypes.data, u.ctypes.data)
+        return arr
+    pre, dec = curves(prefill_curves), curves(decode_curves)
+    ch = np.ascontiguousarray(choices, dtype=np.int32)
+    out = ctypes.c_int()
+    step = ctypes.c_double()
+    _check(load().spear_chunk_select(ctypes.cast(pre, ctypes.c_void_p), ctypes.cast(dec, ctypes.c_void_p),
+                                     len(prefill_curves), int(decode_tokens), ch.ctypes.data_as(ctypes.c_void_p),
+                                     ch.shape[0], float(itl_target_us), ctypes.byref(out), ctypes.byref(step)),
+           "spear_chunk_select")
+    return out.value, step.value
 
 
 # ------------------------------------------------------------ status
