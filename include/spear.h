@@ -231,6 +231,18 @@ spear_status spear_layer_select_mask(const float* damage, const float* cost, int
                                      uint8_t* mask_out, int* rank_out);
 
 /*
+ * Linear centred kernel alignment (Technical Summary 2.1 B: CKA is the
+ * training-free proxy for the quality a module loses to quantisation), host
+ * only.  X [n][dx] and Y [n][dy] are fp32, one row per token; with Xc, Yc
+ * their column-centred forms
+ *   *cka_out = ||Xc^T Yc||_F^2 / (||Xc^T Xc||_F ||Yc^T Yc||_F)   (in [0, 1]),
+ * computed in fp64.  A module's damage score for spear_layer_select_mask is
+ * 1 - CKA(its reference output, its quantised output) on the same tokens.
+ * n >= 2; non-finite inputs or an input without variance are rejected.
+ */
+spear_status spear_linear_cka(const float* X, const float* Y, int n, int dx, int dy, double* cka_out);
+
+/*
  * SLO-constrained chunk selection (Technical Summary 2.2 C), host only.
  * A latency curve holds n >= 1 measured points (M[i], us[i]) of one layer
  * (M strictly increasing, us >= 0); between points the latency is linear in

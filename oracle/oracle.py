@@ -25,7 +25,7 @@ _lib = None
 __all__ = [
     "build_oracle", "f32_to_f16_ru", "f16_to_f32", "f32_to_bf16_rn", "bf16_to_f32",
     "quantize_pack", "unpack_codes", "unpack_zeros", "dequant", "linear",
-    "linear_vector_gate", "layer_select_mask", "chunk_select", "packed_sizes",
+    "linear_vector_gate", "layer_select_mask", "chunk_select", "linear_cka", "packed_sizes",
 ]
 
 
@@ -203,6 +203,22 @@ def linear_vector_gate(layer: dict, x_bf16, W1, c1, W2, c2, *, nthreads: int = 1
         _ptr(x), M, int(nthreads), _ptr(y), _ptr(gam))
     _check(rc, "linear_vector_gate")
     return y, gam
+
+
+# --------------------------------------------------------- linear CKA
+
+def linear_cka(X, Y) -> float:
+    """Linear CKA from its definition (Technical Summary 2.1 B names CKA as
+    the damage proxy): K = X X^T, L = Y Y^T on the raw activations, the
+    centring matrix H = I - 1 1^T / n, HSIC(K, L) = tr(K H L H), and
+    CKA = HSIC(K, L) / sqrt(HSIC(K, K) HSIC(L, L)); fp64 numpy."""
+    X = np.asarray(X, dtype=np.float64)
+    Y = np.asarray(Y, dtype=np.float64)
+    n = X.shape[0]
+    H = np.eye(n) - np.ones((n, n)) / n
+    K, L = X @ X.T, Y @ Y.T
+    hsic = lambda a, b: float(np.trace(a @ H @ b @ H))
+    return hsic(K, L) / np.sqrt(hsic(K, K) * hsic(L, L))
 
 
 # --------------------------------------------------------- chunk selection

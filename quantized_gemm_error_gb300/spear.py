@@ -32,6 +32,7 @@ OUT_BF16, OUT_F32 = 0, 1
 EXPORTS = ["spear_pack_w4_sizes", "spear_pack_w4", "spear_decode_workspace_bytes",
            "spear_linear_decode", "spear_linear_decode_noalloc", "spear_prefill_workspace_bytes", "spear_linear_prefill",
            "spear_workspace_init", "spear_set_launch_overlap", "spear_layer_select_mask", "spear_chunk_select",
+           "spear_linear_cka",
            "spear_get_device_status", "spear_status_string", "spear_last_error", "spear_version"]
 
 
@@ -78,6 +79,7 @@ def load(path: str = LIB_PATH):
             "spear_workspace_init": [P, S, P],
             "spear_layer_select_mask": [P, P, I, ctypes.c_double, I, I, P, P],
             "spear_chunk_select": [P, P, I, I, P, I, ctypes.c_double, ctypes.POINTER(I), ctypes.POINTER(ctypes.c_double)],
+            "spear_linear_cka": [P, P, I, I, I, ctypes.POINTER(ctypes.c_double)],
             "spear_get_device_status": [ctypes.POINTER(I), P],
             "spear_set_launch_overlap": [I],
         }
@@ -269,6 +271,25 @@ def spear_layer_select_mask(damage, cost, budget_bytes: float, rank_min: int, ra
                                           mask.ctypes.data_as(ctypes.c_void_p),
                                           rank.ctypes.data_as(ctypes.c_void_p)), "spear_layer_select_mask")
     return mask, rank
+
+
+def spear_linear_cka(X, Y) -> float:
+    """Linear CKA of two host activation matrices [n][dx], [n][dy] (fp32)."""
+    x = np.ascontiguousarray(X, dtype=np.float32)
+    y = np.ascontiguousarray(Y, dtype=np.float32)
+    if x.ndim != 2 or y.ndim != 2 or x.shape[0] != y.shape[0]:
+        raise ValueError("X and Y must be [n][d] with the same n")
+    out = ctypes.c_double()
+    _check(load().spear_linear_cka(x.ctypes.data_as(ctypes.c_void_p), y.ctypes.data_as(ctypes.c_void_p),
+                                   x.shape[0], x.shape[1], y.shape[1], ctypes.byref(out)), "spear_linear_cka")
+    return out.value
+
+
+def cka_damage(reference_outputs, quantised_outputs):
+    """Per-module damage scores 1 - CKA(reference, quantised) for the
+    module-selection rule; each argument a list of host [n][d] matrices."""
+    return np.array([1.0 - spear_linear_cka(a, b) for a, b in zip(reference_outputs, quantised_outputs)],
+                    dtype=np.float32)
 
 
 class _Curve(ctypes.Structure):
