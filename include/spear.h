@@ -131,7 +131,7 @@ spear_status spear_pack_w4(const float* W, int N, int K, int group_size, int sym
 /*
  * Decode (Technical Summary 2.2 A, decode phase, M small): ONE kernel launch
  * streams the int4 weights, computes g(x) and A x for every token in the same
- * launch and adds alpha*g*B(Ax) in the epilogue.  1 <= M <= 64.
+ * launch and adds alpha*g*B(Ax) in the epilogue.  0 <= M <= 64 (M = 0: no work, SPEAR_OK).
  *   x : device bf16 [M][K];  y : device [M][N], bf16 or fp32 (out_dtype).
  * M <= 16 runs on warp-level MMAs; M >= 17 on the tcgen05 tensor cores.
  * The thread blocks of the launch exchange the M x (rank+1) down-projection
@@ -178,7 +178,7 @@ spear_status spear_linear_decode_noalloc(const spear_w4_layer* L, const uint16_t
 /*
  * Prefill (Technical Summary 2.2 A, prefill phase, M large): tcgen05 tensor-core
  * GEMM over int4 tiles dequantized in shared memory, plus the compensator in
- * one of the modes above.  1 <= M.
+ * one of the modes above.  M >= 0 (M = 0: no work, SPEAR_OK).
  *   x : device bf16 [M][K];  y : device [M][N], bf16 or fp32.
  *   The main GEMM runs on fp16 operands with fp32 accumulation: the
  *   activations are copied to fp16 (exact for |x| < 65504; a larger value is

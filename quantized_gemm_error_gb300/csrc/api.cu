@@ -160,15 +160,20 @@ spear_status spear_pack_w4(const float* W, int N, int K, int group_size, int sym
 
 spear_status spear_decode_workspace_bytes(const spear_w4_layer* L, int M, size_t* bytes) {
   if (int rc = check_layer(L)) return rc;
-  if (M < 1 || M > 64) return fail(SPEAR_ERR_INVALID_ARG, "decode M=%d must be in [1, 64]", M);
+  if (M < 0 || M > 64) return fail(SPEAR_ERR_INVALID_ARG, "decode M=%d must be in [0, 64]", M);
   if (!bytes) return fail(SPEAR_ERR_INVALID_ARG, "bytes is NULL");
+  if (M == 0) {                                      // an empty batch needs no workspace
+    *bytes = 0;
+    return SPEAR_OK;
+  }
   return decode_workspace_bytes(*L, M, bytes);
 }
 
 spear_status spear_linear_decode(const spear_w4_layer* L, const uint16_t* x, int M, void* y, int out_dtype,
                                  void* workspace, size_t ws_bytes, void* stream) {
   if (int rc = check_layer(L)) return rc;
-  if (M < 1 || M > 64) return fail(SPEAR_ERR_INVALID_ARG, "decode M=%d must be in [1, 64]", M);
+  if (M < 0 || M > 64) return fail(SPEAR_ERR_INVALID_ARG, "decode M=%d must be in [0, 64]", M);
+  if (M == 0) return SPEAR_OK;                       // an empty batch: nothing to read or write
   if (!x || !y || !aligned16(x) || !aligned16(y)) return fail(SPEAR_ERR_INVALID_ARG, "x/y NULL or misaligned");
   if (out_dtype != SPEAR_OUT_BF16 && out_dtype != SPEAR_OUT_F32)
     return fail(SPEAR_ERR_INVALID_ARG, "out_dtype=%d", out_dtype);
@@ -179,7 +184,8 @@ spear_status spear_linear_decode(const spear_w4_layer* L, const uint16_t* x, int
 spear_status spear_linear_decode_noalloc(const spear_w4_layer* L, const uint16_t* x, int M, void* y,
                                          int out_dtype, void* stream) {
   if (int rc = check_layer(L)) return rc;
-  if (M < 1 || M > 64) return fail(SPEAR_ERR_INVALID_ARG, "decode M=%d must be in [1, 64]", M);
+  if (M < 0 || M > 64) return fail(SPEAR_ERR_INVALID_ARG, "decode M=%d must be in [0, 64]", M);
+  if (M == 0) return SPEAR_OK;                       // an empty batch: nothing to read or write
   if (!x || !y || !aligned16(x) || !aligned16(y)) return fail(SPEAR_ERR_INVALID_ARG, "x/y NULL or misaligned");
   if (out_dtype != SPEAR_OUT_BF16 && out_dtype != SPEAR_OUT_F32)
     return fail(SPEAR_ERR_INVALID_ARG, "out_dtype=%d", out_dtype);
@@ -188,16 +194,22 @@ spear_status spear_linear_decode_noalloc(const spear_w4_layer* L, const uint16_t
 
 spear_status spear_prefill_workspace_bytes(const spear_w4_layer* L, int M, int mode, size_t* bytes) {
   if (int rc = check_layer(L)) return rc;
-  if (M < 1) return fail(SPEAR_ERR_INVALID_ARG, "prefill M=%d must be positive", M);
+  if (M < 0) return fail(SPEAR_ERR_INVALID_ARG, "prefill M=%d must not be negative", M);
   if (mode < SPEAR_PREFILL_AUTO || mode > SPEAR_PREFILL_STREAM) return fail(SPEAR_ERR_INVALID_ARG, "mode=%d", mode);
   if (!bytes) return fail(SPEAR_ERR_INVALID_ARG, "bytes is NULL");
+  if (M == 0) {
+    *bytes = 0;
+    return SPEAR_OK;
+  }
   return prefill_workspace_bytes(*L, M, mode, bytes);
 }
 
 spear_status spear_linear_prefill(const spear_w4_layer* L, const uint16_t* x, int M, void* y, int out_dtype,
                                   int mode, void* workspace, size_t ws_bytes, void* stream, void* stream_aux) {
   if (int rc = check_layer(L)) return rc;
-  if (M < 1) return fail(SPEAR_ERR_INVALID_ARG, "prefill M=%d must be positive", M);
+  if (M < 0) return fail(SPEAR_ERR_INVALID_ARG, "prefill M=%d must not be negative", M);
+  if (mode < SPEAR_PREFILL_AUTO || mode > SPEAR_PREFILL_STREAM) return fail(SPEAR_ERR_INVALID_ARG, "mode=%d", mode);
+  if (M == 0) return SPEAR_OK;                       // an empty batch: nothing to read or write
   if (!x || !y || !aligned16(x) || !aligned16(y)) return fail(SPEAR_ERR_INVALID_ARG, "x/y NULL or misaligned");
   if (out_dtype != SPEAR_OUT_BF16 && out_dtype != SPEAR_OUT_F32)
     return fail(SPEAR_ERR_INVALID_ARG, "out_dtype=%d", out_dtype);

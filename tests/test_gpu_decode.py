@@ -131,3 +131,21 @@ def test_token_permutation_permutes_rows():
     y = _run(L, x, out_dtype=1)
     yp = _run(L, x[perm], out_dtype=1)
     assert torch.equal(y[torch.from_numpy(perm).cuda()], yp)
+
+
+def test_empty_batch_is_a_no_op():
+    """M = 0 on both paths: nothing to read or write, SPEAR_OK, an empty y;
+    M = 65 on the decode path is refused."""
+    from quantized_gemm_error_gb300 import spear
+    lay, rng = make_layer(512, 1024, 32, seed=25)
+    L = gpu_layer(lay, 128, False)
+    x0 = torch.empty(0, 1024, dtype=torch.bfloat16, device="cuda")
+    assert spear.spear_decode_workspace_bytes(L, 0) == 0
+    assert spear.spear_prefill_workspace_bytes(L, 0) == 0
+    yd = spear.spear_linear_decode(L, x0)
+    yp = spear.spear_linear_prefill(L, x0)
+    torch.cuda.synchronize()
+    assert yd.shape == (0, 512) and yp.shape == (0, 512)
+    assert spear.spear_get_device_status() == 0
+    with pytest.raises(spear.SpearError):
+        spear.spear_linear_decode(L, to_dev_u16(make_tokens(rng, 65, 1024), torch.bfloat16))
