@@ -45,10 +45,19 @@ def decode_kernel_name(M: int) -> str:
     return "decode_tc_kernel" if M >= TC_MIN_M else "decode_kernel"
 
 
-def source_digest(name: str) -> str:
+def code_digest(text: str) -> str:
+    """Digest of C++/CUDA source with comments and whitespace removed, so an
+    edit to the comments alone does not mark the counters stale."""
     import hashlib
-    with open(os.path.join(ROOT, "quantized_gemm_error_gb300", "csrc", name), "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+    import re
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return hashlib.sha256(" ".join(text.split()).encode()).hexdigest()[:16]
+
+
+def source_digest(name: str) -> str:
+    with open(os.path.join(ROOT, "quantized_gemm_error_gb300", "csrc", name)) as f:
+        return code_digest(f.read())
 
 
 def measured_traffic(kernel: str, cases):

@@ -13,15 +13,13 @@
 //    slice partials to the workspace, and the last producer to arrive sums
 //    them in a fixed order, applies the gate and publishes T = alpha g t with
 //    a release flag.
-//  * Streamer blocks split the (16-row tile x 128-k chunk) work items of the
-//    int4 weight evenly ("stream-K"): each block owns one contiguous range,
-//    so every SM streams the same number of weight bytes.  Weights move
-//    global -> shared through a per-warp cp.async ring (L1 bypass), are turned
-//    into exact small integers in registers (nibble | bf16 bias, minus the
-//    biased zero point) and multiplied by the tokens with mma.sync; the group
-//    scale is applied to each 128-k partial in fp32.  A tile split across two
-//    blocks is finished by whichever block arrives last (fixed-order sum of
-//    the parts from the workspace).
+//  * Streamer blocks own contiguous ranges of whole 16-row tiles of the int4
+//    weight (tile counts per block differ by at most one), so no partial sum
+//    leaves a block; the block's 8 warps split each tile's K range.  Weights
+//    move global -> shared through a per-warp cp.async ring (L1 bypass), are
+//    turned into exact small integers in registers (nibble | bf16 bias, minus
+//    the biased zero point) and multiplied by the tokens with mma.sync; the
+//    group scale is applied to each 128-k partial in fp32.
 //  * Only the epilogue depends on T: each streamer waits (bounded) for the
 //    flag after all of its weight traffic, adds B T with one more small mma,
 //    and stores y.  The last streamer resets the flag, so the workspace's
