@@ -48,6 +48,11 @@ __device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
   unsigned s = (unsigned)__cvta_generic_to_shared(smem);
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(s), "l"(gmem) : "memory");
 }
+// 4-byte asynchronous global->shared copy through L1 (small operands).
+__device__ __forceinline__ void cp_async4(void* smem, const void* gmem) {
+  unsigned s = (unsigned)__cvta_generic_to_shared(smem);
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(s), "l"(gmem) : "memory");
+}
 // Programmatic dependent launch: let the next kernel on the stream start
 // launching / wait until the previous kernel completed with its memory
 // visible.  Both are no-ops for a launch without the programmatic attribute.
@@ -140,53 +145,144 @@ __device__ __forceinline__ void nibbles_to_bf16x2_biased(uint32_t w, uint32_t (&
 
 // The vector gate (Technical Summary 2.1 A: gamma is a bottleneck MLP on the
 // rank-r code t = A x), for ntok tokens at once, in two phases with a barrier
-// of the calling threads [tid0, tid0 + nthreads) between and after them:
-//   vector_gate_hidden:  hid[m][i] = relu(c1[i] + sum_j W1s[i][j] t[m][j])   [ntok][h]
-//   vector_gate_apply:   t[m][j] *= sigmoid(c2[j] + sum_i W2s[j][i] hid[m][i])
-// t[m][j] sits at t[m * tm + j * tj] (shared memory); W1s [h][r] and W2s
-// [r][h] are staged in shared memory (stage_gate_weights); c1 [h], c2 [r] are
-// fp32 in global memory.  fp32 accumulation in index order; every (token,
-// unit) pair belongs to one thread, so apply may overwrite t in place.
-__device__ __forceinline__ void vector_gate_hidden(const float* t, int tm, int tj, int ntok, int r, int h,
-                                                   const float* W1s, const float* c1, float* hid, int tid,
-                                                   int nthreads) {
-  for (int e = tid; e < ntok * h; e += nthreads) {
-    const int m = e / h, i = e % h;
-    float acc = __ldg(c1 + i);
-    for (int j = 0; j < r; ++j) acc = fmaf(W1s[i * r + j], t[m * tm + j * tj], acc);
-    hid[e] = fmaxf(acc, 0.0f);
+// of the calling threads between and after them:
+//   hidden:  hid[m][i] = relu(c1[i] + sum_j W1[i][j] t[m][j])
+//   apply:   t[m][j] *= sigmoid(c2[j] + sum_i W2[j][i] hid[m][i])
+// The fp32 weights are read from the shared-memory copy that
+// stage_gate_weights_async makes (a global load inside these loops costs an L2
+// round trip per pair while the weight stream runs), laid out so that the
+// loads of a warp hit distinct banks:
+//   G = [ W1 [h][r + 4] (rows padded) | W2^T [h][r] | c2 [r] | c1 [h] ],
+// every part 16-byte aligned when G is (the rank is a multiple of 16).  The
+// hidden units sit at hid[m * gate_hid_stride(h) + i].  Every (token, unit)
+// element belongs to one thread, so apply may overwrite t in place.
+__host__ __device__ constexpr int gate_smem_floats(int r, int h) { return h * (r + 4) + h * r + r + h; }
+__host__ __device__ constexpr int gate_hid_stride(int h) { return h | 1; }
+
+struct GateSmem {
+  const float *W1, *W2t, *c2, *c1;
+  int r, h;
+  __device__ GateSmem(const float* G, int r_, int h_)
+      : W1(G), W2t(G + h_ * (r_ + 4)), c2(G + h_ * (r_ + 4) + h_ * r_), c1(G + h_ * (r_ + 4) + h_ * r_ + r_),
+        r(r_), h(h_) {}
+};
+
+// Starts the copy of the gate's W1 [h][r], W2 [r][h], c1 [h], c2 [r] (fp32,
+// global) into the layout above as one cp.async group of threads [tid0, tid0
+// + nthreads): issued where the kernel starts, so the copy overlaps its main
+// work.  Before reading G the caller waits for the group (cp_async_wait<0>)
+// and then synchronises those threads.
+__device__ __forceinline__ void stage_gate_weights_async(const float* W1, const float* W2, const float* c1,
+                                                         const float* c2, int r, int h, float* G, int tid,
+                                                         int nthreads) {
+  const int n1 = h * (r + 4), n2 = n1 + h * r, n3 = n2 + r, total = gate_smem_floats(r, h);
+  for (int e = tid; e < total; e += nthreads) {
+    const float* src = nullptr;
+    if (e < n1) {
+      const int i = e / (r + 4), j = e % (r + 4);
+      if (j < r) src = W1 + i * r + j;
+    } else if (e < n2) {
+      const int i = (e - n1) / r, j = (e - n1) % r;
+      src = W2 + j * h + i;
+    } else if (e < n3) {
+      src = c2 + (e - n2);
+    } else {
+      src = c1 + (e - n3);
+    }
+    if (src) cp_async4(G + e, src);
+  }
+  cp_async_commit();
+}
+
+// Token rows t[m][0 .. r) at t + m r (16-byte aligned): 16-byte loads, one
+// hidden unit of one token per thread, then four consecutive components of
+// one token per thread.  Each dot product is four fp32 partial sums (terms
+// q mod 4) added at the end.
+__device__ __forceinline__ void vector_gate_hidden_rows(const float* t, int ntok, const GateSmem& g, float* hid,
+                                                        int tid, int nthreads) {
+  const int r4 = g.r / 4, hs = gate_hid_stride(g.h);
+  for (int e = tid; e < ntok * g.h; e += nthreads) {
+    const int m = e / g.h, i = e % g.h;
+    const float4* w = reinterpret_cast<const float4*>(g.W1 + i * (g.r + 4));
+    const float4* tt = reinterpret_cast<const float4*>(t + m * g.r);
+    float4 a = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+#pragma unroll 4
+    for (int q = 0; q < r4; ++q) {
+      const float4 wv = w[q], tv = tt[q];
+      a.x = fmaf(wv.x, tv.x, a.x);
+      a.y = fmaf(wv.y, tv.y, a.y);
+      a.z = fmaf(wv.z, tv.z, a.z);
+      a.w = fmaf(wv.w, tv.w, a.w);
+    }
+    hid[m * hs + i] = fmaxf(g.c1[i] + ((a.x + a.y) + (a.z + a.w)), 0.0f);
   }
 }
-__device__ __forceinline__ void vector_gate_apply(float* t, int tm, int tj, int ntok, int r, int h,
-                                                  const float* W2s, const float* c2, const float* hid, int tid,
-                                                  int nthreads) {
-  for (int e = tid; e < ntok * r; e += nthreads) {
-    const int m = e / r, j = e % r;
-    float acc = __ldg(c2 + j);
-    for (int i = 0; i < h; ++i) acc = fmaf(W2s[j * h + i], hid[m * h + i], acc);
-    t[m * tm + j * tj] *= 1.0f / (1.0f + expf(-acc));
+__device__ __forceinline__ void vector_gate_apply_rows(float* t, int ntok, const GateSmem& g, const float* hid,
+                                                       int tid, int nthreads) {
+  const int r4 = g.r / 4, hs = gate_hid_stride(g.h);
+  for (int e = tid; e < ntok * r4; e += nthreads) {
+    const int m = e / r4, q = e % r4;
+    float4 a = reinterpret_cast<const float4*>(g.c2)[q];
+    const float* hh = hid + m * hs;
+#pragma unroll 4
+    for (int i = 0; i < g.h; ++i) {
+      const float4 wv = reinterpret_cast<const float4*>(g.W2t + i * g.r)[q];
+      const float hv = hh[i];
+      a.x = fmaf(wv.x, hv, a.x);
+      a.y = fmaf(wv.y, hv, a.y);
+      a.z = fmaf(wv.z, hv, a.z);
+      a.w = fmaf(wv.w, hv, a.w);
+    }
+    float4* tp = reinterpret_cast<float4*>(t + m * g.r) + q;
+    float4 tv = *tp;
+    tv.x *= 1.0f / (1.0f + expf(-a.x));
+    tv.y *= 1.0f / (1.0f + expf(-a.y));
+    tv.z *= 1.0f / (1.0f + expf(-a.z));
+    tv.w *= 1.0f / (1.0f + expf(-a.w));
+    *tp = tv;
   }
 }
 
-// Copies the gate's W1 [h][r] and W2 [r][h] (fp32, global) into shared memory
-// with threads [tid0, tid0 + nthreads) of the block, eight loads in flight per
-// thread; the caller synchronises those threads afterwards.
-__device__ __forceinline__ void stage_gate_weights(const float* W1, const float* W2, int r, int h, float* W1s,
-                                                   float* W2s, int tid, int nthreads) {
-  const int n = h * r;
-  for (int e0 = 0; e0 < 2 * n; e0 += 8 * nthreads) {
-    float v[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int e = e0 + tid + i * nthreads;
-      v[i] = e < n ? __ldg(W1 + e) : e < 2 * n ? __ldg(W2 + (e - n)) : 0.0f;
+// Any layout: t[m][j] at t[m * tm + j * tj]; one (token, unit) pair per
+// thread, dot products as four partial sums (terms q mod 4).
+__device__ __forceinline__ void vector_gate_hidden(const float* t, int tm, int tj, int ntok, const GateSmem& g,
+                                                   float* hid, int tid, int nthreads) {
+  const int hs = gate_hid_stride(g.h);
+  for (int e = tid; e < ntok * g.h; e += nthreads) {
+    const int m = e / g.h, i = e % g.h;
+    const float* w = g.W1 + i * (g.r + 4);
+    const float* tt = t + m * tm;
+    float a0 = 0.0f, a1 = 0.0f, a2 = 0.0f, a3 = 0.0f;
+#pragma unroll 4
+    for (int j = 0; j < g.r; j += 4) {
+      a0 = fmaf(w[j], tt[j * tj], a0);
+      a1 = fmaf(w[j + 1], tt[(j + 1) * tj], a1);
+      a2 = fmaf(w[j + 2], tt[(j + 2) * tj], a2);
+      a3 = fmaf(w[j + 3], tt[(j + 3) * tj], a3);
     }
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int e = e0 + tid + i * nthreads;
-      if (e < n) W1s[e] = v[i];
-      else if (e < 2 * n) W2s[e - n] = v[i];
+    hid[m * hs + i] = fmaxf(g.c1[i] + ((a0 + a1) + (a2 + a3)), 0.0f);
+  }
+}
+__device__ __forceinline__ void vector_gate_apply(float* t, int tm, int tj, int ntok, const GateSmem& g,
+                                                  const float* hid, int tid, int nthreads) {
+  const int hs = gate_hid_stride(g.h);
+  for (int e = tid; e < ntok * g.r; e += nthreads) {
+    const int m = e / g.r, j = e % g.r;
+    const float* hh = hid + m * hs;
+    float a0 = 0.0f, a1 = 0.0f, a2 = 0.0f, a3 = 0.0f;
+    int i = 0;
+#pragma unroll 2
+    for (; i + 4 <= g.h; i += 4) {
+      a0 = fmaf(g.W2t[i * g.r + j], hh[i], a0);
+      a1 = fmaf(g.W2t[(i + 1) * g.r + j], hh[i + 1], a1);
+      a2 = fmaf(g.W2t[(i + 2) * g.r + j], hh[i + 2], a2);
+      a3 = fmaf(g.W2t[(i + 3) * g.r + j], hh[i + 3], a3);
     }
+    if (i < g.h) a0 = fmaf(g.W2t[i * g.r + j], hh[i], a0);
+    if (i + 1 < g.h) a1 = fmaf(g.W2t[(i + 1) * g.r + j], hh[i + 1], a1);
+    if (i + 2 < g.h) a2 = fmaf(g.W2t[(i + 2) * g.r + j], hh[i + 2], a2);
+    const float acc = g.c2[j] + ((a0 + a1) + (a2 + a3));
+    t[m * tm + j * tj] *= 1.0f / (1.0f + expf(-acc));
   }
 }
 

@@ -82,6 +82,11 @@ struct DecodeParams {
 // piece the MMA's k positions {2c, 2c+1, 2c+8, 2c+9} of k-step h map to the
 // lane's k = 8c + 4h + {0, 1, 2, 3}, identically for both operands.
 constexpr int kMaxSlices = 16;
+// producer scratch: cross-warp sums (t and the hidden units reuse them), then
+// the staged gate weights; the streamers' ring alone is larger
+static_assert(kWarps * 2 * 128 >= 16 * (64 + gate_hid_stride(32)), "t and hidden units fit over the cross-warp sums");
+static_assert(kWarps * kStages * 2 * 32 * 16 >= (kWarps * 2 * 128 + gate_smem_floats(64, 32)) * 4,
+              "producer scratch within the streamer's shared memory");
 
 template <int MT>
 __device__ void producer_block(const DecodeParams& p, float* smem) {
@@ -93,6 +98,10 @@ __device__ void producer_block(const DecodeParams& p, float* smem) {
   const int c0 = (int)((long long)sl * p.nchunks / S), c1 = (int)((long long)(sl + 1) * p.nchunks / S);
   const int npieces = (c1 - c0) * 4;                   // 32-k pieces of the slice
   float* red = smem;                                   // [kWarps][MT][4][32]
+  // the vector gate's weights, copied while the slice streams (every producer:
+  // which one sums the slices is known only at the end)
+  float* gs = smem + kWarps * MT * 128;                // W1 [h][r], W2 [r][h], c1 [h], c2 [r]
+  if (p.gh > 0) stage_gate_weights_async(p.gw1, p.gw2, p.gc1, p.gc2, p.r, p.gh, gs, threadIdx.x, kThreads);
 
   auto row_ptr = [&](int i) -> const __nv_bfloat16* {
     if (i < p.r) return p.A + (size_t)i * p.K;
@@ -146,6 +155,7 @@ __device__ void producer_block(const DecodeParams& p, float* smem) {
       }
   }
   if (!waited) pdl_wait();                                 // before the workspace
+  if (p.gh > 0) cp_async_wait<0>();                        // the gate weights (published by the barrier below)
   // cross-warp sum in a fixed order; this block's partial for its 16 rows
 #pragma unroll
   for (int t = 0; t < MT; ++t)
@@ -187,16 +197,14 @@ __device__ void producer_block(const DecodeParams& p, float* smem) {
   if (p.gh > 0) {
     // vector gate: t [Mpad][r] into shared memory, then one warp per token
     // forms gamma(t) and T = alpha gamma(t) t
-    float* ts = smem;                                   // [Mpad][r]
-    float* hs = ts + Mpad * p.r;                        // [Mpad][h] hidden units
-    float* w1s = hs + Mpad * p.gh;                      // [h][r]
-    float* w2s = w1s + p.gh * p.r;                      // [r][h]
-    stage_gate_weights(p.gw1, p.gw2, p.r, p.gh, w1s, w2s, threadIdx.x, kThreads);
+    float* ts = smem;                                   // [Mpad][r] (over the spent cross-warp sums)
+    float* hs = ts + Mpad * p.r;                        // [Mpad][h | 1] hidden units
+    const GateSmem gt(gs, p.r, p.gh);
     for (int e = threadIdx.x; e < Mpad * p.r; e += kThreads) ts[e] = slice_sum(e / p.r, e % p.r);
     __syncthreads();
-    vector_gate_hidden(ts, p.r, 1, Mpad, p.r, p.gh, w1s, p.gc1, hs, threadIdx.x, kThreads);
+    vector_gate_hidden_rows(ts, Mpad, gt, hs, threadIdx.x, kThreads);
     __syncthreads();
-    vector_gate_apply(ts, p.r, 1, Mpad, p.r, p.gh, w2s, p.gc2, hs, threadIdx.x, kThreads);
+    vector_gate_apply_rows(ts, Mpad, gt, hs, threadIdx.x, kThreads);
     __syncthreads();
     for (int e = threadIdx.x; e < Mpad * p.r; e += kThreads)
       p.ws_T[e] = (e / p.r < p.M) ? p.alpha * ts[e] : 0.0f;
@@ -502,6 +510,7 @@ __device__ void streamer_block(const DecodeParams& p, float* smem) {
   cp_async_wait<0>();
 
   // 4. the compensator's down-projection (published by the producers)
+  unsigned ticket = 0;            // thread 0: this block's place among the streamers past the wait
   if (COMP) {
     if (threadIdx.x == 0) {
       const uint64_t tw = globaltimer_ns();
@@ -513,6 +522,8 @@ __device__ void streamer_block(const DecodeParams& p, float* smem) {
       }
       if (!ok) record_status(&g_decode_status, DEV_ERR_TIMEOUT);
       s_flag = ok;
+      // taken here, read at the end: the round trip overlaps the epilogue
+      ticket = atomicAdd(&p.ws_sync[2], 1u);
     }
     __syncthreads();
     // T as bf16 hi + lo (T = hi + lo to ~2^-16 relative)
@@ -566,15 +577,9 @@ __device__ void streamer_block(const DecodeParams& p, float* smem) {
     }
   }
 
-  if (COMP) {
-    __syncthreads();
-    if (threadIdx.x == 0) {
-      const unsigned old = atomicAdd(&p.ws_sync[2], 1u);
-      if (old == (unsigned)(p.P - 1)) {                 // every streamer is past its wait
-        p.ws_sync[2] = 0;
-        atomicExch(&p.ws_sync[1], 0u);
-      }
-    }
+  if (COMP && threadIdx.x == 0 && ticket == (unsigned)(p.P - 1)) {   // every streamer is past its wait
+    p.ws_sync[2] = 0;
+    atomicExch(&p.ws_sync[1], 0u);
   }
 }
 

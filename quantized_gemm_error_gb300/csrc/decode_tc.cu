@@ -95,7 +95,7 @@ struct TcParams {
   float* ws_part;           // [Kp][RT][16][NP] producer-cluster partials
   float* ws_P;              // [NP][r + 1]: (A x)[j] for j < r, w_g . x at j = r
   unsigned* ws_sync;        // [0] producer row tiles published, [1] tile-CTA ticket, [2 + rt] Kp tickets
-  uint32_t off_bf, off_x16, off_xr, off_B;   // dynamic shared memory layout
+  uint32_t off_bf, off_x16, off_xr, off_B, off_gate;   // dynamic shared memory layout
 };
 
 __device__ __forceinline__ void give_up(int* abort_flag) {
@@ -260,6 +260,7 @@ __device__ void tc_tile(const CUtensorMap* tm_w, const CUtensorMap* tm_x, const 
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
   __shared__ int s_pok;
+  unsigned ticket = 0;            // thread 0: this CTA's place among the tile CTAs past the P wait
   __shared__ float s_scale[kTileRows];                     // per-channel scales of the tile rows
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -282,14 +283,19 @@ __device__ void tc_tile(const CUtensorMap* tm_w, const CUtensorMap* tm_x, const 
   uint8_t* x16_ring = smem + p.off_x16;                    // [3][64 tokens][128 B] fp16 tokens
   uint8_t* xr_ring = smem + p.off_xr;                      // [2][NP tokens][128 B] bf16 tokens (TMA)
   uint8_t* B_s = smem + p.off_B;                           // [nr][2r + 16 bytes]
-  // after the main loop: the partial [64 tokens][257] over the raw ring and
-  // the start of the weight ring, T and the gates further into the weight ring
+  float* gate_s = reinterpret_cast<float*>(smem + p.off_gate);   // vector gate: W1, W2, c1, c2
+  // after the main loop: the partial [64 tokens][260] over the raw ring and
+  // the start of the weight ring
   float* red = reinterpret_cast<float*>(smem);
   // T = alpha g t split into bf16 hi + lo (T = hi + lo to ~2^-16 relative),
   // the B operand of the epilogue's B T on warp-level MMAs: in the bf16 token
-  // ring once the last token tile is converted (NP r 4 <= 2 NP 128 bytes)
-  uint32_t* th_s = reinterpret_cast<uint32_t*>(xr_ring);            // [NP][r/2] bf16 pairs, hi
-  uint32_t* tl_s = th_s + NP * p.r / 2;                             // [NP][r/2] bf16 pairs, lo
+  // ring once the last token tile is converted (NP r 4 <= 2 NP 128 bytes);
+  // element (m, jj) holds the hi and the lo bf16 pair of T[m][2jj .. 2jj+1]
+  uint2* thl_s = reinterpret_cast<uint2*>(xr_ring);                 // [NP][r/2]
+  // vector gate: t [NP][r] fp32 over the same bytes, turned into T hi/lo in
+  // place; the hidden units in static memory
+  float* ts = reinterpret_cast<float*>(xr_ring);
+  __shared__ float hs[NP * gate_hid_stride(32)];                    // [NP][h | 1]
   const int b_stride = 2 * p.r + 16;
 
   if (threadIdx.x == 0) {
@@ -328,6 +334,9 @@ __device__ void tc_tile(const CUtensorMap* tm_w, const CUtensorMap* tm_x, const 
     }
     for (int r = threadIdx.x; r < kTileRows; r += kXWarps * 32)
       s_scale[r] = (PERCH && n0 + r < p.N) ? __half2float(__ldg(p.scales + (size_t)(n0 + r) * p.ng)) : 1.0f;
+    // the vector gate's weights, copied while the K loop runs
+    if (COMP && p.gh > 0)
+      stage_gate_weights_async(p.gw1, p.gw2, p.gc1, p.gc2, p.r, p.gh, gate_s, threadIdx.x, kXWarps * 32);
   }
   tc_fence_before();
   __syncthreads();
@@ -582,6 +591,9 @@ __device__ void tc_tile(const CUtensorMap* tm_w, const CUtensorMap* tm_x, const 
         }
         if (!pok) record_status(&g_dtc_status, DEV_ERR_TIMEOUT);
         s_pok = pok;
+        // taken here, read at the end of the kernel: the round trip overlaps
+        // the rest of the work
+        ticket = atomicAdd(&p.ws_sync[1], 1u);
       }
       named_sync(1, kXWarps * 32);
       // one round trip: every thread loads its pairs of P and, for the token of
@@ -591,19 +603,9 @@ __device__ void tc_tile(const CUtensorMap* tm_w, const CUtensorMap* tm_x, const 
       const bool pok = s_pok != 0;
       constexpr int kPer = 8;                              // pairs per thread and pass (r <= 32: one pass)
       if (p.gh > 0) {
-        // vector gate: once the MMAs are done the second fp16 weight slot is
-        // scratch for t [NP][r]; one warp per token forms gamma(t), then
-        // T = alpha gamma(t) t as bf16 hi + lo
-        bool vok = mbar_wait(smem_u32(&acc_full), 0, kPipeWaitNs);
-        vok = __all_sync(0xffffffffu, vok && !s_abort);
-        if (!vok) give_up(&s_abort);
-        // slot 1 holds t [NP][r] and the staged W1 [h][r], W2 [r][h] (<= 32 KB
-        // for r <= 64, h <= 32); hidden units and the gate in static memory
-        float* ts = reinterpret_cast<float*>(bf_ring + kBfBytes);       // [NP][r]
-        float* w1s = ts + NP * p.r;
-        float* w2s = w1s + p.gh * p.r;
-        __shared__ float hs[NP * 32];                                    // [NP][h] hidden units
-        stage_gate_weights(p.gw1, p.gw2, p.r, p.gh, w1s, w2s, tid, kXWarps * 32);
+        // vector gate: t = P [NP][r] into the token ring now; gamma(t) and T
+        // (over the same bytes) are formed by warps 0-19 once the accumulator
+        // is drained
         for (int e0 = 0; e0 < NP * p.r; e0 += kPer * kXWarps * 32) {
           float v[kPer];
 #pragma unroll
@@ -617,20 +619,7 @@ __device__ void tc_tile(const CUtensorMap* tm_w, const CUtensorMap* tm_x, const 
             if (e < NP * p.r) ts[e] = v[i];
           }
         }
-        named_sync(1, kXWarps * 32);
-        vector_gate_hidden(ts, p.r, 1, NP, p.r, p.gh, w1s, p.gc1, hs, tid, kXWarps * 32);
-        named_sync(1, kXWarps * 32);
-        vector_gate_apply(ts, p.r, 1, NP, p.r, p.gh, w2s, p.gc2, hs, tid, kXWarps * 32);
-        named_sync(1, kXWarps * 32);
-        for (int e = tid; e < NP * half_r; e += kXWarps * 32) {
-          const int m = e / half_r, jj = e % half_r;
-          const bool on = pok && m < p.M;
-          const float ta = on ? p.alpha * ts[m * p.r + 2 * jj] : 0.0f;
-          const float tb = on ? p.alpha * ts[m * p.r + 2 * jj + 1] : 0.0f;
-          const float ha = __bfloat162float(__float2bfloat16_rn(ta)), hb = __bfloat162float(__float2bfloat16_rn(tb));
-          th_s[e] = pack_bf16x2(ha, hb);
-          tl_s[e] = pack_bf16x2(ta - ha, tb - hb);
-        }
+        cp_async_wait<0>();                      // the staged gate weights (published by the epilogue's barrier)
       }
       for (int e0 = 0; p.gh == 0 && e0 < NP * half_r; e0 += kPer * kXWarps * 32) {
         float pa[kPer], pb[kPer], pg[kPer];
@@ -654,19 +643,11 @@ __device__ void tc_tile(const CUtensorMap* tm_w, const CUtensorMap* tm_x, const 
             const float gt = (pok && t < p.M) ? p.alpha / (1.0f + expf(-(pg[i] + p.b_g))) : 0.0f;
             const float ta = gt * pa[i], tb = gt * pb[i];
             const float ha = __bfloat162float(__float2bfloat16_rn(ta)), hb = __bfloat162float(__float2bfloat16_rn(tb));
-            th_s[e] = pack_bf16x2(ha, hb);
-            tl_s[e] = pack_bf16x2(ta - ha, tb - hb);
+            thl_s[e] = make_uint2(pack_bf16x2(ha, hb), pack_bf16x2(ta - ha, tb - hb));
           }
         }
       }
       named_sync(1, kXWarps * 32);
-      if (tid == 0) {
-        const unsigned old = atomicAdd(&p.ws_sync[1], 1u);
-        if (old == (unsigned)(p.n_consumers - 1)) {        // every tile CTA has read P
-          p.ws_sync[1] = 0;
-          atomicExch(&p.ws_sync[0], 0u);
-        }
-      }
     }
   }
 
@@ -676,7 +657,29 @@ __device__ void tc_tile(const CUtensorMap* tm_w, const CUtensorMap* tm_x, const 
     // before the cluster reads it: one (16-row, 8-token) tile per warp at a
     // time on mma.sync (B rows as A, T hi/lo as B).  Warps 0-19 only: the
     // TMA and MMA warps never reach this barrier.
-    named_sync(2, kTmaWarp * 32);                          // drained partial, T and B rows in place
+    named_sync(2, kTmaWarp * 32);                          // drained partial, T (or t) and B rows in place
+    if (p.gh > 0) {
+      // vector gate over warps 0-19: T = alpha gamma(t) t, each pair of t
+      // turned into its hi/lo pair in place (uniform branch: every barrier
+      // below is reached by all 640 threads)
+      constexpr int kEpi = kTmaWarp * 32;
+      const GateSmem gt(gate_s, p.r, p.gh);
+      vector_gate_hidden_rows(ts, NP, gt, hs, threadIdx.x, kEpi);
+      named_sync(2, kEpi);
+      vector_gate_apply_rows(ts, NP, gt, hs, threadIdx.x, kEpi);
+      named_sync(2, kEpi);
+      const int half_r = p.r / 2;
+      const bool pok = s_pok != 0;
+      for (int e = threadIdx.x; e < NP * half_r; e += kEpi) {
+        const int m = e / half_r;
+        const bool on = pok && m < p.M;
+        const float2 tv = reinterpret_cast<const float2*>(ts)[e];     // t[m][2jj], t[m][2jj + 1]
+        const float ta = on ? p.alpha * tv.x : 0.0f, tb = on ? p.alpha * tv.y : 0.0f;
+        const float ha = __bfloat162float(__float2bfloat16_rn(ta)), hb = __bfloat162float(__float2bfloat16_rn(tb));
+        thl_s[e] = make_uint2(pack_bf16x2(ha, hb), pack_bf16x2(ta - ha, tb - hb));
+      }
+      named_sync(2, kEpi);
+    }
     if (!s_abort) {
       const int g = lane >> 2, c = lane & 3;
       const int rtiles = nr / 16, ttiles = (p.M + 7) / 8;
@@ -686,15 +689,15 @@ __device__ void tc_tile(const CUtensorMap* tm_w, const CUtensorMap* tm_x, const 
         const uint8_t* blo = B_s + (rt * 16 + g) * b_stride;
         const uint8_t* bhi = blo + 8 * b_stride;
         const int tok = tt * 8 + g;
-        const uint32_t* th = th_s + tok * (p.r / 2);
-        const uint32_t* tl = tl_s + tok * (p.r / 2);
+        const uint2* thl = thl_s + tok * (p.r / 2);
         for (int j0 = 0; j0 < p.r; j0 += 16) {
           const uint32_t a0 = *reinterpret_cast<const uint32_t*>(blo + (j0 + 2 * c) * 2);
           const uint32_t a1 = *reinterpret_cast<const uint32_t*>(bhi + (j0 + 2 * c) * 2);
           const uint32_t a2 = *reinterpret_cast<const uint32_t*>(blo + (j0 + 2 * c + 8) * 2);
           const uint32_t a3 = *reinterpret_cast<const uint32_t*>(bhi + (j0 + 2 * c + 8) * 2);
-          mma_bf16_16816(bt, a0, a1, a2, a3, th[j0 / 2 + c], th[j0 / 2 + c + 4]);
-          mma_bf16_16816(bt, a0, a1, a2, a3, tl[j0 / 2 + c], tl[j0 / 2 + c + 4]);
+          const uint2 t0 = thl[j0 / 2 + c], t1 = thl[j0 / 2 + c + 4];
+          mma_bf16_16816(bt, a0, a1, a2, a3, t0.x, t1.x);
+          mma_bf16_16816(bt, a0, a1, a2, a3, t0.y, t1.y);
         }
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
@@ -747,6 +750,10 @@ __device__ void tc_tile(const CUtensorMap* tm_w, const CUtensorMap* tm_x, const 
       }
     }
   }
+  if (COMP && threadIdx.x == 0 && ticket == (unsigned)(p.n_consumers - 1)) {   // every tile CTA has seen P
+    p.ws_sync[1] = 0;
+    atomicExch(&p.ws_sync[0], 0u);
+  }
   tc_fence_before();
   cluster_sync();                                          // peers are done reading this CTA
   if (warp == kMmaWarp) {
@@ -795,17 +802,17 @@ int np_for(int M) { return M <= 16 ? 16 : M <= 32 ? 32 : 64; }
 
 // ---------------------------------------------------------------- plan --
 struct TcPlan {
-  int device, N, K, G, rank, comp, NP;     // key
+  int device, N, K, G, rank, comp, NP, gh;     // key
   int S, RT, Kp, tiles, units, BF;
   size_t smem;
-  uint32_t off_bf, off_x16, off_xr, off_B;
+  uint32_t off_bf, off_x16, off_xr, off_B, off_gate;
   size_t off_sync, off_part, off_P, total;
   TcKernel fn;
 };
 
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
-size_t tile_smem(int NP, int BF, int nr_max, int rank, TcPlan* c) {
+size_t tile_smem(int NP, int BF, int nr_max, int rank, int gate_floats, TcPlan* c) {
   size_t off = (size_t)kRawStages * kRawBytes;
   c->off_bf = (uint32_t)off;
   off += (size_t)BF * kBfBytes;
@@ -815,12 +822,15 @@ size_t tile_smem(int NP, int BF, int nr_max, int rank, TcPlan* c) {
   off += (size_t)kXrStages * NP * 128;
   c->off_B = (uint32_t)off;
   off += (size_t)align_up(nr_max, 16) * (2 * std::max(rank, 8) + 16);   // whole 16-row MMA tiles
+  c->off_gate = (uint32_t)off;
+  off += (size_t)gate_floats * 4;
   return align_up(off, 1024) + 1024;            // + alignment slack of the dynamic base
 }
 
 int build_tc_plan(const spear_w4_layer& L, int NP, bool comp, const DeviceInfo& di, TcPlan* pl) {
   const bool has_rank = L.rank > 0;             // the split depends on this, not on comp_enabled
   const bool perch = L.group_size == L.K;
+  const int gate_floats = (comp && L.gate_hidden > 0) ? gate_smem_floats(L.rank, L.gate_hidden) : 0;
   pl->NP = NP;
   pl->tiles = (L.N + kTileRows - 1) / kTileRows;
   pl->units = (L.K + kUnitK - 1) / kUnitK;
@@ -845,10 +855,10 @@ int build_tc_plan(const spear_w4_layer& L, int NP, bool comp, const DeviceInfo& 
     const int nr_max = (kTileRows + S - 1) / S;
     // three fp16 weight steps in flight when they fit, else two
     c.BF = kMaxBfStages;
-    size_t sm = tile_smem(NP, c.BF, nr_max, L.rank, &c);
+    size_t sm = tile_smem(NP, c.BF, nr_max, L.rank, gate_floats, &c);
     if (sm > smem_limit) {
       c.BF = 2;
-      sm = tile_smem(NP, c.BF, nr_max, L.rank, &c);
+      sm = tile_smem(NP, c.BF, nr_max, L.rank, gate_floats, &c);
     }
     c.smem = std::max(sm, prod_smem);
     if (c.smem > smem_limit) continue;
@@ -911,12 +921,13 @@ int get_tc_plan(const spear_w4_layer& L, int M, TcPlan* out) {
   if (int rc = device_info(&di)) return rc;
   const int NP = np_for(M);
   const int comp = (L.comp_enabled && L.rank > 0) ? 1 : 0;
+  const int gh = comp ? L.gate_hidden : 0;     // the vector gate's staged weights take shared memory
   static std::mutex mu;
   static std::vector<TcPlan> cache;
   std::lock_guard<std::mutex> lk(mu);
   for (const TcPlan& p : cache)
     if (p.device == di.device && p.N == L.N && p.K == L.K && p.G == L.group_size && p.rank == L.rank &&
-        p.comp == comp && p.NP == NP) {
+        p.comp == comp && p.NP == NP && p.gh == gh) {
       *out = p;
       return SPEAR_OK;
     }
@@ -926,7 +937,7 @@ int get_tc_plan(const spear_w4_layer& L, int M, TcPlan* out) {
     fprintf(stderr, "[spear] decode tc plan N=%d K=%d G=%d rank=%d comp=%d NP=%d: S=%d RT=%d Kp=%d tiles=%d "
             "units=%d BF=%d smem=%zu grid=%d\n", L.N, L.K, L.group_size, L.rank, comp, NP, p.S, p.RT, p.Kp,
             p.tiles, p.units, p.BF, p.smem, (p.tiles + p.RT * p.Kp) * p.S);
-  p.device = di.device; p.N = L.N; p.K = L.K; p.G = L.group_size; p.rank = L.rank; p.comp = comp;
+  p.device = di.device; p.N = L.N; p.K = L.K; p.G = L.group_size; p.rank = L.rank; p.comp = comp; p.gh = gh;
   if (cache.size() > 4096) cache.clear();
   cache.push_back(p);
   *out = p;
@@ -976,7 +987,7 @@ int launch_decode_tc(const spear_w4_layer& L, const uint16_t* x, int M, void* y,
   p.ws_sync = reinterpret_cast<unsigned*>(base + pl.off_sync);
   p.ws_part = reinterpret_cast<float*>(base + pl.off_part);
   p.ws_P = reinterpret_cast<float*>(base + pl.off_P);
-  p.off_bf = pl.off_bf; p.off_x16 = pl.off_x16; p.off_xr = pl.off_xr; p.off_B = pl.off_B;
+  p.off_bf = pl.off_bf; p.off_x16 = pl.off_x16; p.off_xr = pl.off_xr; p.off_B = pl.off_B; p.off_gate = pl.off_gate;
 
   if (int rc = ensure_smem_limit(reinterpret_cast<const void*>(pl.fn), pl.smem)) return rc;
   cudaLaunchConfig_t cfg{};

@@ -417,6 +417,11 @@ __global__ void __launch_bounds__(kCdThreads) comp_down_kernel(const CompDownPar
   const int tok0 = (int)(blockIdx.x / CK) * kCdTok;
   const int npieces = p.K / 32;
   const int pc0 = rank * npieces / CK, pc1 = (rank + 1) * npieces / CK;
+  // the vector gate's weights (h <= 32, r <= 64), copied by rank 0 while its
+  // K slice streams
+  __shared__ __align__(16) float gate_s[gate_smem_floats(64, 32)];
+  if (rank == 0 && p.gh > 0)
+    stage_gate_weights_async(p.gw1, p.gw2, p.gc1, p.gc2, p.r, p.gh, gate_s, threadIdx.x, kCdThreads);
   float acc[RT][kCdMT][4];
 #pragma unroll
   for (int rt = 0; rt < RT; ++rt)
@@ -506,15 +511,15 @@ __global__ void __launch_bounds__(kCdThreads) comp_down_kernel(const CompDownPar
     }
   }
   cluster_sync();                                          // peers are done reading; rank 0's sums in place
-  __shared__ float hid[kCdTok * 32];                       // [16 tokens][h]
-  __shared__ float gw1s[32 * 64], gw2s[64 * 32];           // the gate's W1, W2 (h <= 32, r <= 64)
+  __shared__ float hid[kCdTok * gate_hid_stride(32)];      // [16 tokens][h | 1]
   if (rank == 0 && p.gh > 0) {
     // vector gate on the summed partial (part[j][m]): t scaled in place by gamma(t)
-    stage_gate_weights(p.gw1, p.gw2, p.r, p.gh, gw1s, gw2s, threadIdx.x, kCdThreads);
+    const GateSmem gt(gate_s, p.r, p.gh);
+    cp_async_wait<0>();
     __syncthreads();
-    vector_gate_hidden(&part[0][0], 1, kCdTok, kCdTok, p.r, p.gh, gw1s, p.gc1, hid, threadIdx.x, kCdThreads);
+    vector_gate_hidden(&part[0][0], 1, kCdTok, kCdTok, gt, hid, threadIdx.x, kCdThreads);
     __syncthreads();
-    vector_gate_apply(&part[0][0], 1, kCdTok, kCdTok, p.r, p.gh, gw2s, p.gc2, hid, threadIdx.x, kCdThreads);
+    vector_gate_apply(&part[0][0], 1, kCdTok, kCdTok, gt, hid, threadIdx.x, kCdThreads);
     __syncthreads();
   }
   if (rank == 0) {
