@@ -26,6 +26,11 @@
 //    up-projection: extra K steps with A = [T_hi | T_lo] (the gated
 //    down-projection split into two bf16 halves) and B = the factor B, into a
 //    second accumulator that the epilogue adds unscaled.
+//    Grids of a few 128-token tiles (small M) split K over a cluster of 2 or
+//    4 CTAs: each dequantises its share of the 256-row slab, drains its
+//    partial (scaled, with the correction on rank 0) into its own shared
+//    memory, and finishes 256 / KS output columns by summing the partials of
+//    the cluster in rank order through distributed shared memory.
 //  * comp_down: T[m][j] = alpha * g_m * (A x_m)[j], g_m = sigmoid(w_g . x_m + b_g),
 //    written as bf16 hi/lo pairs; mma.sync over token tiles, one pass over X.
 //  * comp_up_add: Y[m][n] += sum_j T[m][j] B[n][j] in place ("stream" mode:
@@ -80,7 +85,12 @@ struct GemmParams {
   int r;
   int t_row_bytes;      // bytes per T2 row box (<= 128)
   int b_row_bytes;      // bytes per B row (2r)
+  int ks;               // CTAs of a cluster splitting K (1, 2 or 4; 128-token tiles only)
 };
+
+// K split: the partial accumulators of a cluster meet in shared memory,
+// [128 tokens][256 + 4] fp32 per CTA (16-byte rows, conflict-free)
+constexpr int kRedStride = kBN + 4;
 
 __device__ __forceinline__ uint32_t sw_layout(int row_bytes) {
   return row_bytes >= 128 ? LAYOUT_SW128 : row_bytes == 64 ? LAYOUT_SW64 : LAYOUT_SW32;
@@ -102,7 +112,14 @@ w4_gemm_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n0 = blockIdx.x * kBN, m0 = blockIdx.y * BM;
   const int k_stages = p.K / kBK;
-  const int total_stages = k_stages + p.comp_stages;
+  // K split over a cluster of KS CTAs: this CTA's main K steps are [kb, ke);
+  // the fused correction's steps go to rank 0
+  const int KS = p.ks;
+  const int krank = KS > 1 ? (int)cluster_ctarank() : 0;
+  const int kb = (int)((long long)krank * k_stages / KS), ke = (int)((long long)(krank + 1) * k_stages / KS);
+  const int nmain = ke - kb;
+  const int ncomp = krank == 0 ? p.comp_stages : 0;
+  const int total_stages = nmain + ncomp;
 
   auto x_slot = [&](int s) { return smem + s * kStageBytes; };
   auto w_slot = [&](int s) { return smem + s * kStageBytes + kXBytes; };
@@ -147,12 +164,13 @@ w4_gemm_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
           break;
         }
         const uint32_t full = smem_u32(&bar_full[slot]);
-        if (s < k_stages) {
+        if (s < nmain) {
+          const int sg = kb + s;        // K step
           mbar_arrive_expect_tx(full, kXBytes + kRawBytes);
-          tma_load_2d(smem_u32(x_slot(slot)), &tm_x, s * kBK, m0, full);
-          tma_load_2d(smem_u32(raw_slot(slot)), &tm_wq, s * (kBK / 2), n0, full);
+          tma_load_2d(smem_u32(x_slot(slot)), &tm_x, sg * kBK, m0, full);
+          tma_load_2d(smem_u32(raw_slot(slot)), &tm_wq, sg * (kBK / 2), n0, full);
         } else {
-          const int j = s - k_stages;   // compensator step: T box j and the factor B
+          const int j = s - nmain;      // compensator step: T box j and the factor B
           mbar_arrive_expect_tx(full, BM * p.t_row_bytes + kBN * p.b_row_bytes);
           tma_load_2d(smem_u32(x_slot(slot)), &tm_t, j * 64, m0, full);
           tma_load_2d(smem_u32(w_slot(slot)), &tm_b, 0, n0, full);
@@ -175,11 +193,11 @@ w4_gemm_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
         const int slot = s % kStages;
         const uint32_t ph = (s / kStages) & 1;
         ok = mbar_wait(smem_u32(&bar_full[slot]), ph, kWaitNs) && !s_abort;
-        if (ok && s < k_stages) ok = mbar_wait(smem_u32(&bar_cvt[slot]), ph, kWaitNs) && !s_abort;
+        if (ok && s < nmain) ok = mbar_wait(smem_u32(&bar_cvt[slot]), ph, kWaitNs) && !s_abort;
         if (!ok) { give_up(); break; }
         tc_fence_after();
         const uint32_t xa = smem_u32(x_slot(slot)), wa = smem_u32(w_slot(slot));
-        if (s < k_stages) {
+        if (s < nmain) {
 #pragma unroll
           for (int k = 0; k < kBK / 16; ++k) {
             const uint64_t bd = smem_desc(wa + 32 * k, 1024, LAYOUT_SW128);
@@ -193,7 +211,7 @@ w4_gemm_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
           // A = T box j (columns 64j.. of [T_hi | T_lo]); B = the factor B (k = rank).
           // BM = 128: accumulated into the second accumulator (columns 256..511);
           // BM = 256 (group scales only): added into the main accumulators.
-          const int j = s - k_stages;
+          const int j = s - nmain;
           const uint32_t a_layout = sw_layout(p.t_row_bytes), b_layout = sw_layout(p.b_row_bytes);
           for (int i = 0; i < p.t_row_bytes / 32; ++i) {
             const int col = 64 * j + 16 * i;                 // column of [T_hi | T_lo]
@@ -237,12 +255,12 @@ w4_gemm_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
       return __half_as_ushort(__ldg(p.scales + (size_t)n * p.ng + gi));
     };
     bool ok = true;
-    auto convert = [&](int s, uint32_t zb, uint32_t sb) {
+    auto convert = [&](int s, uint32_t zb, uint32_t sb) {      // s: this CTA's step (K step kb + s)
       const int slot = s % kStages;
       ok = __all_sync(0xffffffffu, ok && mbar_wait(smem_u32(&bar_full[slot]), (s / kStages) & 1, kWaitNs) &&
                                        !s_abort);
       if (ok) {
-        const int gi = s / stages_per_group;
+        const int gi = (kb + s) / stages_per_group;
         const uint32_t z = (gi & 1) ? (zb >> 4) : (zb & 15u);
         const uint32_t s2 = sb * 0x00010001u;                      // fp16x2 of the group scale
         const uint8_t* raw = raw_slot(slot) + ct * 32;
@@ -276,19 +294,21 @@ w4_gemm_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
     };
     // zero points and scales travel 4 groups ahead of their use in named
     // registers (slot = group mod 4, never indexed at run time)
-    uint32_t z0 = load_z(0), z1 = load_z(1), z2 = load_z(2), z3 = load_z(3);
-    uint32_t c0 = load_s(0), c1 = load_s(1), c2 = load_s(2), c3 = load_s(3);
+    // (groups gb .. ge - 1 hold this CTA's K steps)
+    const int gb = kb / stages_per_group, ge = (ke + stages_per_group - 1) / stages_per_group;
+    uint32_t z0 = load_z(gb), z1 = load_z(gb + 1), z2 = load_z(gb + 2), z3 = load_z(gb + 3);
+    uint32_t c0 = load_s(gb), c1 = load_s(gb + 1), c2 = load_s(gb + 2), c3 = load_s(gb + 3);
     auto group = [&](int gi, uint32_t& zs, uint32_t& cs) {
-      const int s0 = gi * stages_per_group, s1 = std::min(s0 + stages_per_group, k_stages);
-      for (int s = s0; s < s1; ++s) convert(s, zs, cs);
+      const int s0 = std::max(gi * stages_per_group, kb), s1 = std::min((gi + 1) * stages_per_group, ke);
+      for (int s = s0; s < s1; ++s) convert(s - kb, zs, cs);
       zs = load_z(gi + 4);
       cs = load_s(gi + 4);
     };
-    for (int g0 = 0; g0 < ngroups; g0 += 4) {
-      if (g0 + 0 < ngroups) group(g0 + 0, z0, c0);
-      if (g0 + 1 < ngroups) group(g0 + 1, z1, c1);
-      if (g0 + 2 < ngroups) group(g0 + 2, z2, c2);
-      if (g0 + 3 < ngroups) group(g0 + 3, z3, c3);
+    for (int g0 = gb; g0 < ge; g0 += 4) {
+      if (g0 + 0 < ge) group(g0 + 0, z0, c0);
+      if (g0 + 1 < ge) group(g0 + 1, z1, c1);
+      if (g0 + 2 < ge) group(g0 + 2, z2, c2);
+      if (g0 + 3 < ge) group(g0 + 3, z3, c3);
     }
 
     // epilogue: TMEM lanes 32*(warp%4) .. +31 are this warp's rows (tokens);
@@ -301,7 +321,7 @@ w4_gemm_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
       const int c_begin = ((warp - 2) >> 2) * (kBN / 2);
       // BM = 256: the second accumulator (columns 256..) holds tokens 128..255
       // and the correction is already in both
-      const bool sep_comp = kMH == 1 && p.comp_stages;
+      const bool sep_comp = kMH == 1 && ncomp > 0;
 #pragma unroll 1
       for (int it = 0; it < kMH * (kBN / 2 / 32); ++it) {
         const int mh = it / (kBN / 2 / 32), cch = c_begin / 32 + it % (kBN / 2 / 32);
@@ -334,6 +354,15 @@ w4_gemm_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
 #pragma unroll
           for (int i = 0; i < 32; ++i) v[i] += __uint_as_float(rc[i]);
         }
+        if (KS > 1) {
+          // K split: this CTA's partial (scaled, with the correction on rank 0)
+          // into its own shared memory; the cluster sums it below
+          float* prow = reinterpret_cast<float*>(smem) + (32 * q + lane) * kRedStride + cch * 32;
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            reinterpret_cast<float4*>(prow)[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+          continue;
+        }
         if (tok < p.M) {
           if (p.out_f32) {
             float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.y) + (size_t)tok * p.N + n);
@@ -351,6 +380,39 @@ w4_gemm_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
     }
   }
 
+  if (KS > 1) {
+    // every thread of the cluster: rank R finishes output columns
+    // [R 256 / KS, (R + 1) 256 / KS) of the tile, the partials summed in rank
+    // order (16-byte shared-memory loads across the cluster, all in flight)
+    cluster_sync();                                        // every partial is in place
+    if (!s_abort) {
+      const int c4n = kBN / KS / 4, cb = krank * (kBN / KS);
+      const uint32_t red_base = smem_u32(smem);
+      const bool f32 = p.out_f32 != 0;
+      for (int idx = threadIdx.x; idx < BM * c4n; idx += kGemmThreads) {
+        const int t = idx / c4n, col = cb + 4 * (idx % c4n);
+        const int tok = m0 + t, n = n0 + col;
+        const uint32_t la = red_base + (uint32_t)(t * kRedStride + col) * 4u;
+        float4 pv[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          if (q < KS) pv[q] = dsmem_ld_f32x4(dsmem_addr(la, (uint32_t)q));
+        float4 v = pv[0];
+#pragma unroll
+        for (int q = 1; q < 4; ++q)
+          if (q < KS) { v.x += pv[q].x; v.y += pv[q].y; v.z += pv[q].z; v.w += pv[q].w; }
+        if (tok >= p.M || n >= p.N) continue;               // N is a multiple of 64: n + 3 < N
+        const size_t o = (size_t)tok * p.N + n;
+        if (f32) {
+          *reinterpret_cast<float4*>(reinterpret_cast<float*>(p.y) + o) = v;
+        } else {
+          *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(p.y) + o) =
+              make_uint2(pack_bf16x2(v.x, v.y), pack_bf16x2(v.z, v.w));
+        }
+      }
+    }
+    cluster_sync();                                        // peers are done reading this CTA
+  }
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
@@ -628,6 +690,16 @@ int pick_bm(int M, int N, bool perch_fused, int num_sms) {
   return 135 * w256 < 100 * w128 ? 256 : 128;
 }
 
+// K split for grids that would leave most SMs idle (a few 128-token tiles:
+// each CTA would dequantise a whole 256-row slab of the weight alone): up to
+// 4 CTAs of a cluster take equal K ranges while the grid stays within one wave.
+int pick_ks(int BM, int ctas, int k_steps, int num_sms) {
+  int ks = 1;
+  if (BM != 128) return ks;
+  while (ks < 4 && 2 * ks * ctas <= num_sms && k_steps >= 16 * ks) ks *= 2;
+  return ks;
+}
+
 int launch_gemm(const spear_w4_layer& L, const __half* x16, int M, void* y, int out_f32, const __nv_bfloat16* T2,
                 int r_fused, cudaStream_t st) {
   DeviceInfo di;
@@ -666,11 +738,26 @@ int launch_gemm(const spear_w4_layer& L, const __half* x16, int M, void* y, int 
   auto fn = BM == 256 ? w4_gemm_tc<256> : w4_gemm_tc<128>;
   const size_t smem = BM == 256 ? (size_t)TileCfg<256>::kStages * TileCfg<256>::kStageBytes + 1024
                                 : (size_t)TileCfg<128>::kStages * TileCfg<128>::kStageBytes + 1024;
+  static_assert((size_t)128 * kRedStride * 4 <= (size_t)TileCfg<128>::kStages * TileCfg<128>::kStageBytes,
+                "the K-split partial fits in the 128-token tile's stage buffers");
   if (int rc = ensure_smem_limit(reinterpret_cast<const void*>(fn), smem)) return rc;
   dim3 grid((L.N + kBN - 1) / kBN, (M + BM - 1) / BM);
   if (grid.y > 65535) return fail(SPEAR_ERR_UNSUPPORTED, "prefill: M=%d too large", M);
-  fn<<<grid, kGemmThreads, smem, st>>>(tm_x, tm_wq, tm_t, tm_b, p);
-  return cuda_check(cudaGetLastError(), "prefill gemm launch");
+  p.ks = pick_ks(BM, (int)(grid.x * grid.y), L.K / kBK, di.num_sms);
+  if (log_plans() && p.ks > 1) fprintf(stderr, "[spear] prefill gemm: K split over %d CTAs\n", p.ks);
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(grid.x, grid.y, p.ks);
+  cfg.blockDim = dim3(kGemmThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 1;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = p.ks;
+  cfg.attrs = attr;
+  cfg.numAttrs = p.ks > 1 ? 1 : 0;
+  return cuda_check(cudaLaunchKernelEx(&cfg, fn, tm_x, tm_wq, tm_t, tm_b, p), "prefill gemm launch");
 }
 
 int launch_comp_down(const spear_w4_layer& L, const uint16_t* x, int M, __nv_bfloat16* T2, __half* x16,
