@@ -286,6 +286,36 @@ def test_vector_gate_reduces_to_closed_forms():
                                atol=1e-14)
 
 
+
+def test_vector_gate_routes_single_components():
+    """Sparse W1, W2 that route one rank component through one hidden unit each
+    give gamma in closed form from t = A x (a textbook matmul): a transposed W1
+    or W2, a dropped c1, c2 or relu changes which components move, or how."""
+    lay, rng = make_layer(24, 256, 8, seed=11)
+    x = make_tokens(rng, 32, 256)
+    L = _layer_dict(lay, 128, False)
+    t = bf16_bits_to_f32(x).astype(np.float64) @ bf16_bits_to_f32(lay.A).astype(np.float64).T   # [M][8]
+    W1 = np.zeros((2, 8), np.float32)
+    W1[0, 3] = 1.0                       # hidden 0 = relu(t_3 + 0.05)
+    W1[1, 5] = -1.0                      # hidden 1 = relu(-t_5 - 0.02)
+    c1 = np.array([0.05, -0.02], np.float32)
+    W2 = np.zeros((8, 2), np.float32)
+    W2[6, 0] = 8.0                       # gamma_6 = sigmoid(8 hidden_0 + c2_6)
+    W2[1, 1] = -6.0                      # gamma_1 = sigmoid(-6 hidden_1 + c2_1)
+    c2 = np.linspace(-1.5, 1.5, 8).astype(np.float32)
+    _, gam = oracle.linear_vector_gate(L, x, W1, c1, W2, c2)
+    sig = lambda v: 1.0 / (1.0 + np.exp(-v))
+    h0 = np.maximum(t[:, 3] + float(c1[0]), 0.0)
+    h1 = np.maximum(-t[:, 5] + float(c1[1]), 0.0)
+    want = np.tile(sig(c2.astype(np.float64)), (x.shape[0], 1))
+    want[:, 6] = sig(8.0 * h0 + float(c2[6]))
+    want[:, 1] = sig(-6.0 * h1 + float(c2[1]))
+    # both sides of each relu occur among the tokens
+    assert (h0 > 0).any() and (h0 == 0).any()
+    assert (h1 > 0).any() and (h1 == 0).any()
+    np.testing.assert_allclose(gam, want, rtol=1e-6, atol=0)
+
+
 # -------------------------------------------------------- module selection
 
 def test_layer_select_worked_example():
