@@ -22,14 +22,17 @@
 //   warps 4-19 turn each 64-k step of int4 codes into (u - z) s in fp16 (one
 //             rounding; the nibble enters as the mantissa of 1024 or 64, so
 //             the subtraction of 1024 + z or 64 + z is exact), written in the
-//             tensor core's swizzled K-major layout;
+//             tensor core's swizzled K-major layout; after the last MMA they
+//             drain the accumulator into this CTA's partial in shared memory;
 //   warps 0-3 convert the token tile to fp16 (exact for |x| < 65504, larger
-//             values are reported), later drain the accumulator;
+//             values are reported), then read the published P and form T
+//             (scalar gate) or load t = A x (vector gate) in the spent ring;
 //   warp 21   one thread issues tcgen05.mma with the tokens as the 64-row A
 //             operand and the weights as the 256-column B operand:
 //             D[64 x 256] (+)= X[64 x 16] W[256 x 16]^T, fp32 in tensor memory.
-// Epilogue: the S partials are summed in a fixed order through DSMEM, each CTA
-// of the cluster finishing 256 / S rows: + B T from the published P, then y.
+// Epilogue: warps 0-19 run the vector gate's MLP (if any) and add B T into the
+// partial rows this CTA finishes; then the S partials of the cluster are
+// summed in a fixed order through DSMEM, each CTA finishing 256 / S rows of y.
 //
 // Shared memory carries every weight several times (int4 in, fp16 out, fp16
 // read by the tensor core: ~10 bytes per int4 byte), which bounds this kernel

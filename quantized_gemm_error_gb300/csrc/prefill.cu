@@ -4,13 +4,13 @@
 //
 // Kernels
 //  * w4_gemm_tc: Y[M][N] = X[M][K] * dequant(Wq)^T on the 5th-generation tensor
-//    cores, fp16 operands, fp32 accumulation.  One 128 (tokens) x 256
+//    cores, fp16 operands, fp32 accumulation.  One 128- or 256-token x 256
 //    (outputs) tile per thread block; K in steps of 64.  A TMA warp loads the
-//    fp16 copy of the X tile (128-byte swizzle) and the raw int4 tile; four
+//    fp16 copy of the X tile (128-byte swizzle) and the raw int4 tile; eight
 //    converter warps expand the int4 tile to fp16 straight into the tensor
-//    core's swizzled K-major layout; one thread issues tcgen05.mma into a
-//    128 x 256 fp32 accumulator in tensor memory; the same four warps then
-//    drain it (tcgen05.ld) and store Y.
+//    core's swizzled K-major layout; one thread issues tcgen05.mma into fp32
+//    accumulators in tensor memory; the same eight warps then drain them
+//    (tcgen05.ld) and store Y.
 //      - per-channel scales: the tile holds the exact integers (u - z) and the
 //        fp32 scale of each output column is applied in the epilogue;
 //      - group scales: the tile holds (u - z) * s rounded once to fp16
