@@ -149,9 +149,10 @@ __device__ __forceinline__ void nibbles_to_bf16x2_biased(uint32_t w, uint32_t (&
 //   hidden:  hid[m][i] = relu(c1[i] + sum_j W1[i][j] t[m][j])
 //   apply:   t[m][j] *= sigmoid(c2[j] + sum_i W2[j][i] hid[m][i])
 // The fp32 weights are read from the shared-memory copy that
-// stage_gate_weights_async makes (a global load inside these loops costs an L2
-// round trip per pair while the weight stream runs), laid out so that the
-// loads of a warp hit distinct banks:
+// stage_gate_weights_async makes, laid out so that the loads of a warp hit
+// distinct banks (W1 [h][r] and W2 [r][h] as given put a warp's rows a
+// multiple of 32 floats apart: 8-way conflicts that made these loops cost
+// more than the rest of the tensor-core decode's epilogue):
 //   G = [ W1 [h][r + 4] (rows padded) | W2^T [h][r] | c2 [r] | c1 [h] ],
 // every part 16-byte aligned when G is (the rank is a multiple of 16).  The
 // hidden units sit at hid[m * gate_hid_stride(h) + i].  Every (token, unit)
