@@ -45,6 +45,11 @@ def decode_kernel_name(M: int) -> str:
     return "decode_tc_kernel" if M >= TC_MIN_M else "decode_kernel"
 
 
+# the files each decode kernel is compiled from (its own and the shared headers)
+KERNEL_SOURCES = {"decode_kernel": ("decode.cu", "common.cuh"),
+                  "decode_tc_kernel": ("decode_tc.cu", "common.cuh", "sm100_ptx.cuh", "tmap.h")}
+
+
 def code_digest(text: str) -> str:
     """Digest of C++/CUDA source with comments and whitespace removed, so an
     edit to the comments alone does not mark the counters stale."""
@@ -67,9 +72,9 @@ def measured_traffic(kernel: str, cases):
     if not os.path.exists(DRAM_SUMMARY):
         return None
     d = json.load(open(DRAM_SUMMARY))
-    src = "decode_tc.cu" if kernel == "decode_tc_kernel" else "decode.cu"
-    if d.get("sources", {}).get(src) != source_digest(src):
-        return None
+    for src in KERNEL_SOURCES[kernel]:
+        if d.get("sources", {}).get(src) != source_digest(src):
+            return None
     per = [d["launches"].get(f"{kernel} K={c['K']} N={c['N']} M={c['M']}") for c in cases]
     if not per or any(v is None for v in per):
         return None
