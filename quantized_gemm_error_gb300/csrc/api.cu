@@ -47,6 +47,9 @@ int check_layer(const spear_w4_layer* L) {
       return fail(SPEAR_ERR_INVALID_ARG, "compensator buffers must be 16-byte aligned");
     if (vec && (!L->gate_w1 || !L->gate_c1 || !L->gate_w2 || !L->gate_c2))
       return fail(SPEAR_ERR_INVALID_ARG, "vector-gate buffers are NULL");
+    if (vec && (!aligned16(L->gate_w1) || !aligned16(L->gate_c1) || !aligned16(L->gate_w2) ||
+                !aligned16(L->gate_c2)))
+      return fail(SPEAR_ERR_INVALID_ARG, "vector-gate buffers must be 16-byte aligned");
     if (!std::isfinite(L->alpha) || (!vec && std::isnan(L->b_g)))
       return fail(SPEAR_ERR_INVALID_ARG, "alpha must be finite and b_g not NaN");
   }

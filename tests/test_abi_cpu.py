@@ -70,6 +70,16 @@ def test_invalid_layer_rejected_before_any_device_work(lib):
     assert lib.spear_decode_workspace_bytes(ctypes.byref(L), 65, ctypes.byref(n)) == 1   # M > 64
     assert lib.spear_linear_prefill(ctypes.byref(L), None, 8, None, 0, 0, None, 0, None, None) == 1
     assert lib.spear_linear_decode(ctypes.byref(L), 16, 1, 32, 7, None, 0, None) == 1      # out_dtype
+    # the vector gate: hidden width in [1, 32], its four buffers present and aligned
+    L.gate_hidden = 33
+    assert lib.spear_decode_workspace_bytes(ctypes.byref(L), 1, ctypes.byref(n)) == 1
+    assert b"gate_hidden" in lib.spear_last_error()
+    L.gate_hidden = 8
+    assert lib.spear_decode_workspace_bytes(ctypes.byref(L), 1, ctypes.byref(n)) == 1
+    assert b"vector-gate buffers are NULL" in lib.spear_last_error()
+    L.gate_w1, L.gate_c1, L.gate_w2, L.gate_c2 = 96, 112, 128, 148           # gate_c2 misaligned
+    assert lib.spear_decode_workspace_bytes(ctypes.byref(L), 1, ctypes.byref(n)) == 1
+    assert b"aligned" in lib.spear_last_error()
 
 
 def test_layer_select_matches_worked_example_and_oracle(lib):
