@@ -636,7 +636,7 @@ def run_stack(args):
     exceed L2, so every replay streams them from HBM."""
     import torch
     from quantized_gemm_error_gb300 import spear
-    from quantized_gemm_error_gb300.stack import StackStep, build_stack, select_blocks
+    from quantized_gemm_error_gb300.stack import StackStep, build_stack, memory_bytes, select_blocks
     device = torch.device("cuda", 0)
     torch.cuda.set_device(device)
     spear.load()
@@ -670,6 +670,7 @@ def run_stack(args):
                    "compensated_blocks": [int(b) for b in np.flatnonzero(mask)], "rank": wl["r"],
                    "prefill_M": step.Mp, "decode_M": step.Md, "launch": "cuda-graph",
                    "l2": "3.2 GB of int4 weights stream from HBM every pass"},
+        "memory": memory_bytes(ranks),
         "prefill_path": {"TFLOP_s": round(step.prefill_flops() / tp / 1e12, 1),
                          "frac_bf16_burst": round(step.prefill_flops() / tp / 1e12 / peaks["bf16_tflops"], 4)},
         "decode_path": {"ms": round(out["decode"], 4), "tokens_s": round(step.Md / td, 1),

@@ -37,6 +37,20 @@ def rank_cost_bytes(K: int, N: int) -> int:
     return 2 * (K + N)
 
 
+def memory_bytes(ranks) -> dict:
+    """Device bytes of the stack's packed weights (int4 codes and per-channel
+    fp16 scales; symmetric, so no zero points) and of its compensators (A, B
+    and w_g in bf16), from the shapes; ranks[b] is block b's rank (0: none)."""
+    w = c = 0
+    for r in ranks:
+        r = int(r)
+        for _, K, N in BLOCK_LINEARS:
+            w += N * K // 2 + N * 2
+            if r:
+                c += 2 * (r * K + N * r + K)
+    return {"weight_bytes": w, "compensator_bytes": c, "overhead": c / w}
+
+
 def select_blocks(nblocks: int, nmasked: int, rank: int, seed: int = 0):
     """Module selection over blocks with synthetic damage scores: `nmasked`
     seeded blocks carry equal damage and the rest almost none, so the
@@ -162,4 +176,4 @@ class StackStep:
         return b
 
 
-__all__ = ["BLOCK_LINEARS", "rank_cost_bytes", "select_blocks", "build_stack", "StackLayer", "StackStep"]
+__all__ = ["BLOCK_LINEARS", "rank_cost_bytes", "memory_bytes", "select_blocks", "build_stack", "StackLayer", "StackStep"]
