@@ -213,6 +213,21 @@ def spear_workspace_init(ws: torch.Tensor, stream=None):
            "spear_workspace_init")
 
 
+def _check_io(layer: W4Layer, x: torch.Tensor, y: Optional[torch.Tensor], out_dtype: int):
+    """Shapes and dtypes the C ABI cannot see: x bf16 [M][K]; y, when given,
+    [M][N] in the requested output type (a wrong type would be written past
+    its end)."""
+    if x.dtype != torch.bfloat16 or x.dim() != 2 or x.shape[1] != layer.K:
+        raise ValueError(f"x must be a bfloat16 [M][{layer.K}] tensor, got {x.dtype} {tuple(x.shape)}")
+    if out_dtype not in (OUT_BF16, OUT_F32):
+        raise ValueError(f"out_dtype must be OUT_BF16 or OUT_F32, got {out_dtype}")
+    if y is not None:
+        want = torch.float32 if out_dtype == OUT_F32 else torch.bfloat16
+        if y.dtype != want or tuple(y.shape) != (x.shape[0], layer.N):
+            raise ValueError(f"y must be a {want} [{x.shape[0]}][{layer.N}] tensor, got {y.dtype} "
+                             f"{tuple(y.shape)}")
+
+
 def _out(y, M, N, out_dtype, device):
     if y is not None:
         return y
@@ -222,6 +237,7 @@ def _out(y, M, N, out_dtype, device):
 def spear_linear_decode(layer: W4Layer, x: torch.Tensor, *, y=None, out_dtype: int = OUT_BF16,
                         workspace: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
     """y = dequant(Wq) x + alpha g(x) B (A x) for M <= 64 tokens, one kernel launch."""
+    _check_io(layer, x, y, out_dtype)
     M = x.shape[0]
     y = _out(y, M, layer.N, out_dtype, x.device)
     if workspace is None:
@@ -237,6 +253,7 @@ def spear_linear_decode_noalloc(layer: W4Layer, x: torch.Tensor, *, y: torch.Ten
     """Decode for callers that cannot allocate device memory: the library keeps
     the scratch in a fixed 8 MiB array of its own, so the caller passes only
     inputs and the output buffer.  Calls that overlap on the GPU race."""
+    _check_io(layer, x, y, out_dtype)
     L = layer.c_struct()
     _check(load().spear_linear_decode_noalloc(ctypes.byref(L), _ptr(x), x.shape[0], _ptr(y), out_dtype,
                                               _stream(stream)), "spear_linear_decode_noalloc")
@@ -247,6 +264,7 @@ def spear_linear_prefill(layer: W4Layer, x: torch.Tensor, *, y=None, out_dtype: 
                          mode: int = PREFILL_AUTO, workspace: Optional[torch.Tensor] = None,
                          stream=None, stream_aux=None) -> torch.Tensor:
     """Same layer for large M on the tcgen05 tensor-core path."""
+    _check_io(layer, x, y, out_dtype)
     M = x.shape[0]
     y = _out(y, M, layer.N, out_dtype, x.device)
     if workspace is None:
