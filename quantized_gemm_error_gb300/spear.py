@@ -143,7 +143,38 @@ class W4Layer:
     gate_w2: Optional[torch.Tensor] = None
     gate_c2: Optional[torch.Tensor] = None
 
+    def check(self):
+        """Shapes and dtypes of the layer's tensors, which the C ABI (plain
+        pointers) cannot see; the library checks the rest (shape rules, rank,
+        hidden width, alignment)."""
+        N, K, G, r = self.N, self.K, self.group_size, self.rank
+        if G <= 0 or K % G:
+            raise ValueError(f"group_size={G} must divide K={K}")
+
+        def need(t, name, dtype, shape):
+            if t is None:
+                raise ValueError(f"{name} is missing")
+            if t.dtype != dtype or tuple(t.shape) != tuple(shape):
+                raise ValueError(f"{name} must be {dtype} {tuple(shape)}, got {t.dtype} {tuple(t.shape)}")
+
+        need(self.qweight, "qweight", torch.uint8, (N, K // 2))
+        need(self.scales, "scales", torch.float16, (N, K // G))
+        if not self.symmetric:
+            need(self.zeros, "zeros", torch.uint8, (N, (K // G + 1) // 2))
+        if self.comp_enabled and r > 0:
+            need(self.A, "A", torch.bfloat16, (r, K))
+            need(self.B, "B", torch.bfloat16, (N, r))
+            if self.gate_w1 is None:
+                need(self.w_g, "w_g", torch.bfloat16, (K,))
+            else:
+                h = int(self.gate_w1.shape[0]) if self.gate_w1.dim() == 2 else -1
+                need(self.gate_w1, "gate_w1", torch.float32, (h, r))
+                need(self.gate_c1, "gate_c1", torch.float32, (h,))
+                need(self.gate_w2, "gate_w2", torch.float32, (r, h))
+                need(self.gate_c2, "gate_c2", torch.float32, (r,))
+
     def c_struct(self) -> _Layer:
+        self.check()
         h = int(self.gate_w1.shape[0]) if self.gate_w1 is not None else 0
         return _Layer(self.N, self.K, self.group_size, int(self.symmetric), _ptr(self.qweight),
                       _ptr(self.scales), _ptr(self.zeros), int(self.rank), _ptr(self.A), _ptr(self.B),

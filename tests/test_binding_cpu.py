@@ -40,3 +40,29 @@ def test_noalloc_decode_checks_its_output_too():
     x = torch.zeros(2, 256, dtype=torch.bfloat16)
     with pytest.raises(ValueError, match="bfloat16"):
         spear.spear_linear_decode_noalloc(L, x, y=torch.zeros(2, 128, dtype=torch.float32))
+
+
+def test_layer_tensors_are_checked():
+    import dataclasses
+    L = _layer()
+    L.check()
+    bad = [dict(qweight=torch.zeros(128, 64, dtype=torch.uint8)),           # [N][K/2] is [128][128]
+           dict(scales=torch.zeros(128, 2, dtype=torch.float32)),
+           dict(symmetric=False),                                          # zero points missing
+           dict(group_size=96)]
+    for kw in bad:
+        with pytest.raises(ValueError):
+            dataclasses.replace(L, **kw).check()
+    bf = lambda *s: torch.zeros(*s, dtype=torch.bfloat16)
+    C = dataclasses.replace(L, rank=16, A=bf(16, 256), B=bf(128, 16), w_g=bf(256))
+    C.check()
+    with pytest.raises(ValueError, match="B"):
+        dataclasses.replace(C, B=bf(16, 128)).check()                      # transposed
+    with pytest.raises(ValueError, match="w_g"):
+        dataclasses.replace(C, w_g=None).check()
+    f32 = lambda *s: torch.zeros(*s, dtype=torch.float32)
+    V = dataclasses.replace(C, w_g=None, gate_w1=f32(8, 16), gate_c1=f32(8), gate_w2=f32(16, 8), gate_c2=f32(16))
+    V.check()
+    with pytest.raises(ValueError, match="gate_w2"):
+        dataclasses.replace(V, gate_w2=f32(8, 16)).check()
+    dataclasses.replace(C, comp_enabled=False, A=None, B=None, w_g=None).check()   # plain layer: no factors

@@ -73,7 +73,9 @@ def test_prefill_vector_gate_matches_oracle(N, K, G, sym, r, h, M, mode):
 def test_vector_gate_hidden_width_is_checked():
     from quantized_gemm_error_gb300 import spear
     L, _, g, rng = _layers(256, 512, 128, False, 16, 4, seed=7)
-    big = torch.zeros(33, 16, device="cuda")
+    h = 33                                                   # one past the library's limit
+    big = dict(gate_w1=torch.zeros(h, 16, device="cuda"), gate_c1=torch.zeros(h, device="cuda"),
+               gate_w2=torch.zeros(16, h, device="cuda"), gate_c2=torch.zeros(16, device="cuda"))
     with pytest.raises(spear.SpearError):
-        spear.spear_linear_decode(dataclasses.replace(L, gate_w1=big), to_dev_u16(make_tokens(rng, 1, 512),
-                                                                                     torch.bfloat16))
+        spear.spear_linear_decode(dataclasses.replace(L, **big), to_dev_u16(make_tokens(rng, 1, 512),
+                                                                              torch.bfloat16))
