@@ -7,18 +7,19 @@
  * Recovery Enabling Efficient Low-Bit LLM Serving" (gist.science explainer of
  * the paper).  Technical Summary 2.1 A gives the compensated effective weight
  * W + alpha * B * diag(gate) * A with a per-token gate; 2.1 B the
- * entropy-aware module selection; 2.2 A the phase-aware dispatch (decode:
- * compensator fused into the low-bit GEMM epilogue, one kernel; prefill:
- * compensator as a separate kernel overlapped with the GEMM through a CUDA
- * graph); 3.1 the RTN per-channel int4 setting.
+ * entropy-aware module selection on CKA damage scores; 2.2 A the phase-aware
+ * dispatch (decode: compensator fused into the low-bit GEMM epilogue, one
+ * kernel; prefill: compensator as a separate kernel overlapped with the GEMM
+ * through a CUDA graph); 2.2 C the SLO-constrained chunk size; 3.1 the RTN
+ * per-channel int4 setting.
  *
  * Per token x (one row of x [M][K]) every linear call computes
  *
  *     y = dequant(Wq) x  +  alpha * g(x) * B (A x),   g(x) = sigmoid(w_g . x + b_g)
  *
- * (the explainer leaves the gate's exact form open; this library fixes it to
- * the scalar sigmoid above; the explainer's bottleneck-MLP form of the gate is
- * not part of this ABI).
+ * with the scalar gate above by default; a layer with gate_hidden > 0 takes
+ * the explainer's vector gate instead, a bottleneck MLP gamma on A x applied
+ * per rank component (see spear_w4_layer).
  *
  * Conventions
  *  - Every function returns a spear_status code (0 = SPEAR_OK).  On failure
