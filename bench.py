@@ -225,12 +225,21 @@ def time_oracle(cases, nthreads):
     return time.perf_counter() - t0, nbytes
 
 
+def host_threads() -> int:
+    """Threads for the oracle: the CPUs this process may run on (its affinity
+    set), not every CPU of the machine."""
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
 def cpu_baseline(row_fraction: float = 1.0):
     """The oracle timed on this host's cores on a bounded sample of the decode
     step: every (shape, M) call of the step, a fixed seeded subset of output
     rows (row_fraction of N), fp64 accumulation; throughput scaled to the
     metric's unit (algorithmic bytes of the rows covered per second)."""
-    nthreads = os.cpu_count() or 1
+    nthreads = host_threads()
     cases = []
     rng = np.random.default_rng(0)
     for (K, N) in DECODE_SHAPES:
@@ -239,7 +248,8 @@ def cpu_baseline(row_fraction: float = 1.0):
             rows = np.sort(rng.choice(N, size=max(16, int(N * row_fraction)), replace=False)).astype(np.int32)
             cases.append((L, x, rows))
     secs, nbytes = time_oracle(cases, nthreads)
-    return {"value": nbytes / secs / 1e9, "unit": "GB/s", "cores": nthreads, "kind": "oracle",
+    return {"value": nbytes / secs / 1e9, "unit": "GB/s", "cores": nthreads, "host_cpus": os.cpu_count(),
+            "kind": "oracle",
             "sample": f"the 12 decode calls of one step, {row_fraction:.4g} of each layer's output rows "
                       f"(seeded), fp64 accumulation, {secs:.1f} s"}
 
@@ -249,7 +259,7 @@ def cpu_baseline(row_fraction: float = 1.0):
 def run_reference(args, world, rank):
     if rank != 0:
         return
-    nthreads = os.cpu_count() or 1
+    nthreads = host_threads()
     # size each step's sample so the whole run stays within about two minutes
     probe_L, probe_x = oracle_case(4096, 4096, 1, seed=1)
     rows = np.arange(64, dtype=np.int32)
@@ -282,7 +292,8 @@ def run_reference(args, world, rank):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_s / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "config": {"workload": "llama7b_decode_g128_r32"},
-        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": nthreads, "kind": "oracle", "sample": sample},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": nthreads, "host_cpus": os.cpu_count(),
+                         "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }), flush=True)
 
