@@ -3,7 +3,6 @@ each rank's shard, run through the library's decode and prefill calls on one
 GPU in turn, gives its slice of y within the layer's tolerance of the oracle,
 and the slices together cover every output.  (The shards would run on
 separate GPUs; every box here has one.)"""
-import numpy as np
 import pytest
 import torch
 

@@ -5,7 +5,6 @@ and sampled outputs of a plain and a compensated layer match the oracle on
 both paths (prefill M = 1056, decode M = 32).
 
 Source: SPEAR explainer, Technical Summary 2.1 A/B and 2.2 A."""
-import numpy as np
 import pytest
 import torch
 
