@@ -1,8 +1,8 @@
 """GPU parity for the column-parallel split (quantized_gemm_error_gb300/shard.py):
 each rank's shard, run through the library's decode and prefill calls on one
 GPU in turn, gives its slice of y within the layer's tolerance of the oracle,
-and the slices together cover every output.  (The shards would run on
-separate GPUs; every box here has one.)"""
+and the slices together cover every output.  (Deployed, each shard runs on
+a GPU of its own; the test runs them one after another on one GPU.)"""
 import pytest
 import torch
 

@@ -1,8 +1,8 @@
 """The bench's multi-rank host logic on CPU with two gloo ranks (127.0.0.1):
 rendezvous from the torchrun environment variables, the barrier, and the
-max-over-ranks reduction the timed region uses.  With one GPU per box the
-library runs replicas (no collective on the data path); this covers the
-process plumbing around them."""
+max-over-ranks reduction the timed region uses.  Each rank runs the whole
+step on its own GPU (replicas: no collective on the data path); this covers
+the process plumbing around them."""
 import json
 import multiprocessing as mp
 import os
