@@ -164,13 +164,18 @@ spear_status spear_linear_decode(const spear_w4_layer* L, const uint16_t* x, int
  * the library holds it until the process exits) instead of a workspace.
  *   - A shape whose decode scratch exceeds 8 MiB is rejected with
  *     SPEAR_ERR_UNSUPPORTED; spear_last_error() gives the bytes needed.
- *   - The first call on a device sets the scratch up (looks up its device
- *     address and zero-fills it, synchronously); make that first call before
- *     any stream capture.
+ *   - The first call on a device sets the scratch up: it looks up the
+ *     array's device address (host work only, no device work); make that
+ *     first call before any stream capture.
  *   - Every call clears the scratch's synchronisation words on `stream` and
  *     otherwise reuses what the previous call left there.  All calls share
  *     the one array: calls that overlap on the GPU (other streams, other host
  *     threads) race and give wrong results.
+ *   - After spear_get_device_status reports SPEAR_ERR_TIMEOUT, synchronise
+ *     the device before the next call here: a thread block of the launch
+ *     that timed out may still write the shared array.
+ *   - This call never uses launch overlap (spear_set_launch_overlap): the
+ *     clear on `stream` must finish before the kernel starts.
  * Nothing here allocates device memory.
  */
 spear_status spear_linear_decode_noalloc(const spear_w4_layer* L, const uint16_t* x, int M,
@@ -203,8 +208,8 @@ spear_status spear_workspace_init(void* workspace, size_t bytes, void* stream);
 
 /*
  * Launch overlap for chains of decode calls (process-wide, default off).
- * With enable != 0, decode launches (spear_linear_decode and _noalloc) use
- * programmatic dependent launch: a decode kernel may start while the kernel
+ * With enable != 0, spear_linear_decode launches use programmatic dependent
+ * launch (spear_linear_decode_noalloc never does): a decode kernel may start while the kernel
  * before it on the same stream is still finishing, and streams its weights
  * meanwhile; it waits for that kernel to complete (with its memory visible)
  * before it reads x, touches the workspace or writes y.  The caller

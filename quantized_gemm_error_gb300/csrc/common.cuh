@@ -16,6 +16,17 @@ enum : unsigned {
   DEV_ERR_TIMEOUT = 5,
 };
 
+// A pointer into shared memory moved up to the next multiple of `align`
+// bytes (a power of two) by offsetting the original pointer.  (Rounding an
+// integer copy of the pointer instead would hide its address space from the
+// compiler, and every access through the result would become a slower
+// generic load or store.)
+template <typename T>
+__device__ __forceinline__ T* smem_align_up(T* p, uint32_t align) {
+  const uint32_t a = (uint32_t)__cvta_generic_to_shared(p);
+  return reinterpret_cast<T*>(reinterpret_cast<uint8_t*>(p) + ((align - (a & (align - 1))) & (align - 1)));
+}
+
 // Keeps the first error: later errors do not overwrite it.
 __device__ __forceinline__ void record_status(unsigned* word, unsigned code) {
   atomicCAS(word, 0u, code);

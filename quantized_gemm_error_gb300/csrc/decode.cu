@@ -266,10 +266,9 @@ __device__ void streamer_block(const DecodeParams& p, float* smem) {
   __half* sc_s = reinterpret_cast<__half*>(Ts + (COMP ? Mpad * kMaxRank : 0));   // [max_tiles * 16][ng]
   uint8_t* z_s = reinterpret_cast<uint8_t*>(sc_s + p.max_tiles * 16 * p.ng);     // [max_tiles * 16][zrow]
   const int zrow = (p.ng + 1) / 2;
-  __nv_bfloat16* B_s = reinterpret_cast<__nv_bfloat16*>(
-      (reinterpret_cast<uintptr_t>(z_s + p.max_tiles * 16 * zrow) + 15) & ~uintptr_t(15));  // [max_tiles * 16][r]
-  uint4* xs = reinterpret_cast<uint4*>((reinterpret_cast<uintptr_t>(B_s + (COMP ? p.max_tiles * 16 * p.r : 0)) +
-                                        15) & ~uintptr_t(15));            // [M][xrow] (XS)
+  __nv_bfloat16* B_s = reinterpret_cast<__nv_bfloat16*>(smem_align_up(z_s + p.max_tiles * 16 * zrow, 16));  // [max_tiles * 16][r]
+  uint4* xs = reinterpret_cast<uint4*>(
+      smem_align_up(reinterpret_cast<uint8_t*>(B_s + (COMP ? p.max_tiles * 16 * p.r : 0)), 16));   // [M][xrow] (XS)
   float* Ps = reinterpret_cast<float*>(xs + (XS ? p.M * xrow : 0));  // [M][nchunks] 1024 E + 64 O (XS)
   float* Xs = Ps + (XS ? p.M * p.nchunks : 0);                       // [M][nchunks] E + O (XS)
   __shared__ int s_flag;
@@ -772,6 +771,10 @@ bool use_tc(const spear_w4_layer& L, int M) {
 }
 
 int decode_workspace_bytes(const spear_w4_layer& L, int M, size_t* bytes) {
+  if (decode_ks_supports(L, M)) {                     // the cluster K-split kernel needs no workspace
+    *bytes = 0;
+    return SPEAR_OK;
+  }
   if (use_tc(L, M)) return decode_tc_workspace_bytes(L, M, bytes);
   Plan pl;
   if (int rc = get_plan(L, M, &pl)) return rc;
@@ -781,6 +784,7 @@ int decode_workspace_bytes(const spear_w4_layer& L, int M, size_t* bytes) {
 
 int launch_decode(const spear_w4_layer& L, const uint16_t* x, int M, void* y, int out_f32, void* ws,
                   size_t ws_bytes, cudaStream_t st, bool overlap) {
+  if (decode_ks_supports(L, M)) return launch_decode_ks(L, x, M, y, out_f32, st, overlap);
   if (use_tc(L, M)) return launch_decode_tc(L, x, M, y, out_f32, ws, ws_bytes, st, overlap);
   Plan pl;
   if (int rc = get_plan(L, M, &pl)) return rc;
@@ -838,7 +842,9 @@ std::mutex g_noalloc_mu;
 void* g_noalloc_ptr[64] = {};      // device address of the scratch array, per device
 
 // Once per device, with that device current: the array's device address (the
-// symbol itself is only a host-side stand-in) and one zero fill.
+// symbol itself is only a host-side stand-in).  No device work: every call
+// clears the synchronisation words on its own stream, and the kernels write
+// the rest of the scratch before they read it.
 int noalloc_scratch(void** out) {
   int dev = 0;
   if (int rc = cuda_check(cudaGetDevice(&dev), "cudaGetDevice")) return rc;
@@ -848,7 +854,6 @@ int noalloc_scratch(void** out) {
     void* ptr = nullptr;
     if (int rc = cuda_check(cudaGetSymbolAddress((void**)&ptr, g_noalloc_scratch), "decode scratch address"))
       return rc;
-    if (int rc = cuda_check(cudaMemset(ptr, 0, kNoallocScratchBytes), "decode scratch zero fill")) return rc;
     g_noalloc_ptr[dev] = ptr;
   }
   *out = g_noalloc_ptr[dev];
@@ -858,6 +863,8 @@ int noalloc_scratch(void** out) {
 
 int launch_decode_noalloc(const spear_w4_layer& L, const uint16_t* x, int M, void* y, int out_f32,
                           cudaStream_t st) {
+  // the cluster K-split kernel keeps everything it exchanges on chip
+  if (decode_ks_supports(L, M)) return launch_decode_ks(L, x, M, y, out_f32, st, false);
   size_t total = 0, sync_bytes = 0;
   if (use_tc(L, M)) {
     if (int rc = decode_tc_workspace_bytes(L, M, &total)) return rc;

@@ -770,7 +770,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 decode_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_x,
                  const TcParams p) {
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* smem = smem_align_up(smem_raw, 1024);
   pdl_launch_dependents();                                 // every CTA is resident: let the next kernel queue
   const int rank = (int)cluster_ctarank();
   const int cid = (int)blockIdx.x / p.S;

@@ -54,6 +54,13 @@ int launch_decode_noalloc(const spear_w4_layer& L, const uint16_t* x, int M, voi
                           cudaStream_t st);
 int read_and_clear_status_decode(unsigned* out, cudaStream_t st);
 
+// ---- decode_ks.cu (cluster K-split decode, 1..32 tokens, no workspace)
+bool decode_ks_supports(const spear_w4_layer& L, int M);
+int launch_decode_ks(const spear_w4_layer& L, const uint16_t* x, int M, void* y, int out_f32, cudaStream_t st,
+                     bool overlap);
+void decode_ks_set_wait_limit_ns(uint64_t ns);
+int read_and_clear_status_decode_ks(unsigned* out, cudaStream_t st);
+
 // ---- decode_tc.cu (tensor-core decode path)
 int decode_tc_workspace_bytes(const spear_w4_layer& L, int M, size_t* bytes);
 size_t decode_tc_sync_bytes();

@@ -104,7 +104,7 @@ w4_gemm_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
   using C = TileCfg<BM>;
   constexpr int kStages = C::kStages, kXBytes = C::kXBytes, kStageBytes = C::kStageBytes, kMH = C::kMH;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* smem = smem_align_up(smem_raw, 1024);
   __shared__ __align__(8) uint64_t bar_full[kStages], bar_cvt[kStages], bar_empty[kStages], bar_acc;
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;

@@ -12,6 +12,10 @@ shared scratch), and the largest workload shape must fit that scratch.
 This file is collected last so that a run stopping at the first failure has
 already run every other test; it also passes when run alone.
 """
+import os
+import subprocess
+import sys
+
 import numpy as np
 import pytest
 import torch
@@ -81,3 +85,36 @@ def test_noalloc_serves_the_largest_workload_shape():
     torch.cuda.synchronize()
     assert sp.spear_get_device_status() == 0
     assert torch.equal(y, ref)
+
+
+_FIRST_CALL_ON_SIDE_STREAM = r"""
+import sys
+sys.path[:0] = [ROOT, os.path.join(ROOT, "tests")]
+import numpy as np, torch
+from spear_testutil import check_close, gpu_layer, make_layer, make_tokens, to_dev_u16
+from quantized_gemm_error_gb300 import spear as sp
+torch.cuda.set_device(0)
+lay, rng = make_layer(2048, 4096, 32, seed=99)
+L = gpu_layer(lay, 128, False)
+x = to_dev_u16(make_tokens(rng, 12, 4096, outlier_frac=0.01), torch.bfloat16)
+torch.cuda.synchronize()
+side = torch.cuda.Stream()                       # a non-blocking stream
+y = torch.full((12, 2048), float("nan"), dtype=torch.float32, device="cuda")
+with torch.cuda.stream(side):
+    sp.spear_linear_decode_noalloc(L, x, y=y, out_dtype=sp.OUT_F32, stream=side)   # first call of the process
+    ref = sp.spear_linear_decode(L, x, out_dtype=sp.OUT_F32, stream=side)
+side.synchronize()
+assert sp.spear_get_device_status() == 0
+check_close(y, ref.cpu().numpy().astype(np.float64), "first noalloc call on a side stream")
+print("ok")
+"""
+
+
+def test_noalloc_first_call_of_a_process_on_a_side_stream():
+    """The first no-alloc call of a fresh process, issued on a non-blocking
+    stream, gives the workspace path's output: its one-time set-up is ordered
+    before the kernel whatever stream the caller uses."""
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    code = f"import os\nROOT = {root!r}\n" + _FIRST_CALL_ON_SIDE_STREAM
+    res = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, timeout=600)
+    assert res.returncode == 0 and "ok" in res.stdout, res.stdout[-2000:] + res.stderr[-4000:]
