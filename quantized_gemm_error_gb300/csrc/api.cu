@@ -337,11 +337,12 @@ spear_status spear_get_device_status(int* out, void* stream) {
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   unsigned s_pack = 0, s_dec = 0, s_pre = 0;
   if (int rc = read_and_clear_status_pack(&s_pack, st)) return rc;
-  unsigned s_dtc = 0, s_dks = 0;
+  unsigned s_dtc = 0, s_dks = 0, s_dtm = 0;
   if (int rc = read_and_clear_status_decode(&s_dec, st)) return rc;
   if (int rc = read_and_clear_status_decode_tc(&s_dtc, st)) return rc;
   if (int rc = read_and_clear_status_decode_ks(&s_dks, st)) return rc;
-  if (!s_dec) s_dec = s_dks ? s_dks : s_dtc;
+  if (int rc = read_and_clear_status_decode_tm(&s_dtm, st)) return rc;
+  if (!s_dec) s_dec = s_dtm ? s_dtm : s_dks ? s_dks : s_dtc;
   if (int rc = read_and_clear_status_prefill(&s_pre, st)) return rc;
   if (int rc = cuda_check(cudaStreamSynchronize(st), "status sync")) return rc;
   *out = (int)(s_pack ? s_pack : s_dec ? s_dec : s_pre);

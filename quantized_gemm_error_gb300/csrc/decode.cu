@@ -771,7 +771,7 @@ bool use_tc(const spear_w4_layer& L, int M) {
 }
 
 int decode_workspace_bytes(const spear_w4_layer& L, int M, size_t* bytes) {
-  if (decode_ks_supports(L, M)) {                     // the cluster K-split kernel needs no workspace
+  if (decode_tm_supports(L, M) || decode_ks_supports(L, M)) {   // the cluster K-split kernels need no workspace
     *bytes = 0;
     return SPEAR_OK;
   }
@@ -784,6 +784,7 @@ int decode_workspace_bytes(const spear_w4_layer& L, int M, size_t* bytes) {
 
 int launch_decode(const spear_w4_layer& L, const uint16_t* x, int M, void* y, int out_f32, void* ws,
                   size_t ws_bytes, cudaStream_t st, bool overlap) {
+  if (decode_tm_supports(L, M)) return launch_decode_tm(L, x, M, y, out_f32, st, overlap);
   if (decode_ks_supports(L, M)) return launch_decode_ks(L, x, M, y, out_f32, st, overlap);
   if (use_tc(L, M)) return launch_decode_tc(L, x, M, y, out_f32, ws, ws_bytes, st, overlap);
   Plan pl;
@@ -864,6 +865,7 @@ int noalloc_scratch(void** out) {
 int launch_decode_noalloc(const spear_w4_layer& L, const uint16_t* x, int M, void* y, int out_f32,
                           cudaStream_t st) {
   // the cluster K-split kernel keeps everything it exchanges on chip
+  if (decode_tm_supports(L, M)) return launch_decode_tm(L, x, M, y, out_f32, st, false);
   if (decode_ks_supports(L, M)) return launch_decode_ks(L, x, M, y, out_f32, st, false);
   size_t total = 0, sync_bytes = 0;
   if (use_tc(L, M)) {

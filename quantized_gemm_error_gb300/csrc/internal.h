@@ -61,6 +61,13 @@ int launch_decode_ks(const spear_w4_layer& L, const uint16_t* x, int M, void* y,
 void decode_ks_set_wait_limit_ns(uint64_t ns);
 int read_and_clear_status_decode_ks(unsigned* out, cudaStream_t st);
 
+// ---- decode_tm.cu (cluster K-split decode on tcgen05, weights in tensor memory, 1..64 tokens)
+bool decode_tm_supports(const spear_w4_layer& L, int M);
+int launch_decode_tm(const spear_w4_layer& L, const uint16_t* x, int M, void* y, int out_f32, cudaStream_t st,
+                     bool overlap);
+void decode_tm_set_wait_limit_ns(uint64_t ns);
+int read_and_clear_status_decode_tm(unsigned* out, cudaStream_t st);
+
 // ---- decode_tc.cu (tensor-core decode path)
 int decode_tc_workspace_bytes(const spear_w4_layer& L, int M, size_t* bytes);
 size_t decode_tc_sync_bytes();
