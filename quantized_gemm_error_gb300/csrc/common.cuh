@@ -48,6 +48,13 @@ __device__ __forceinline__ void st_release_gpu(unsigned* p, unsigned v) {
   asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
+// Atomic add with acquire-release semantics at GPU scope (returns the old value).
+__device__ __forceinline__ unsigned atom_add_acq_rel_gpu(unsigned* p, unsigned v) {
+  unsigned old;
+  asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+
 // 16-byte load through L1 (read-only path): for small operands reused by
 // many warps (activations, low-rank factors).
 __device__ __forceinline__ uint4 ldg16(const void* p) {

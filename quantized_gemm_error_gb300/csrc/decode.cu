@@ -20,10 +20,13 @@
 //    turned into exact small integers in registers (nibble | bf16 bias, minus
 //    the biased zero point) and multiplied by the tokens with mma.sync; the
 //    group scale is applied to each 128-k partial in fp32.
-//  * Only the epilogue depends on T: each streamer waits (bounded) for the
-//    flag after all of its weight traffic, adds B T with one more small mma,
-//    and stores y.  The last streamer resets the flag, so the workspace's
-//    synchronisation words are zero again between calls.
+//  * Only the epilogue depends on T.  A helper warp of each streamer block
+//    stages the block's factor-B rows, waits (bounded) for the flag, loads T
+//    into shared memory while the other eight warps stream the weights, and
+//    hands both over at one named barrier before the epilogue, which adds B T
+//    with one more small mma and stores y.  The last helper past the flag
+//    resets it, so the workspace's synchronisation words are zero again
+//    between calls.
 //
 // HBM traffic per call: N K / 2 (codes) + N K/G * 2 (scales) + zeros + (r+1) K 2
 // (A, w_g) + N r 2 (B) + M K 2 (x) + M N 2 (y): the roofline of this kernel.
@@ -34,14 +37,19 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "sm100_ptx.cuh"
 
 namespace spear {
 namespace {
 
 __device__ unsigned g_decode_status;
 
-constexpr int kThreads = 256;
+using sm100::named_arrive;
+using sm100::named_sync;
+
+constexpr int kThreads = 256;              // the warps that compute
 constexpr int kWarps = 8;
+constexpr int kBlockThreads = kThreads + 32; // + one helper warp (streamer blocks of compensated layers)
 constexpr int kStages = 6;            // cp.async ring depth per warp (1 KB per stage)
 constexpr int kChunkK = 128;          // k per work item
 constexpr int kMaxRank = 64;
@@ -161,7 +169,7 @@ __device__ void producer_block(const DecodeParams& p, float* smem) {
   for (int t = 0; t < MT; ++t)
 #pragma unroll
     for (int i = 0; i < 4; ++i) red[((warp * MT + t) * 4 + i) * 32 + lane] = acc[t][i];
-  __syncthreads();
+  named_sync(1, kThreads);
   for (int e = threadIdx.x; e < MT * 4 * 32; e += kThreads) {
     const int t = e / 128, i = (e / 32) & 3, ln = e & 31;
     float v = 0.0f;
@@ -170,18 +178,19 @@ __device__ void producer_block(const DecodeParams& p, float* smem) {
     const int row = (ln >> 2) + 8 * (i >> 1);
     const int tok = t * 8 + 2 * (ln & 3) + (i & 1);
     p.ws_prod[((size_t)q * Mpad + tok) * 16 + row] = v;
-    __threadfence();
   }
-  __syncthreads();
+  named_sync(1, kThreads);
 
-  // arrive; the last producer sums the slices, applies the gate, publishes T
+  // arrive; the last producer sums the slices, applies the gate, publishes T.
+  // The ticket is an acquire-release atomic: it publishes this block's
+  // partials (ordered before it by the barrier) and, in the last producer,
+  // makes every other producer's partials visible.
   __shared__ unsigned s_last;
   if (threadIdx.x == 0) {
-    const unsigned old = atomicAdd(&p.ws_sync[0], 1u);
+    const unsigned old = atom_add_acq_rel_gpu(&p.ws_sync[0], 1u);
     s_last = (old == (unsigned)(p.Q - 1));
-    __threadfence();
   }
-  __syncthreads();
+  named_sync(1, kThreads);
   if (!s_last) return;
   auto slice_sum = [&](int m, int i) {                  // fixed order over slices
     const int rti = i / 16, ri = i % 16;
@@ -201,26 +210,28 @@ __device__ void producer_block(const DecodeParams& p, float* smem) {
     float* hs = ts + Mpad * p.r;                        // [Mpad][h | 1] hidden units
     const GateSmem gt(gs, p.r, p.gh);
     for (int e = threadIdx.x; e < Mpad * p.r; e += kThreads) ts[e] = slice_sum(e / p.r, e % p.r);
-    __syncthreads();
+    named_sync(1, kThreads);
     vector_gate_hidden_rows(ts, Mpad, gt, hs, threadIdx.x, kThreads);
-    __syncthreads();
+    named_sync(1, kThreads);
     vector_gate_apply_rows(ts, Mpad, gt, hs, threadIdx.x, kThreads);
-    __syncthreads();
+    named_sync(1, kThreads);
     for (int e = threadIdx.x; e < Mpad * p.r; e += kThreads)
       p.ws_T[e] = (e / p.r < p.M) ? p.alpha * ts[e] : 0.0f;
   } else {
-    float* gate = smem;                                 // [Mpad]
-    for (int m = threadIdx.x; m < Mpad; m += kThreads)
-      gate[m] = 1.0f / (1.0f + expf(-(slice_sum(m, p.r) + p.b_g)));
-    __syncthreads();
+    // t and the gate row in one pass over the slices, then T = alpha g t
+    float* ts = smem;                                   // [Mpad][r + 1] (over the spent cross-warp sums)
+    const int rr = p.r + 1;
+    for (int e = threadIdx.x; e < Mpad * rr; e += kThreads) ts[e] = slice_sum(e / rr, e % rr);
+    named_sync(1, kThreads);
     for (int e = threadIdx.x; e < Mpad * p.r; e += kThreads) {
       const int m = e / p.r, j = e % p.r;
-      const float v = slice_sum(m, j);
-      p.ws_T[e] = (m < p.M) ? p.alpha * gate[m] * v : 0.0f;
+      const float gate = 1.0f / (1.0f + expf(-(ts[m * rr + p.r] + p.b_g)));
+      p.ws_T[e] = (m < p.M) ? p.alpha * gate * ts[m * rr + j] : 0.0f;
     }
   }
-  __threadfence();
-  __syncthreads();
+  // T is published by thread 0's release store, ordered after every
+  // thread's T writes by the barrier
+  named_sync(1, kThreads);
   if (threadIdx.x == 0) {
     p.ws_sync[0] = 0;                                   // ticket ready for the next call
     st_release_gpu(&p.ws_sync[1], 1u);
@@ -271,7 +282,56 @@ __device__ void streamer_block(const DecodeParams& p, float* smem) {
       smem_align_up(reinterpret_cast<uint8_t*>(B_s + (COMP ? p.max_tiles * 16 * p.r : 0)), 16));   // [M][xrow] (XS)
   float* Ps = reinterpret_cast<float*>(xs + (XS ? p.M * xrow : 0));  // [M][nchunks] 1024 E + 64 O (XS)
   float* Xs = Ps + (XS ? p.M * p.nchunks : 0);                       // [M][nchunks] E + O (XS)
-  __shared__ int s_flag;
+
+  if (warp == kWarps) {
+    // ------------------------------------------------ helper warp
+    // The factor-B rows (weights: before waiting for the kernel ahead), then
+    // the flag (bounded), a ticket, and T as bf16 hi + lo (T = hi + lo to
+    // ~2^-16 relative), all while the compute warps stream the weights.
+    if (!COMP) return;
+    const size_t row0 = (size_t)t0 * 16, nb = (size_t)ntl * 16 * p.r * 2 / 16;
+    for (size_t e = lane; e < nb; e += 32)
+      cp_async16(reinterpret_cast<uint4*>(B_s) + e, reinterpret_cast<const uint4*>(p.B + row0 * p.r) + e);
+    cp_async_commit();
+    pdl_wait();                                             // the workspace follows the kernel ahead
+    unsigned ok = 0, ticket = 0;
+    if (lane == 0) {
+      const uint64_t tw = globaltimer_ns();
+      for (unsigned i = 0;; ++i) {
+        if (ld_acquire_gpu(&p.ws_sync[1])) { ok = 1; break; }
+        if ((i & 63) == 63 && globaltimer_ns() - tw > kWaitLimitNs) break;
+        __nanosleep(32);
+      }
+      if (!ok) record_status(&g_decode_status, DEV_ERR_TIMEOUT);
+      ticket = atomicAdd(&p.ws_sync[2], 1u);
+    }
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    // all of this lane's pairs of T in flight at once (one L2 round trip)
+    constexpr int kTPairs = MT * 8 * kMaxRank / 2 / 32;
+    const int npairs = Mpad * p.r / 2;
+    float2 tv[kTPairs];
+#pragma unroll
+    for (int i = 0; i < kTPairs; ++i) {
+      const int e = lane + 32 * i;
+      tv[i] = (ok && e < npairs) ? __ldcg(reinterpret_cast<const float2*>(p.ws_T) + e) : make_float2(0.0f, 0.0f);
+    }
+#pragma unroll
+    for (int i = 0; i < kTPairs; ++i) {
+      const int e = lane + 32 * i;                          // pair e: T[m][2 jj'], T[m][2 jj' + 1]
+      if (e < npairs) {
+        const __nv_bfloat16 h0 = __float2bfloat16_rn(tv[i].x), h1 = __float2bfloat16_rn(tv[i].y);
+        Ts[e] = pack_bf16x2(__bfloat162float(h0), __bfloat162float(h1));
+        Ts[npairs + e] = pack_bf16x2(tv[i].x - __bfloat162float(h0), tv[i].y - __bfloat162float(h1));
+      }
+    }
+    cp_async_wait<0>();                                     // the B rows
+    named_arrive(2, kBlockThreads);                         // B rows and T are in place
+    if (lane == 0 && ticket == (unsigned)(p.P - 1)) {       // every streamer is past its wait
+      p.ws_sync[2] = 0;
+      atomicExch(&p.ws_sync[1], 0u);
+    }
+    return;
+  }
 
   // work items of this warp: (tile, chunk), chunk = warp + 8 j; the issue
   // cursor walks them with pointer increments only
@@ -294,9 +354,9 @@ __device__ void streamer_block(const DecodeParams& p, float* smem) {
   };
 
   // 1. tokens (XS) into registers (they come from L2); then, as one cp.async
-  // group ahead of the weight stream, the block's scales, zero points and
-  // factor-B rows, so the only wait before the main loop is for bytes that
-  // travel together with the first weights
+  // group ahead of the weight stream, the block's scales and zero points, so
+  // the only wait before the main loop is for bytes that travel together with
+  // the first weights
   const int xunits = XS ? p.M * k8 : 0;
   constexpr int kXBatch = XS ? 4 : 1;
   uint4 xr[kXBatch];
@@ -308,7 +368,6 @@ __device__ void streamer_block(const DecodeParams& p, float* smem) {
     const size_t row0 = (size_t)t0 * 16, rows = (size_t)ntl * 16;
     stage(sc_s, p.scales + row0 * p.ng, rows * p.ng * 2);
     if (!p.sym) stage(z_s, p.zeros + row0 * zrow, rows * zrow);
-    if (COMP) stage(B_s, p.B + row0 * p.r, rows * p.r * 2);
     cp_async_commit();
   }
 #pragma unroll
@@ -377,7 +436,7 @@ __device__ void streamer_block(const DecodeParams& p, float* smem) {
     if (bad) record_status(&g_decode_status, DEV_ERR_INVALID);
   }
   cp_async_wait<kStages - 1>();                            // the staged scales, zeros and B
-  __syncthreads();
+  named_sync(1, kThreads);
 
   // 3. main loop
   int slot = 0;
@@ -497,48 +556,19 @@ __device__ void streamer_block(const DecodeParams& p, float* smem) {
     for (int t = 0; t < MT; ++t)
 #pragma unroll
       for (int i = 0; i < 4; ++i) red[((warp * MT + t) * 4 + i) * 32 + lane] = acc[t][i];
-    __syncthreads();
+    named_sync(1, kThreads);
     for (int e = threadIdx.x; e < MT * 128; e += kThreads) {
       float v = 0.0f;
 #pragma unroll
       for (int w = 0; w < kWarps; ++w) v += red[w * MT * 128 + e];
       ybuf[tl * MT * 128 + e] = v;
     }
-    __syncthreads();
+    named_sync(1, kThreads);
   }
   cp_async_wait<0>();
 
-  // 4. the compensator's down-projection (published by the producers)
-  unsigned ticket = 0;            // thread 0: this block's place among the streamers past the wait
-  if (COMP) {
-    if (threadIdx.x == 0) {
-      const uint64_t tw = globaltimer_ns();
-      unsigned ok = 0;
-      for (unsigned i = 0;; ++i) {
-        if (ld_acquire_gpu(&p.ws_sync[1])) { ok = 1; break; }
-        if ((i & 63) == 63 && globaltimer_ns() - tw > kWaitLimitNs) break;
-        __nanosleep(32);
-      }
-      if (!ok) record_status(&g_decode_status, DEV_ERR_TIMEOUT);
-      s_flag = ok;
-      // taken here, read at the end: the round trip overlaps the epilogue
-      ticket = atomicAdd(&p.ws_sync[2], 1u);
-    }
-    __syncthreads();
-    // T as bf16 hi + lo (T = hi + lo to ~2^-16 relative)
-    for (int e = threadIdx.x; e < Mpad * p.r / 2; e += kThreads) {
-      const int m = e / (p.r / 2), jj = (e % (p.r / 2)) * 2;
-      float ta = 0.0f, tb = 0.0f;
-      if (s_flag) {
-        ta = __ldcg(p.ws_T + m * p.r + jj);
-        tb = __ldcg(p.ws_T + m * p.r + jj + 1);
-      }
-      const __nv_bfloat16 h0 = __float2bfloat16_rn(ta), h1 = __float2bfloat16_rn(tb);
-      Ts[m * (p.r / 2) + jj / 2] = pack_bf16x2(__bfloat162float(h0), __bfloat162float(h1));
-      Ts[Mpad * (p.r / 2) + m * (p.r / 2) + jj / 2] = pack_bf16x2(ta - __bfloat162float(h0), tb - __bfloat162float(h1));
-    }
-    __syncthreads();
-  }
+  // 4. the compensator's down-projection and the B rows (from the helper warp)
+  if (COMP) named_sync(2, kBlockThreads);
 
   // 5. epilogue: y = acc (* per-channel scale) + B T, one (tile, token tile) per warp
   for (int item = warp; item < ntl * MT; item += kWarps) {
@@ -576,20 +606,16 @@ __device__ void streamer_block(const DecodeParams& p, float* smem) {
     }
   }
 
-  if (COMP && threadIdx.x == 0 && ticket == (unsigned)(p.P - 1)) {   // every streamer is past its wait
-    p.ws_sync[2] = 0;
-    atomicExch(&p.ws_sync[1], 0u);
-  }
 }
 
 template <int MT, bool COMP, bool PERCH, bool XS>
-__global__ void __launch_bounds__(kThreads, (MT <= 2 ? 2 : 1)) decode_kernel(const DecodeParams p) {
+__global__ void __launch_bounds__(kBlockThreads, (MT <= 2 ? 2 : 1)) decode_kernel(const DecodeParams p) {
   extern __shared__ __align__(16) float smem[];
   pdl_launch_dependents();                                 // every block is resident: let the next kernel queue
   if ((int)blockIdx.x < p.Q) {
     // The plain layer keeps the same block split as the compensated one (its
     // producer blocks idle), so forcing the gate to zero reproduces it bit for bit.
-    if (COMP) producer_block<MT>(p, smem);
+    if (COMP && threadIdx.x < kThreads) producer_block<MT>(p, smem);
   } else {
     streamer_block<MT, COMP, PERCH, XS>(p, smem);
   }
@@ -680,7 +706,7 @@ int build_plan(const spear_w4_layer& L, int MT, int M, bool comp, bool try_xs, c
       return fail(SPEAR_ERR_UNSUPPORTED, "decode: shape needs %zu B of shared memory", pl->smem);
     if (int rc = ensure_smem_limit(reinterpret_cast<const void*>(pl->fn), pl->smem)) return rc;
     int per_sm = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, pl->fn, kThreads, pl->smem) != cudaSuccess ||
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, pl->fn, kBlockThreads, pl->smem) != cudaSuccess ||
         per_sm < 1)
       return fail(SPEAR_ERR_CUDA, "decode: occupancy query failed");
     const int cap = std::min(per_sm, 2) * di.num_sms;
@@ -816,7 +842,7 @@ int launch_decode(const spear_w4_layer& L, const uint16_t* x, int M, void* y, in
   if (int rc = ensure_smem_limit(reinterpret_cast<const void*>(pl.fn), pl.smem)) return rc;
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(pl.Q + pl.P);
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(kBlockThreads);
   cfg.dynamicSmemBytes = pl.smem;
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
