@@ -526,6 +526,19 @@ def run_ours(args, world, rank, local):
             prefill = run_prefill(torch, spear, device, stream, peaks)
         except Exception as e:  # the decode line still prints; the failure is reported in it
             prefill = {"error": f"{type(e).__name__}: {e}"}
+    # the other two workloads, on rank 0 (a few seconds of GPU time each)
+    stack = llama70b = None
+    del copies, graphs, e2e_graphs
+    torch.cuda.empty_cache()
+    if rank == 0 and not args.no_extra:
+        try:
+            stack = stack_section(torch, spear, device, peaks, steps=10, warmup=3)
+        except Exception as e:
+            stack = {"error": f"{type(e).__name__}: {e}"}
+        try:
+            llama70b = llama70b_section(torch, spear, device, stream, peaks, l2_bytes)
+        except Exception as e:
+            llama70b = {"error": f"{type(e).__name__}: {e}"}
 
     # roofline of the kernel with the largest share of the step: algorithmic
     # bytes per launch over its mean launch time (CUDA events, graph replays)
@@ -570,6 +583,8 @@ def run_ours(args, world, rank, local):
             "vector_gate_overhead_step": round(sum(c["vector_gate_us"] for c in cases) / tot_off - 1, 4),
             "decode_cases": cases,
             "prefill": prefill,
+            "stack": stack,
+            "llama70b": llama70b,
         }
         print(json.dumps(result), flush=True)
     return result
@@ -661,58 +676,192 @@ def profile_prefill_case(spec: str):
     print(f"prefill K={K} N={N} M={M} mode={mode} x{iters}: status {spear.spear_get_device_status()}")
 
 
-def run_stack(args):
+def stack_section(torch, spear, device, peaks, steps: int, warmup: int) -> dict:
     """The Llama-7B 32-block decoder stack (per-channel symmetric int4; rank-64
     compensators on the 4 blocks the selection rule picks): one mixed step of
     chunked prefill (a 1024-token chunk and 32 decode tokens, 1056 tokens
     through all 224 linears on the prefill path) and the 32 decode tokens
     alone on the decode path, each one CUDA graph.  Weights (3.2 GB of int4)
     exceed L2, so every replay streams them from HBM."""
-    import torch
-    from quantized_gemm_error_gb300 import spear
+    from quantized_gemm_error_gb300.inputs import workload
     from quantized_gemm_error_gb300.stack import StackStep, build_stack, memory_bytes, select_blocks
-    device = torch.device("cuda", 0)
-    torch.cuda.set_device(device)
-    spear.load()
-    spear.spear_set_launch_overlap(True)
-    wl = __import__("quantized_gemm_error_gb300.inputs", fromlist=["workload"]).workload("llama7b_stack_sym_r64")
+    wl = workload("llama7b_stack_sym_r64")
     mask, ranks = select_blocks(wl["blocks"], wl["masked_blocks"], wl["r"], seed=0)
     layers = build_stack(ranks, device, seed=0, recipe="device")
     step = StackStep(layers, wl["prefill_M"][0], wl["decode_M"][0], device, seed=0)
     step.capture()
-    peaks, _ = load_peaks()
     out = {}
     for name in ("prefill", "decode"):
-        for _ in range(args.warmup):
+        for _ in range(warmup):
             step.replay(name)
         torch.cuda.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(step.stream)
-        for _ in range(args.steps):
+        for _ in range(steps):
             step.replay(name)
         e1.record(step.stream)
         torch.cuda.synchronize()
-        out[name] = e0.elapsed_time(e1) / args.steps            # ms per pass
+        out[name] = e0.elapsed_time(e1) / steps            # ms per pass
     status = spear.spear_get_device_status()
     tp, td = out["prefill"] / 1e3, out["decode"] / 1e3
-    line = {
-        "metric": "decoder-stack mixed step tokens/s (1056 tokens x 224 linears, prefill path)",
-        "value": round(step.Mp / tp, 1), "unit": "tokens/s", "n_gpus": 1, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": round(out["prefill"], 4), "higher_is_better": True,
-        "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": "llama7b_stack_sym_r64", "blocks": wl["blocks"], "linears": len(layers),
-                   "compensated_blocks": [int(b) for b in np.flatnonzero(mask)], "rank": wl["r"],
-                   "prefill_M": step.Mp, "decode_M": step.Md, "launch": "cuda-graph",
-                   "l2": "3.2 GB of int4 weights stream from HBM every pass"},
+    res = {
+        "workload": "llama7b_stack_sym_r64", "blocks": wl["blocks"], "linears": len(layers),
+        "compensated_blocks": [int(b) for b in np.flatnonzero(mask)], "rank": wl["r"],
+        "prefill_M": step.Mp, "decode_M": step.Md, "launch": "cuda-graph", "steps": steps, "warmup": warmup,
+        "l2": "3.2 GB of int4 weights stream from HBM every pass",
         "memory": memory_bytes(ranks),
-        "prefill_path": {"TFLOP_s": round(step.prefill_flops() / tp / 1e12, 1),
-                         "frac_bf16_burst": round(step.prefill_flops() / tp / 1e12 / peaks["bf16_tflops"], 4)},
-        "decode_path": {"ms": round(out["decode"], 4), "tokens_s": round(step.Md / td, 1),
+        "mixed_step": {"ms": round(out["prefill"], 4), "tokens_s": round(step.Mp / tp, 1),
+                       "TFLOP_s": round(step.prefill_flops() / tp / 1e12, 1),
+                       "frac_bf16_burst": round(step.prefill_flops() / tp / 1e12 / peaks["bf16_tflops"], 4)},
+        "decode_step": {"ms": round(out["decode"], 4), "tokens_s": round(step.Md / td, 1),
                         "GB_s": round(step.decode_bytes() / td / 1e9, 1),
                         "frac_hbm": round(step.decode_bytes() / td / 1e9 / peaks["hbm_gbs"], 4)},
-        "gpu_launches": None, "status": status,
+        "status": status,
+    }
+    del step, layers
+    torch.cuda.empty_cache()
+    return res
+
+
+def run_stack(args):
+    """The decoder stack alone, as its own JSON line (--stack)."""
+    import torch
+    from quantized_gemm_error_gb300 import spear
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(device)
+    spear.load()
+    spear.spear_set_launch_overlap(True)
+    peaks, _ = load_peaks()
+    st = stack_section(torch, spear, device, peaks, args.steps, args.warmup)
+    tp = st["mixed_step"]["ms"] / 1e3
+    line = {
+        "metric": "decoder-stack mixed step tokens/s (1056 tokens x 224 linears, prefill path)",
+        "value": st["mixed_step"]["tokens_s"], "unit": "tokens/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": st["mixed_step"]["ms"], "higher_is_better": True,
+        "dtype": "bf16", "data": "synthetic",
+        "config": {k: st[k] for k in ("workload", "blocks", "linears", "compensated_blocks", "rank", "prefill_M",
+                                      "decode_M", "launch", "l2")},
+        "memory": st["memory"],
+        "prefill_path": {"TFLOP_s": st["mixed_step"]["TFLOP_s"], "frac_bf16_burst": st["mixed_step"]["frac_bf16_burst"]},
+        "decode_path": st["decode_step"],
+        "gpu_launches": None, "status": st["status"], "seconds_per_step": tp,
     }
     print(json.dumps(line), flush=True)
+
+
+def llama70b_section(torch, spear, device, stream, peaks, l2_bytes) -> dict:
+    """Llama-70B linears (8192x8192, 8192x28672, 28672x8192; int4 group 128
+    asymmetric, rank 64, 1 % outlier channels x20): decode GB/s at M in
+    {1, 8, 32}, every call on its own weight copy (each shape's copies >= 4x
+    L2), and prefill TFLOP/s at M in {256, 512, 1024, 2048, 4096} (fused and
+    concurrent-stream modes, the faster one counted), each against the plain
+    W4 layer."""
+    from quantized_gemm_error_gb300.inputs import make_layer, make_tokens, workload
+    wl = workload("llama70b_g128_r64")
+    r, Gw, sym, outl = wl["r"], wl["G"], wl["sym"], wl["outlier_frac"]
+    assert Gw == G and sym == SYM             # decode_bytes / prefill_flops use the module's format
+
+    def dev16(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(device)
+
+    aux = torch.cuda.Stream(device)
+    dec, pre = [], []
+    for (K, N) in wl["shapes"]:
+        lay, rng = make_layer(N, K, r, seed=K + N + 7)
+        q, s_, z = spear.spear_pack_w4(torch.from_numpy(lay.W).to(device), Gw, sym)
+        A, B, wg = dev16(lay.A), dev16(lay.B), dev16(lay.w_g)
+        del lay
+        L0 = spear.W4Layer(N, K, Gw, sym, q, s_, z, r, A, B, wg, 0.0, 1.0, True)
+        wbytes = decode_bytes(K, N, 0, r)
+        ncopy = int(np.ceil(4 * l2_bytes / wbytes))
+        copies = [L0] + [spear.W4Layer(N, K, Gw, sym, q.clone(), s_.clone(), z.clone(), r, A.clone(), B.clone(),
+                                       wg.clone(), 0.0, 1.0, True) for _ in range(ncopy - 1)]
+        for M in wl["decode_M"]:
+            x = dev16(make_tokens(rng, M, K, outlier_frac=outl))
+            y = torch.empty(M, N, dtype=torch.bfloat16, device=device)
+            ws = spear.new_workspace(spear.spear_decode_workspace_bytes(L0, M), device)
+            torch.cuda.synchronize()
+            res = {}
+            for comp in (True, False):
+                def calls():
+                    for L in copies:
+                        spear.spear_linear_decode(L if comp else L.with_comp(False), x, y=y, workspace=ws,
+                                                  stream=stream)
+                with torch.cuda.stream(stream):
+                    calls()
+                torch.cuda.synchronize()
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=stream):
+                    calls()
+                g.replay()
+                torch.cuda.synchronize()
+                reps = 5
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                with torch.cuda.stream(stream):
+                    for _ in range(reps):
+                        g.replay()
+                b.record(stream)
+                torch.cuda.synchronize()
+                res[comp] = a.elapsed_time(b) / (reps * ncopy) * 1e3
+                del g
+            assert spear.spear_get_device_status(stream) == 0
+            gbs = decode_bytes(K, N, M, r) / res[True] / 1e3
+            dec.append({"K": K, "N": N, "M": M, "kernel": decode_kernel_name(M), "us": round(res[True], 3),
+                        "GB_s": round(gbs, 1), "frac_hbm_measured": round(gbs / peaks["hbm_gbs"], 4),
+                        "plain_us": round(res[False], 3), "comp_overhead": round(res[True] / res[False] - 1, 4),
+                        "weight_copies": ncopy})
+            del x, y, ws
+        del copies
+        torch.cuda.empty_cache()
+        for M in wl["prefill_M"]:
+            x = dev16(make_tokens(rng, M, K, outlier_frac=outl))
+            y = torch.empty(M, N, dtype=torch.bfloat16, device=device)
+            ws = spear.new_workspace(max(spear.spear_prefill_workspace_bytes(L0, M, m)
+                                         for m in (spear.PREFILL_FUSED, spear.PREFILL_STREAM)), device, zero=False)
+            torch.cuda.synchronize()
+            res = {}
+            for name, Lc, mode in (("fused", L0, spear.PREFILL_FUSED), ("stream", L0, spear.PREFILL_STREAM),
+                                   ("plain", L0.with_comp(False), spear.PREFILL_FUSED)):
+                def call():
+                    spear.spear_linear_prefill(Lc, x, y=y, mode=mode, workspace=ws, stream=stream, stream_aux=aux)
+                with torch.cuda.stream(stream):
+                    for _ in range(2):
+                        call()
+                torch.cuda.synchronize()
+                reps = max(2, int(1e13 / prefill_flops(K, N, M, r)))
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                with torch.cuda.stream(stream):
+                    a.record(stream)
+                    for _ in range(reps):
+                        call()
+                    b.record(stream)
+                torch.cuda.synchronize()
+                res[name] = a.elapsed_time(b) / reps * 1e3
+            assert spear.spear_get_device_status(stream) == 0
+            best = min(res["fused"], res["stream"])
+            tfl = prefill_flops(K, N, M, r) / best / 1e6
+            pre.append({"K": K, "N": N, "M": M, "fused_us": round(res["fused"], 1),
+                        "stream_us": round(res["stream"], 1), "plain_us": round(res["plain"], 1),
+                        "TFLOP_s": round(tfl, 1), "frac_bf16_burst": round(tfl / peaks["bf16_tflops"], 4),
+                        "comp_overhead": round(best / res["plain"] - 1, 4),
+                        "best_mode": "fused" if res["fused"] <= res["stream"] else "stream"})
+            del x, y, ws
+        del L0, q, s_, z, A, B, wg
+        torch.cuda.empty_cache()
+    dec_bytes = sum(decode_bytes(c["K"], c["N"], c["M"], r) for c in dec)
+    dec_us = sum(c["us"] for c in dec)
+    pre_fl = sum(prefill_flops(c["K"], c["N"], c["M"], r) for c in pre)
+    pre_us = sum(min(c["fused_us"], c["stream_us"]) for c in pre)
+    return {"workload": "llama70b_g128_r64", "shapes_KxN": [list(t) for t in wl["shapes"]], "rank": r,
+            "group_size": Gw, "symmetric": sym,
+            "decode": {"GB_s": round(dec_bytes / dec_us / 1e3, 1),
+                       "frac_hbm_measured": round(dec_bytes / dec_us / 1e3 / peaks["hbm_gbs"], 4),
+                       "comp_overhead": round(dec_us / sum(c["plain_us"] for c in dec) - 1, 4),
+                       "l2": "each call on its own weight copy; each shape's copies >= 4x L2", "cases": dec},
+            "prefill": {"TFLOP_s": round(pre_fl / pre_us / 1e6, 1),
+                        "frac_bf16_burst": round(pre_fl / pre_us / 1e6 / peaks["bf16_tflops"], 4),
+                        "cases": pre}}
 
 
 def run_schedule(args):
@@ -777,6 +926,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="skip the decoder-stack and Llama-70B sections of the default line")
     ap.add_argument("--profile-prefill", metavar="K,N,M,MODE,ITERS", default=None,
                     help="run one prefill case ITERS times for a profiler and exit")
     ap.add_argument("--stack", action="store_true",

@@ -3,7 +3,8 @@ output rows the oracle computes one by one:
 
 * Llama-70B linears (8192x8192, 8192x28672, 28672x8192; int4 group 128
   asymmetric, rank 64, 1 % outlier channels x20): decode M in {1, 8, 32},
-  prefill M in {256, 4096};
+  prefill M in {256, 512, 1024, 2048, 4096};
+* the Llama-7B prefill linears at their largest chunk, M = 8192;
 * the Llama-7B decoder-block stack's layer shapes (per-output-channel symmetric
   int4; rank 64 on the masked blocks, plain W4 on the rest) at one mixed step:
   prefill M = 1056 (a 1024-token chunk and 32 decode tokens), decode M = 32.
@@ -22,6 +23,7 @@ pytestmark = pytest.mark.gpu
 
 W70 = workload("llama70b_g128_r64")
 STACK = workload("llama7b_stack_sym_r64")
+P7 = workload("llama7b_prefill_g128_r32")
 
 _held = {}
 
@@ -56,7 +58,7 @@ def test_llama70b_decode_sampled(K, N, M):
     _check(L, OL, M, K, N, "decode", 128, M, W70["outlier_frac"])
 
 
-@pytest.mark.parametrize("K,N,M", [(K, N, M) for (K, N) in W70["shapes"] for M in (256, 4096)])
+@pytest.mark.parametrize("K,N,M", [(K, N, M) for (K, N) in W70["shapes"] for M in W70["prefill_M"]])
 def test_llama70b_prefill_sampled(K, N, M):
     L, OL = _layer(N, K, W70["r"], W70["G"], W70["sym"], seed=N + K)
     _check(L, OL, M, K, N, "prefill", 48 if M > 1024 else 96, M, W70["outlier_frac"])
@@ -70,3 +72,11 @@ def test_llama7b_stack_layers_sampled(K, N, masked):
     L, OL = _layer(N, K, r, K, True, seed=3 * N + K + r)
     _check(L, OL, STACK["prefill_M"][0], K, N, "prefill", 96, 11, STACK["outlier_frac"])
     _check(L, OL, STACK["decode_M"][0], K, N, "decode", 128, 12, STACK["outlier_frac"])
+
+
+@pytest.mark.parametrize("K,N", P7["shapes"])
+def test_llama7b_prefill_largest_chunk_sampled(K, N):
+    """M = 8192, the prefill workload's largest chunk."""
+    M = max(P7["prefill_M"])
+    L, OL = _layer(N, K, P7["r"], P7["G"], P7["sym"], seed=5 * N + K)
+    _check(L, OL, M, K, N, "prefill", 48, 8192 + K, P7["outlier_frac"])
