@@ -54,7 +54,8 @@ enum {
   SPEAR_ERR_UNSUPPORTED = 2,   /* valid call outside what the kernels cover */
   SPEAR_ERR_WORKSPACE = 3,     /* workspace missing or too small            */
   SPEAR_ERR_CUDA = 4,          /* a CUDA runtime call failed                */
-  SPEAR_ERR_TIMEOUT = 5        /* a bounded device-side wait gave up        */
+  SPEAR_ERR_TIMEOUT = 5,       /* a bounded device-side wait gave up        */
+  SPEAR_ERR_BOUNDS = 6         /* an index check of the debug build failed  */
 };
 
 /* Prefill modes (Technical Summary 2.2 A, "semi-fused" prefill). */
@@ -219,6 +220,19 @@ spear_status spear_workspace_init(void* workspace, size_t bytes, void* stream);
  * capture, where it becomes a programmatic graph edge).
  */
 spear_status spear_set_launch_overlap(int enable);
+
+/*
+ * Limit of the device-side waits on other thread blocks (process-wide).  A
+ * decode launch's blocks wait for the down-projection that other blocks of
+ * the same launch publish (and the cluster kernels for their peers); each
+ * such wait gives up after `ns` nanoseconds, records SPEAR_ERR_TIMEOUT in the
+ * device status word and lets its kernel finish with the compensator term
+ * left out.  ns = 0 restores the defaults (200 ms; 2 s in the cluster
+ * kernels).  For tests and diagnostics: a limit shorter than a legitimate
+ * wait makes correct calls fail.  Host only; takes effect for launches issued
+ * afterwards.
+ */
+spear_status spear_set_wait_limit_ns(uint64_t ns);
 
 /*
  * Module selection (Technical Summary 2.1 B), host only.  damage[L] >= 0 is a

@@ -19,6 +19,9 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OBJ_DIR = os.path.join(PKG, "lib", "obj")
 LIB_PATH = os.path.join(PKG, "lib", "libspear.so")
+# the bounds-checked build (-DSPEAR_DEBUG_CHECKS): built on request only
+DEBUG_OBJ_DIR = os.path.join(PKG, "lib", "obj_debug")
+DEBUG_LIB_PATH = os.path.join(PKG, "lib", "libspear_debug.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
@@ -39,16 +42,21 @@ def _stale(target: str, deps: list[str]) -> bool:
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build_library(force: bool = False, verbose: bool = False, extra_flags: list[str] | None = None) -> str:
-    os.makedirs(OBJ_DIR, exist_ok=True)
+def build_library(force: bool = False, verbose: bool = False, extra_flags: list[str] | None = None,
+                  debug: bool = False) -> str:
+    """Builds lib/libspear.so, or with debug=True lib/libspear_debug.so: the
+    same sources with the kernels' index checks compiled in (a failed check
+    reports SPEAR_ERR_BOUNDS through spear_get_device_status)."""
+    obj_dir, lib_path = (DEBUG_OBJ_DIR, DEBUG_LIB_PATH) if debug else (OBJ_DIR, LIB_PATH)
+    os.makedirs(obj_dir, exist_ok=True)
     nvcc = _nvcc()
     sources = sorted(glob.glob(os.path.join(CSRC, "*.cu")))
     headers = sorted(glob.glob(os.path.join(CSRC, "*.cuh")) + glob.glob(os.path.join(CSRC, "*.h"))
                      + glob.glob(os.path.join(INCLUDE, "*.h")))
-    flags = NVCC_FLAGS + ARCH + (extra_flags or [])
+    flags = NVCC_FLAGS + ARCH + (["-DSPEAR_DEBUG_CHECKS"] if debug else []) + (extra_flags or [])
 
     def compile_one(src: str) -> str:
-        obj = os.path.join(OBJ_DIR, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(obj_dir, os.path.basename(src)[:-3] + ".o")
         if force or _stale(obj, [src] + headers):
             cmd = [nvcc, *flags, "-c", src, "-o", obj]
             if verbose:
@@ -62,15 +70,15 @@ def build_library(force: bool = False, verbose: bool = False, extra_flags: list[
 
     with cf.ThreadPoolExecutor(max_workers=min(8, len(sources))) as ex:
         objs = list(ex.map(compile_one, sources))
-    if force or _stale(LIB_PATH, objs):
-        tmp = LIB_PATH + f".tmp{os.getpid()}"
+    if force or _stale(lib_path, objs):
+        tmp = lib_path + f".tmp{os.getpid()}"
         cmd = [nvcc, *ARCH, "-shared", "-cudart", "shared", "-o", tmp, *objs]
         res = subprocess.run(cmd, capture_output=True, text=True)
         if res.returncode != 0:
             raise RuntimeError(f"link failed:\n{res.stdout}\n{res.stderr}")
-        os.replace(tmp, LIB_PATH)
-    return LIB_PATH
+        os.replace(tmp, lib_path)
+    return lib_path
 
 
 if __name__ == "__main__":
-    print(build_library(force="--force" in sys.argv, verbose="-v" in sys.argv))
+    print(build_library(force="--force" in sys.argv, verbose="-v" in sys.argv, debug="--debug" in sys.argv))

@@ -74,10 +74,15 @@ int cuda_check(cudaError_t e, const char* what) {
 
 namespace {
 std::atomic<bool> g_launch_overlap{false};
+std::atomic<uint64_t> g_wait_limit_ns{0};
 }  // namespace
 
 void set_launch_overlap(bool on) { g_launch_overlap.store(on); }
 bool launch_overlap() { return g_launch_overlap.load(); }
+uint64_t wait_limit_ns(uint64_t default_ns) {
+  const uint64_t v = g_wait_limit_ns.load();
+  return v ? v : default_ns;
+}
 
 bool log_plans() {
   static const bool on = [] {
@@ -327,6 +332,11 @@ spear_status spear_layer_select_mask(const float* damage, const float* cost, int
   return SPEAR_OK;
 }
 
+spear_status spear_set_wait_limit_ns(uint64_t ns) {
+  spear::g_wait_limit_ns.store(ns);
+  return SPEAR_OK;
+}
+
 spear_status spear_set_launch_overlap(int enable) {
   spear::set_launch_overlap(enable != 0);
   return SPEAR_OK;
@@ -357,6 +367,7 @@ const char* spear_status_string(int status) {
     case SPEAR_ERR_WORKSPACE: return "SPEAR_ERR_WORKSPACE";
     case SPEAR_ERR_CUDA: return "SPEAR_ERR_CUDA";
     case SPEAR_ERR_TIMEOUT: return "SPEAR_ERR_TIMEOUT";
+    case SPEAR_ERR_BOUNDS: return "SPEAR_ERR_BOUNDS";
     default: return "SPEAR_ERR_UNKNOWN";
   }
 }

@@ -14,7 +14,22 @@ enum : unsigned {
   DEV_OK = 0,
   DEV_ERR_INVALID = 1,
   DEV_ERR_TIMEOUT = 5,
+  DEV_ERR_BOUNDS = 6,
 };
+
+// Index checks of the debug build (compiled with -DSPEAR_DEBUG_CHECKS): a
+// check that fails records SPEAR_ERR_BOUNDS in the kernel's status word and
+// the kernel carries on (no trap).  The release build evaluates nothing.
+#ifdef SPEAR_DEBUG_CHECKS
+#define SPEAR_CHECK(word, cond)                                              \
+  do {                                                                       \
+    if (!(cond)) ::spear::record_status((word), ::spear::DEV_ERR_BOUNDS);   \
+  } while (0)
+#else
+#define SPEAR_CHECK(word, cond) \
+  do {                          \
+  } while (0)
+#endif
 
 // A pointer into shared memory moved up to the next multiple of `align`
 // bytes (a power of two) by offsetting the original pointer.  (Rounding an

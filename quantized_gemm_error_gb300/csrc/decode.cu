@@ -79,6 +79,8 @@ struct DecodeParams {
   float* ws_prod;           // [Q][Mpad][16]
   float* ws_T;              // [Mpad][r]
   unsigned* ws_sync;        // [0] producer ticket, [1] T flag, [2] streamer ticket
+  uint64_t wait_ns;         // limit of the wait for T
+  size_t smem_bytes;        // dynamic shared memory of the launch (index checks of the debug build)
 };
 
 
@@ -105,6 +107,7 @@ __device__ void producer_block(const DecodeParams& p, float* smem) {
   const int q = blockIdx.x, rt = q % RT, sl = q / RT, S = p.Q / RT;
   const int c0 = (int)((long long)sl * p.nchunks / S), c1 = (int)((long long)(sl + 1) * p.nchunks / S);
   const int npieces = (c1 - c0) * 4;                   // 32-k pieces of the slice
+  SPEAR_CHECK(&g_decode_status, 0 <= c0 && c0 <= c1 && c1 <= p.nchunks && sl < S && S <= kMaxSlices);
   float* red = smem;                                   // [kWarps][MT][4][32]
   // the vector gate's weights, copied while the slice streams (every producer:
   // which one sums the slices is known only at the end)
@@ -177,6 +180,7 @@ __device__ void producer_block(const DecodeParams& p, float* smem) {
     // C fragment element i of lane ln: row (ln/4) + 8 (i/2), token t*8 + 2 (ln%4) + (i%2)
     const int row = (ln >> 2) + 8 * (i >> 1);
     const int tok = t * 8 + 2 * (ln & 3) + (i & 1);
+    SPEAR_CHECK(&g_decode_status, q < p.Q && tok < Mpad && row < 16);
     p.ws_prod[((size_t)q * Mpad + tok) * 16 + row] = v;
   }
   named_sync(1, kThreads);
@@ -196,6 +200,7 @@ __device__ void producer_block(const DecodeParams& p, float* smem) {
     const int rti = i / 16, ri = i % 16;
     float part[kMaxSlices];
 #pragma unroll
+    SPEAR_CHECK(&g_decode_status, (S - 1) * RT + rti < p.Q && m < Mpad);
     for (int ss = 0; ss < kMaxSlices; ++ss)
       part[ss] = ss < S ? __ldcg(p.ws_prod + ((size_t)(ss * RT + rti) * Mpad + m) * 16 + ri) : 0.0f;
     float v = 0.0f;
@@ -282,6 +287,9 @@ __device__ void streamer_block(const DecodeParams& p, float* smem) {
       smem_align_up(reinterpret_cast<uint8_t*>(B_s + (COMP ? p.max_tiles * 16 * p.r : 0)), 16));   // [M][xrow] (XS)
   float* Ps = reinterpret_cast<float*>(xs + (XS ? p.M * xrow : 0));  // [M][nchunks] 1024 E + 64 O (XS)
   float* Xs = Ps + (XS ? p.M * p.nchunks : 0);                       // [M][nchunks] E + O (XS)
+  SPEAR_CHECK(&g_decode_status, 0 <= t0 && t0 <= t1 && t1 <= p.tiles && ntl <= p.max_tiles);
+  SPEAR_CHECK(&g_decode_status, reinterpret_cast<const uint8_t*>(Xs + (XS ? p.M * p.nchunks : 0)) <=
+                                    reinterpret_cast<const uint8_t*>(smem) + p.smem_bytes);
 
   if (warp == kWarps) {
     // ------------------------------------------------ helper warp
@@ -299,7 +307,7 @@ __device__ void streamer_block(const DecodeParams& p, float* smem) {
       const uint64_t tw = globaltimer_ns();
       for (unsigned i = 0;; ++i) {
         if (ld_acquire_gpu(&p.ws_sync[1])) { ok = 1; break; }
-        if ((i & 63) == 63 && globaltimer_ns() - tw > kWaitLimitNs) break;
+        if ((i & 63) == 63 && globaltimer_ns() - tw > p.wait_ns) break;
         __nanosleep(32);
       }
       if (!ok) record_status(&g_decode_status, DEV_ERR_TIMEOUT);
@@ -309,6 +317,7 @@ __device__ void streamer_block(const DecodeParams& p, float* smem) {
     // all of this lane's pairs of T in flight at once (one L2 round trip)
     constexpr int kTPairs = MT * 8 * kMaxRank / 2 / 32;
     const int npairs = Mpad * p.r / 2;
+    SPEAR_CHECK(&g_decode_status, 2 * npairs <= Mpad * kMaxRank && p.r <= kMaxRank);
     float2 tv[kTPairs];
 #pragma unroll
     for (int i = 0; i < kTPairs; ++i) {
@@ -344,6 +353,8 @@ __device__ void streamer_block(const DecodeParams& p, float* smem) {
   int issued = 0, ij = 0;
   auto issue = [&](int slot) {
     if (issued < nitems) {
+      SPEAR_CHECK(&g_decode_status, slot < kStages && src >= p.qweight &&
+                                        src + 8 * half_k + 16 <= p.qweight + (size_t)p.N * half_k);
       cp_async16(my_ring + (slot * 2 + 0) * 32 + lane, src);
       cp_async16(my_ring + (slot * 2 + 1) * 32 + lane, src + 8 * half_k);
       ++issued;
@@ -600,6 +611,7 @@ __device__ void streamer_block(const DecodeParams& p, float* smem) {
       const int tok = t * 8 + 2 * c + (i & 1);
       const int n = (i < 2) ? n_lo : n_hi;
       if (tok < p.M) {
+        SPEAR_CHECK(&g_decode_status, n < p.N);
         if (p.out_f32) reinterpret_cast<float*>(p.y)[(size_t)tok * p.N + n] = v[i];
         else reinterpret_cast<__nv_bfloat16*>(p.y)[(size_t)tok * p.N + n] = __float2bfloat16_rn(v[i]);
       }
@@ -838,6 +850,8 @@ int launch_decode(const spear_w4_layer& L, const uint16_t* x, int M, void* y, in
   p.ws_sync = reinterpret_cast<unsigned*>(base + pl.off_sync);
   p.ws_prod = reinterpret_cast<float*>(base + pl.off_prod);
   p.ws_T = reinterpret_cast<float*>(base + pl.off_T);
+  p.wait_ns = wait_limit_ns(kWaitLimitNs);
+  p.smem_bytes = pl.smem;
 
   if (int rc = ensure_smem_limit(reinterpret_cast<const void*>(pl.fn), pl.smem)) return rc;
   cudaLaunchConfig_t cfg{};

@@ -877,7 +877,6 @@ int get_ks_plan(const spear_w4_layer& L, int M, KsPlan* out) {
   return SPEAR_OK;
 }
 
-uint64_t g_ks_wait_ns = kWaitNs;
 
 }  // namespace
 
@@ -892,7 +891,6 @@ bool decode_ks_supports(const spear_w4_layer& L, int M) {
   return rc == SPEAR_OK;
 }
 
-void decode_ks_set_wait_limit_ns(uint64_t ns) { g_ks_wait_ns = ns ? ns : kWaitNs; }
 
 int launch_decode_ks(const spear_w4_layer& L, const uint16_t* x, int M, void* y, int out_f32, cudaStream_t st,
                      bool overlap) {
@@ -929,7 +927,7 @@ int launch_decode_ks(const spear_w4_layer& L, const uint16_t* x, int M, void* y,
   p.b_g = L.b_g; p.alpha = L.alpha;
   p.gh = comp ? L.gate_hidden : 0;
   p.gw1 = L.gate_w1; p.gc1 = L.gate_c1; p.gw2 = L.gate_w2; p.gc2 = L.gate_c2;
-  p.wait_ns = g_ks_wait_ns;
+  p.wait_ns = wait_limit_ns(kWaitNs);
 
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(pl.Gc * pl.C);

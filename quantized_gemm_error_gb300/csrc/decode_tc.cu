@@ -99,6 +99,7 @@ struct TcParams {
   float* ws_P;              // [NP][r + 1]: (A x)[j] for j < r, w_g . x at j = r
   unsigned* ws_sync;        // [0] producer row tiles published, [1] tile-CTA ticket, [2 + rt] Kp tickets
   uint32_t off_bf, off_x16, off_xr, off_B, off_gate;   // dynamic shared memory layout
+  uint64_t t_wait_ns;       // limit of the wait for the published P
 };
 
 __device__ __forceinline__ void give_up(int* abort_flag) {
@@ -195,6 +196,7 @@ __device__ void tc_producer(const TcParams& p, uint8_t* smem, int pc, int rank) 
   if (rank == 0) {
     // sum the S partials in rank order
     float* dst = p.Kp == 1 ? nullptr : p.ws_part + ((size_t)kp * p.RT + rt) * 16 * NP;
+    SPEAR_CHECK(&g_dtc_status, kp < p.Kp && rt < p.RT && p.S <= kMaxS && p.Kp <= kMaxKp);
     for (int e = threadIdx.x; e < 16 * NP; e += kThreads) {
       const uint32_t la = smem_u32(part + e);
       float pv[kMaxS];
@@ -351,6 +353,7 @@ __device__ void tc_tile(const CUtensorMap* tm_w, const CUtensorMap* tm_x, const 
     if (lane == 0) {
       prefetch_tmap(tm_w);
       prefetch_tmap(tm_x);
+      SPEAR_CHECK(&g_dtc_status, n0 < p.N && (nunits == 0 || unit_of(nunits - 1) * kUnitK < p.K));
       int ri = 0, xi = 0;
       // the first weight units need no slot wait and read only the layer's
       // weights: issue them before waiting for the kernel ahead (overlapped launches)
@@ -589,7 +592,7 @@ __device__ void tc_tile(const CUtensorMap* tm_w, const CUtensorMap* tm_x, const 
         int pok = 0;
         for (unsigned i = 0;; ++i) {
           if (ld_acquire_gpu(&p.ws_sync[0]) >= (unsigned)p.RT) { pok = 1; break; }
-          if ((i & 63) == 63 && globaltimer_ns() - tw > kTWaitNs) break;
+          if ((i & 63) == 63 && globaltimer_ns() - tw > p.t_wait_ns) break;
           __nanosleep(64);
         }
         if (!pok) record_status(&g_dtc_status, DEV_ERR_TIMEOUT);
@@ -732,6 +735,7 @@ __device__ void tc_tile(const CUtensorMap* tm_w, const CUtensorMap* tm_x, const 
         if (qq < S) { v.x += pv[qq].x; v.y += pv[qq].y; v.z += pv[qq].z; v.w += pv[qq].w; }
       if (nn >= p.N) continue;
       const size_t o = (size_t)t * p.N + nn;
+      SPEAR_CHECK(&g_dtc_status, t < p.M && nn < p.N && (!vec || nn + 3 < p.N));
       if (vec) {                                           // nn + 3 < N as N and nn are multiples of 4
         if (p.out_f32) {
           *reinterpret_cast<float4*>(reinterpret_cast<float*>(p.y) + o) = v;
@@ -990,6 +994,7 @@ int launch_decode_tc(const spear_w4_layer& L, const uint16_t* x, int M, void* y,
   p.ws_sync = reinterpret_cast<unsigned*>(base + pl.off_sync);
   p.ws_part = reinterpret_cast<float*>(base + pl.off_part);
   p.ws_P = reinterpret_cast<float*>(base + pl.off_P);
+  p.t_wait_ns = wait_limit_ns(kTWaitNs);
   p.off_bf = pl.off_bf; p.off_x16 = pl.off_x16; p.off_xr = pl.off_xr; p.off_B = pl.off_B; p.off_gate = pl.off_gate;
 
   if (int rc = ensure_smem_limit(reinterpret_cast<const void*>(pl.fn), pl.smem)) return rc;

@@ -34,6 +34,9 @@ bool log_plans();
 // Programmatic dependent launch for decode kernels (spear_set_launch_overlap).
 void set_launch_overlap(bool on);
 bool launch_overlap();
+// Limit of the waits on other thread blocks (spear_set_wait_limit_ns): the
+// set value, or `default_ns` while none is set.
+uint64_t wait_limit_ns(uint64_t default_ns);
 
 // Raises (never lowers) the dynamic shared-memory limit of kernel `fn` on the
 // current device to at least `bytes`.  Launches captured in CUDA graphs keep
@@ -58,14 +61,12 @@ int read_and_clear_status_decode(unsigned* out, cudaStream_t st);
 bool decode_ks_supports(const spear_w4_layer& L, int M);
 int launch_decode_ks(const spear_w4_layer& L, const uint16_t* x, int M, void* y, int out_f32, cudaStream_t st,
                      bool overlap);
-void decode_ks_set_wait_limit_ns(uint64_t ns);
 int read_and_clear_status_decode_ks(unsigned* out, cudaStream_t st);
 
 // ---- decode_tm.cu (cluster K-split decode on tcgen05, weights in tensor memory, 1..64 tokens)
 bool decode_tm_supports(const spear_w4_layer& L, int M);
 int launch_decode_tm(const spear_w4_layer& L, const uint16_t* x, int M, void* y, int out_f32, cudaStream_t st,
                      bool overlap);
-void decode_tm_set_wait_limit_ns(uint64_t ns);
 int read_and_clear_status_decode_tm(unsigned* out, cudaStream_t st);
 
 // ---- decode_tc.cu (tensor-core decode path)

@@ -109,6 +109,7 @@ pack_w4_kernel(const float* __restrict__ W, int N, int K, int G, int sym, uint8_
   for (int h = 0; h < 2; ++h) {
     const int gi = 2 * pair + h;
     if (gi >= ng) break;
+    SPEAR_CHECK(&g_pack_status, n < N && gi * G + G <= K && (gi * G) % 2 == 0);
     const int z = quantize_group(w, gi * G, G, sym, qrow, scales + (size_t)n * ng + gi, lane);
     zbyte |= z << (4 * h);
   }

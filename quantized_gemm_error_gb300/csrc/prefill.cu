@@ -120,6 +120,7 @@ w4_gemm_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
   const int nmain = ke - kb;
   const int ncomp = krank == 0 ? p.comp_stages : 0;
   const int total_stages = nmain + ncomp;
+  SPEAR_CHECK(&g_prefill_status, 0 <= kb && kb <= ke && ke <= k_stages && krank < KS && n0 < p.N && m0 < p.M);
 
   auto x_slot = [&](int s) { return smem + s * kStageBytes; };
   auto w_slot = [&](int s) { return smem + s * kStageBytes + kXBytes; };
@@ -364,6 +365,7 @@ w4_gemm_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
           continue;
         }
         if (tok < p.M) {
+          SPEAR_CHECK(&g_prefill_status, n + 32 <= p.N);
           if (p.out_f32) {
             float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.y) + (size_t)tok * p.N + n);
 #pragma unroll
@@ -402,6 +404,7 @@ w4_gemm_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
         for (int q = 1; q < 4; ++q)
           if (q < KS) { v.x += pv[q].x; v.y += pv[q].y; v.z += pv[q].z; v.w += pv[q].w; }
         if (tok >= p.M || n >= p.N) continue;               // N is a multiple of 64: n + 3 < N
+        SPEAR_CHECK(&g_prefill_status, n + 4 <= p.N);
         const size_t o = (size_t)tok * p.N + n;
         if (f32) {
           *reinterpret_cast<float4*>(reinterpret_cast<float*>(p.y) + o) = v;
@@ -654,6 +657,7 @@ __global__ void __launch_bounds__(256) comp_up_add_kernel(const CompUpParams p) 
     for (int hh = 0; hh < 2; ++hh) {
       const int tok = tok0 + g + 8 * hh;
       if (tok >= p.M) continue;
+      SPEAR_CHECK(&g_prefill_status, n + 2 <= p.N);
       const float2 m32 = *reinterpret_cast<const float2*>(p.y32 + (size_t)tok * p.N + n);
       const float v0 = m32.x + acc[t][2 * hh], v1 = m32.y + acc[t][2 * hh + 1];
       if (p.out_f32) {

@@ -24,14 +24,15 @@ LIB_PATH = os.path.join(_PKG, "lib", "libspear.so")
 
 SPEAR_OK = 0
 STATUS_NAMES = {0: "SPEAR_OK", 1: "SPEAR_ERR_INVALID_ARG", 2: "SPEAR_ERR_UNSUPPORTED",
-                3: "SPEAR_ERR_WORKSPACE", 4: "SPEAR_ERR_CUDA", 5: "SPEAR_ERR_TIMEOUT"}
+                3: "SPEAR_ERR_WORKSPACE", 4: "SPEAR_ERR_CUDA", 5: "SPEAR_ERR_TIMEOUT", 6: "SPEAR_ERR_BOUNDS"}
 PREFILL_AUTO, PREFILL_FUSED, PREFILL_STREAM = 0, 1, 2
 OUT_BF16, OUT_F32 = 0, 1
 
 # every symbol include/spear.h declares
 EXPORTS = ["spear_pack_w4_sizes", "spear_pack_w4", "spear_decode_workspace_bytes",
            "spear_linear_decode", "spear_linear_decode_noalloc", "spear_prefill_workspace_bytes", "spear_linear_prefill",
-           "spear_workspace_init", "spear_set_launch_overlap", "spear_layer_select_mask", "spear_chunk_select",
+           "spear_workspace_init", "spear_set_launch_overlap", "spear_set_wait_limit_ns", "spear_layer_select_mask",
+           "spear_chunk_select",
            "spear_linear_cka",
            "spear_get_device_status", "spear_status_string", "spear_last_error", "spear_version"]
 
@@ -82,6 +83,7 @@ def load(path: str = LIB_PATH):
             "spear_linear_cka": [P, P, I, I, I, ctypes.POINTER(ctypes.c_double)],
             "spear_get_device_status": [ctypes.POINTER(I), P],
             "spear_set_launch_overlap": [I],
+            "spear_set_wait_limit_ns": [ctypes.c_uint64],
         }
         for name, args in sig.items():
             fn = getattr(lib, name)
@@ -383,6 +385,13 @@ def spear_set_launch_overlap(enable: bool) -> None:
     guarantees that the kernel right before a decode call does not write that
     layer's weights; see include/spear.h."""
     _check(load().spear_set_launch_overlap(1 if enable else 0), "spear_set_launch_overlap")
+
+
+def spear_set_wait_limit_ns(ns: int) -> None:
+    """Process-wide limit of the device-side waits on other thread blocks (0:
+    the defaults); a wait that runs out records SPEAR_ERR_TIMEOUT.  For tests
+    and diagnostics; see include/spear.h."""
+    _check(load().spear_set_wait_limit_ns(int(ns)), "spear_set_wait_limit_ns")
 
 
 def version() -> str:
