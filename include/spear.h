@@ -145,8 +145,14 @@ spear_status spear_pack_w4(const float* W, int N, int K, int group_size, int sym
  * Every block of a launch stays resident at once; a shape too wide for that
  * (e.g. N = 131072 at 12 tokens) returns SPEAR_ERR_UNSUPPORTED.
  * Some launches carry the activations in fp16 (M <= 8 with M*K*2 <= 48 KB,
- * and M >= 17): there |x| must stay below 65504; a larger value is reported
- * as SPEAR_ERR_INVALID_ARG through spear_get_device_status.
+ * and M >= 17); any finite bf16 input is still computed.  With M <= 8 a
+ * token whose max |x| reaches 2^15 enters as x 2^-e (a power of two, exact in
+ * fp16 for every value above 2^-24 2^e) and its outputs are multiplied by
+ * 2^e.  With M >= 17 a token holding a value of 65504 or more (beyond fp16)
+ * has its main-term partial sums recomputed in fp32 from the int4 codes and
+ * the bf16 values, outside the tensor cores (slower, for such tokens only).
+ * A non-finite token value is reported as SPEAR_ERR_INVALID_ARG through
+ * spear_get_device_status.
  */
 spear_status spear_decode_workspace_bytes(const spear_w4_layer* L, int M, size_t* bytes);
 spear_status spear_linear_decode(const spear_w4_layer* L, const uint16_t* x, int M,
@@ -187,11 +193,13 @@ spear_status spear_linear_decode_noalloc(const spear_w4_layer* L, const uint16_t
  * GEMM over int4 tiles dequantized in shared memory, plus the compensator in
  * one of the modes above.  M >= 0 (M = 0: no work, SPEAR_OK).
  *   x : device bf16 [M][K];  y : device [M][N], bf16 or fp32.
- *   The main GEMM runs on fp16 operands with fp32 accumulation: the
- *   activations are copied to fp16 (exact for |x| < 65504; a larger value is
- *   reported as SPEAR_ERR_INVALID_ARG through spear_get_device_status) and a
- *   group-scaled weight is rounded once to fp16.  The compensator terms stay
- *   in bf16 with fp32 accumulation.
+ *   The main GEMM runs on fp16 operands with fp32 accumulation: each token is
+ *   copied to fp16 as x 2^-e, the smallest power-of-two scale that brings its
+ *   max |x| below 2^15 (exact for every value above 2^-24 2^e; e = 0 for most
+ *   tokens), and its outputs are multiplied by 2^e; a group-scaled weight is
+ *   rounded once to fp16.  A non-finite token value is reported as
+ *   SPEAR_ERR_INVALID_ARG through spear_get_device_status.  The compensator
+ *   terms stay in bf16 with fp32 accumulation.
  *   workspace : device, at least spear_prefill_workspace_bytes(); no zeroing
  *               needed.  stream_aux is used by SPEAR_PREFILL_STREAM only (it
  *               may be NULL otherwise); the call orders it after `stream` and
@@ -261,6 +269,15 @@ spear_status spear_layer_select_mask(const float* damage, const float* cost, int
  * n >= 2; non-finite inputs or an input without variance are rejected.
  */
 spear_status spear_linear_cka(const float* X, const float* Y, int n, int dx, int dy, double* cka_out);
+
+/*
+ * A module's damage score for spear_layer_select_mask (Technical Summary
+ * 2.1 B), host only: *damage_out = 1 - CKA(X_ref, Y_quant) with the same
+ * arguments, checks and arithmetic as spear_linear_cka (X_ref: the module's
+ * reference output, Y_quant: its quantised output on the same n tokens).
+ */
+spear_status spear_cka_damage(const float* X_ref, const float* Y_quant, int n, int dx, int dy,
+                              double* damage_out);
 
 /*
  * SLO-constrained chunk selection (Technical Summary 2.2 C), host only.

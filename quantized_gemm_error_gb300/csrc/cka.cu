@@ -108,3 +108,11 @@ spear_status spear_linear_cka(const float* X, const float* Y, int n, int dx, int
   *cka_out = xy / std::sqrt(xx * yy);
   return SPEAR_OK;
 }
+
+spear_status spear_cka_damage(const float* X_ref, const float* Y_quant, int n, int dx, int dy, double* damage_out) {
+  if (!damage_out) return fail(SPEAR_ERR_INVALID_ARG, "cka_damage: damage_out is NULL");
+  double cka = 0.0;
+  if (spear_status rc = spear_linear_cka(X_ref, Y_quant, n, dx, dy, &cka)) return rc;
+  *damage_out = 1.0 - cka;
+  return SPEAR_OK;
+}

@@ -169,6 +169,26 @@ __device__ __forceinline__ uint32_t f16x2_mul(uint32_t a, uint32_t b) {
   return *reinterpret_cast<uint32_t*>(&r);
 }
 
+// Power-of-two token scaling for the fp16 operand copies of the activations:
+// a token x_m enters as x_m 2^-e_m with the smallest e_m >= 0 that brings
+// max|x_m| below 2^15, which is exact in fp16 for every value above 2^-24 2^e_m
+// (bf16 carries 8 significant bits, fp16 11); the fp32 accumulator is
+// multiplied by 2^e_m afterwards.  e = 0 for max|x| < 2^15 and for a
+// non-finite max (reported separately).
+__device__ __forceinline__ int token_scale_exp(float amax) {
+  if (!(amax >= 32768.0f) || !(amax <= 3.4e38f)) return 0;
+  return (int)((__float_as_uint(amax) >> 23) & 0xFF) - 127 - 14;   // floor(log2 amax) - 14
+}
+// 2^k as a float, -126 <= k <= 127 (exact)
+__device__ __forceinline__ float exp2_int(int k) { return __uint_as_float((uint32_t)(k + 127) << 23); }
+// max |x| of 8 bf16 values (NaN propagates as a value above every finite one)
+__device__ __forceinline__ float bf16x8_absmax(uint4 v) {
+  const uint32_t m = 0x7fff7fffu;
+  const uint32_t a = __vmaxu2(__vmaxu2(v.x & m, v.y & m), __vmaxu2(v.z & m, v.w & m));   // bf16 bits order like |x|
+  const uint32_t b = __vmaxu2(a, a >> 16);
+  return __uint_as_float((b & 0xffffu) << 16);
+}
+
 // Four bf16x2 values holding (128 + nibble) for the 8 nibbles of `w`:
 // out[i] = (128 + nib_i, 128 + nib_{i+4}) for i = 0..3 (nib_j = bits 4j..4j+3).
 __device__ __forceinline__ void nibbles_to_bf16x2_biased(uint32_t w, uint32_t (&out)[4]) {

@@ -287,6 +287,9 @@ __device__ void streamer_block(const DecodeParams& p, float* smem) {
       smem_align_up(reinterpret_cast<uint8_t*>(B_s + (COMP ? p.max_tiles * 16 * p.r : 0)), 16));   // [M][xrow] (XS)
   float* Ps = reinterpret_cast<float*>(xs + (XS ? p.M * xrow : 0));  // [M][nchunks] 1024 E + 64 O (XS)
   float* Xs = Ps + (XS ? p.M * p.nchunks : 0);                       // [M][nchunks] E + O (XS)
+  __shared__ int s_xbigw[kWarps];                          // per compute warp: a staged unit reaches 2^15 (rare)
+  __shared__ unsigned s_xmax[8];                           // bits of max |x| per staged token (rare path)
+  __shared__ float s_xdn[8], s_xup[8];                     // 2^-e, 2^e per staged token
   SPEAR_CHECK(&g_decode_status, 0 <= t0 && t0 <= t1 && t1 <= p.tiles && ntl <= p.max_tiles);
   SPEAR_CHECK(&g_decode_status, reinterpret_cast<const uint8_t*>(Xs + (XS ? p.M * p.nchunks : 0)) <=
                                     reinterpret_cast<const uint8_t*>(smem) + p.smem_bytes);
@@ -404,11 +407,45 @@ __device__ void streamer_block(const DecodeParams& p, float* smem) {
     }
   }
 
-  // 2. tokens for XS: fp16 in B-fragment order plus per-chunk even/odd sums
+  // 2. tokens for XS: fp16 in B-fragment order plus per-chunk even/odd sums.
+  // A token whose max |x| reaches 2^15 enters as x 2^-e (power-of-two token
+  // scaling: exact in fp16 down to 2^-24 2^e); the epilogue multiplies its
+  // outputs by 2^e.  The pass below converts every token unscaled and only
+  // flags a value at or above 2^15 (or not finite); the (rare) flagged call
+  // then takes each token's maximum and converts the tokens that need it again.
+  bool any_big = false;
   if (XS) {
-    bool bad = false;
+    bool big = false;
     // 16 consecutive units (128 k) of one token are 16 consecutive lanes: their
-    // E / O partials reduce with 4 shuffles (padding units contribute zeros).
+    // E / O partials and maxima reduce with 4 shuffles (padding units contribute zeros).
+    auto stage = [&](int e, uint4 v, float sc, bool write) -> float {
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};            // (x0,x1) (x2,x3) (x4,x5) (x6,x7)
+      float f[8];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) { f[2 * i] = bf16x2_lo(w[i]) * sc; f[2 * i + 1] = bf16x2_hi(w[i]) * sc; }
+      float ev = (f[0] + f[2]) + (f[4] + f[6]);
+      float od = (f[1] + f[3]) + (f[5] + f[7]);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) big |= !(fabsf(f[i]) < 32768.0f);
+      auto h2 = [](float lo, float hi) {
+        const __half2 h = __floats2half2_rn(lo, hi);
+        return *reinterpret_cast<const uint32_t*>(&h);
+      };
+      if (write && e < xunits) {
+        const int m = e / k8, kk = e % k8;
+        xs[m * xrow + kk] = make_uint4(h2(f[0], f[4]), h2(f[1], f[5]), h2(f[2], f[6]), h2(f[3], f[7]));
+      }
+#pragma unroll
+      for (int o = 1; o < 16; o <<= 1) {
+        ev += __shfl_xor_sync(0xffffffffu, ev, o);
+        od += __shfl_xor_sync(0xffffffffu, od, o);
+      }
+      if (write && (lane & 15) == 0 && e < xunits) {
+        const int m = e / k8, ch = (e % k8) / 16;
+        Ps[m * p.nchunks + ch] = 1024.0f * ev + 64.0f * od;
+        Xs[m * p.nchunks + ch] = ev + od;
+      }
+    };
     for (int j0 = 0; j0 < xunits; j0 += kThreads * kXBatch) {
 #pragma unroll
       for (int j = 0; j < kXBatch; ++j) {
@@ -416,38 +453,73 @@ __device__ void streamer_block(const DecodeParams& p, float* smem) {
         uint4 v;
         if (j0 == 0) v = xr[j];
         else v = e < xunits ? ldg16(p.x + (size_t)e * 8) : make_uint4(0, 0, 0, 0);
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};          // (x0,x1) (x2,x3) (x4,x5) (x6,x7)
-        float f[8];
+        stage(e, v, 1.0f, true);
+      }
+    }
+    big = __any_sync(0xffffffffu, big);
+    if (lane == 0) s_xbigw[warp] = big ? 1 : 0;            // read after the barrier below
+  }
+  cp_async_wait<kStages - 1>();                            // the staged scales, zeros and B
+  named_sync(1, kThreads);
+  if (XS) {
 #pragma unroll
-        for (int i = 0; i < 4; ++i) { f[2 * i] = bf16x2_lo(w[i]); f[2 * i + 1] = bf16x2_hi(w[i]); }
-        float ev = (f[0] + f[2]) + (f[4] + f[6]);
-        float od = (f[1] + f[3]) + (f[5] + f[7]);
+    for (int w = 0; w < kWarps; ++w) any_big |= s_xbigw[w] != 0;
+  }
+  if (XS && any_big) {
+    // rare: each token's max |x|, its scale, and the tokens at or above 2^15
+    // converted again with it (E / O sums too); a non-finite value is reported
+    if (threadIdx.x < 8) s_xmax[threadIdx.x] = 0u;
+    named_sync(1, kThreads);
+    for (int e0 = 0; e0 < xunits; e0 += kThreads) {
+      const int e = threadIdx.x + e0;
+      float amax = e < xunits ? bf16x8_absmax(ldg16(p.x + (size_t)e * 8)) : 0.0f;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) bad |= !(fabsf(f[i]) < 65504.0f);
+      for (int o = 1; o < 16; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+      if ((lane & 15) == 0 && e < xunits) atomicMax(&s_xmax[e / k8], __float_as_uint(amax));
+    }
+    named_sync(1, kThreads);
+    if (threadIdx.x < 8) {
+      const int ex = token_scale_exp(__uint_as_float(s_xmax[threadIdx.x]));
+      s_xdn[threadIdx.x] = exp2_int(-ex);
+      s_xup[threadIdx.x] = exp2_int(ex);
+    }
+    named_sync(1, kThreads);
+    bool bad = false;
+    for (int e0 = 0; e0 < xunits; e0 += kThreads) {
+      const int e = threadIdx.x + e0;
+      const int m = e < xunits ? e / k8 : 0;
+      const uint4 v = e < xunits ? ldg16(p.x + (size_t)e * 8) : make_uint4(0, 0, 0, 0);
+      // (the same per-unit work as the first pass, for the tokens with a scale)
+      const float sc = s_xdn[m];
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+      float f[8];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) { f[2 * i] = bf16x2_lo(w[i]) * sc; f[2 * i + 1] = bf16x2_hi(w[i]) * sc; }
+      float ev = (f[0] + f[2]) + (f[4] + f[6]);
+      float od = (f[1] + f[3]) + (f[5] + f[7]);
+      bad |= !(bf16x8_absmax(v) <= 3.4e38f);
+      const bool write = e < xunits && s_xup[m] != 1.0f;
+      if (write) {
         auto h2 = [](float lo, float hi) {
           const __half2 h = __floats2half2_rn(lo, hi);
           return *reinterpret_cast<const uint32_t*>(&h);
         };
-        if (e < xunits) {
-          const int m = e / k8, kk = e % k8;
-          xs[m * xrow + kk] = make_uint4(h2(f[0], f[4]), h2(f[1], f[5]), h2(f[2], f[6]), h2(f[3], f[7]));
-        }
+        xs[m * xrow + e % k8] = make_uint4(h2(f[0], f[4]), h2(f[1], f[5]), h2(f[2], f[6]), h2(f[3], f[7]));
+      }
 #pragma unroll
-        for (int o = 1; o < 16; o <<= 1) {
-          ev += __shfl_xor_sync(0xffffffffu, ev, o);
-          od += __shfl_xor_sync(0xffffffffu, od, o);
-        }
-        if ((lane & 15) == 0 && e < xunits) {
-          const int m = e / k8, ch = (e % k8) / 16;
-          Ps[m * p.nchunks + ch] = 1024.0f * ev + 64.0f * od;
-          Xs[m * p.nchunks + ch] = ev + od;
-        }
+      for (int o = 1; o < 16; o <<= 1) {
+        ev += __shfl_xor_sync(0xffffffffu, ev, o);
+        od += __shfl_xor_sync(0xffffffffu, od, o);
+      }
+      if (write && (lane & 15) == 0) {
+        const int ch = (e % k8) / 16;
+        Ps[m * p.nchunks + ch] = 1024.0f * ev + 64.0f * od;
+        Xs[m * p.nchunks + ch] = ev + od;
       }
     }
     if (bad) record_status(&g_decode_status, DEV_ERR_INVALID);
+    named_sync(1, kThreads);
   }
-  cp_async_wait<kStages - 1>();                            // the staged scales, zeros and B
-  named_sync(1, kThreads);
 
   // 3. main loop
   int slot = 0;
@@ -592,6 +664,10 @@ __device__ void streamer_block(const DecodeParams& p, float* smem) {
       const float slo = __half2float(sc_s[tl * 16 * p.ng + g * p.ng]);
       const float shi = __half2float(sc_s[tl * 16 * p.ng + (g + 8) * p.ng]);
       v[0] *= slo; v[1] *= slo; v[2] *= shi; v[3] *= shi;
+    }
+    if (XS && any_big) {                                   // staged tokens' scale 2^e (outputs of tokens 2c, 2c + 1)
+      const float u0 = 2 * c < p.M ? s_xup[2 * c] : 1.0f, u1 = 2 * c + 1 < p.M ? s_xup[2 * c + 1] : 1.0f;
+      v[0] *= u0; v[1] *= u1; v[2] *= u0; v[3] *= u1;
     }
     if (COMP) {
       const int rh = p.r / 2;

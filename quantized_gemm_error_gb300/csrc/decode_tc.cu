@@ -24,9 +24,11 @@
 //             the subtraction of 1024 + z or 64 + z is exact), written in the
 //             tensor core's swizzled K-major layout; after the last MMA they
 //             drain the accumulator into this CTA's partial in shared memory;
-//   warps 0-3 convert the token tile to fp16 (exact for |x| < 65504, larger
-//             values are reported), then read the published P and form T
-//             (scalar gate) or load t = A x (vector gate) in the spent ring;
+//   warps 0-3 convert the token tile to fp16 (exact for |x| < 65504) and
+//             flag the tokens holding a larger value, then read the published
+//             P and form T (scalar gate) or load t = A x (vector gate) in the
+//             spent ring; after the drain the converter warps recompute a
+//             flagged token's partial in fp32 (tc_exact_rows);
 //   warp 21   one thread issues tcgen05.mma with the tokens as the 64-row A
 //             operand and the weights as the 256-column B operand:
 //             D[64 x 256] (+)= X[64 x 16] W[256 x 16]^T, fp32 in tensor memory.
@@ -247,6 +249,63 @@ __device__ void tc_producer(const TcParams& p, uint8_t* smem, int pc, int rank) 
 }
 
 // ---------------------------------------------------------- tile CTAs --
+// Rows n and n + 32 of the tile's partial for token t, computed in fp32 over
+// the CTA's K units from the int4 codes and the bf16 token: the path for a
+// token with a value beyond the fp16 range (the tensor core would see inf).
+// Each weight is formed as the converters form it (u - z exact, times the
+// group scale with one fp16 rounding; per-channel: u - z, the scale applied
+// to the sum), so only the summation order differs from the tensor-core path.
+template <bool PERCH>
+__device__ __forceinline__ void tc_exact_rows(const TcParams& p, float* red, const float* s_scale, int n, int t,
+                                           int rank, int nunits) {
+  const int zrow = (p.ng + 1) / 2;
+  const int row0 = n % kTileRows;
+  const __nv_bfloat16* xt = p.x + (size_t)t * p.K;
+  float acc[2] = {0.0f, 0.0f};
+  bool nonfinite = false;
+  for (int i = 0; i < nunits; ++i) {
+    const int k0 = (rank + i * p.S) * kUnitK, k1 = min(p.K, k0 + kUnitK);
+    for (int k = k0; k < k1; k += 32) {
+      float xf[32];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const uint4 v = __ldg(reinterpret_cast<const uint4*>(xt + k) + j);
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          xf[8 * j + 2 * e] = __uint_as_float(w[e] << 16);
+          xf[8 * j + 2 * e + 1] = __uint_as_float(w[e] & 0xFFFF0000u);
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < 32; ++j) nonfinite |= !(fabsf(xf[j]) <= 3.402823466e38f);
+      const int g = PERCH ? 0 : k / 128;
+#pragma unroll
+      for (int rr = 0; rr < 2; ++rr) {
+        const int nn = n + 32 * rr;
+        if (nn >= p.N) continue;
+        const uint32_t zb = p.sym ? 0x88u : (uint32_t)__ldg(p.zeros + (size_t)nn * zrow + g / 2);
+        const int z = (int)((g & 1) ? (zb >> 4) : (zb & 15u));
+        const __half sc = PERCH ? __float2half(1.0f) : __ldg(p.scales + (size_t)nn * p.ng + g);
+        const uint4 cv = __ldg(reinterpret_cast<const uint4*>(p.qweight + (size_t)nn * (p.K / 2) + k / 2));
+        const uint32_t cw[4] = {cv.x, cv.y, cv.z, cv.w};
+        float a = acc[rr];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const int u = (int)((cw[j >> 3] >> (4 * (j & 7))) & 15u);
+          const float wv = PERCH ? (float)(u - z) : __half2float(__hmul(__int2half_rn(u - z), sc));
+          a = fmaf(wv, xf[j], a);
+        }
+        acc[rr] = a;
+      }
+    }
+  }
+  if (nonfinite) record_status(&g_dtc_status, DEV_ERR_INVALID);   // inf or NaN among the token's values
+#pragma unroll
+  for (int rr = 0; rr < 2; ++rr)
+    red[t * kRedStride + row0 + 32 * rr] = (n + 32 * rr < p.N) ? s_scale[row0 + 32 * rr] * acc[rr] : 0.0f;
+}
+
 // One CTA = 256 weight rows x its K units.  The tensor core sees the tokens
 // as the 64-row A operand (M = 64: accumulator row m lives in TMEM lane
 // (m mod 16) + 32 (m / 16)) and the weights as the 256-column B operand, so
@@ -265,6 +324,7 @@ __device__ void tc_tile(const CUtensorMap* tm_w, const CUtensorMap* tm_x, const 
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
   __shared__ int s_pok;
+  __shared__ unsigned s_big[2];   // tokens whose fp16 copy overflowed on this CTA's K range (bit t)
   unsigned ticket = 0;            // thread 0: this CTA's place among the tile CTAs past the P wait
   __shared__ float s_scale[kTileRows];                     // per-channel scales of the tile rows
 
@@ -320,9 +380,10 @@ __device__ void tc_tile(const CUtensorMap* tm_w, const CUtensorMap* tm_x, const 
       mbar_init(smem_u32(&bf_full[i]), kConvWarps);
       mbar_init(smem_u32(&bf_empty[i]), 1);
     }
-    mbar_init(smem_u32(&acc_full), 1);
+    mbar_init(smem_u32(&acc_full), 1 + kXWarps);          // the last commit and the token warps' flags
     s_abort = 0;
     s_pok = 0;
+    s_big[0] = s_big[1] = 0u;
     fence_mbar_init();
   }
   if (warp == kMmaWarp) {
@@ -542,6 +603,15 @@ __device__ void tc_tile(const CUtensorMap* tm_w, const CUtensorMap* tm_x, const 
                             s_scale[c0 + i + 3] * __uint_as_float(v[i + 3]));
         }
       }
+      // tokens of this warp whose fp16 copy overflowed: their rows of the
+      // partial are recomputed here in fp32 (the flags were set before the
+      // token warps arrived on acc_full)
+      const uint32_t big16 = (s_big[q >> 1] >> (16 * (q & 1))) & 0xFFFFu;
+      if (big16 != 0u) {
+        __syncwarp();
+        for (uint32_t b = big16; b != 0u; b &= b - 1u)
+          tc_exact_rows<PERCH>(p, red, s_scale, n0 + cb + lane, 16 * q + (__ffs(b) - 1), rank, nunits);
+      }
     } else {
       give_up(&s_abort);
     }
@@ -549,7 +619,8 @@ __device__ void tc_tile(const CUtensorMap* tm_w, const CUtensorMap* tm_x, const 
     // --------------------------- token converters + epilogue (warps 0-3)
     const int tid = threadIdx.x;                           // 0..127
     pdl_wait();                                            // they read the workspace
-    bool ok = true, bad = false;
+    bool ok = true;
+    uint32_t bigm = 0;                                     // bit i: chunk tid + 128 i held |x| >= 65504
     for (int s = 0; s < nsteps; ++s) {
       const int rs = s % kXrStages, xs = s % kX16Stages;
       ok = ok && mbar_wait(smem_u32(&xr_full[rs]), (s / kXrStages) & 1, kPipeWaitNs) &&
@@ -559,15 +630,15 @@ __device__ void tc_tile(const CUtensorMap* tm_w, const CUtensorMap* tm_x, const 
         const uint8_t* src = xr_ring + rs * NP * 128;
         uint8_t* dst = x16_ring + xs * kX16Bytes;
 #pragma unroll
-        for (int c = tid; c < NP * 8; c += kXWarps * 32) {
+        for (int i = 0; i < NP * 8 / (kXWarps * 32); ++i) {
           // 16-byte chunk c: token c / 8, k 8 (c % 8) .. +7; same swizzled place in both tiles
-          const int t = c >> 3, off = t * 128 + (((c & 7) ^ (t & 7)) << 4);
+          const int c = tid + i * (kXWarps * 32), t = c >> 3, off = t * 128 + (((c & 7) ^ (t & 7)) << 4);
           const uint4 v = *reinterpret_cast<const uint4*>(src + off);
           const float x0 = bf16x2_lo(v.x), x1 = bf16x2_hi(v.x), x2 = bf16x2_lo(v.y), x3 = bf16x2_hi(v.y);
           const float x4 = bf16x2_lo(v.z), x5 = bf16x2_hi(v.z), x6 = bf16x2_lo(v.w), x7 = bf16x2_hi(v.w);
           const float m = fmaxf(fmaxf(fmaxf(fabsf(x0), fabsf(x1)), fmaxf(fabsf(x2), fabsf(x3))),
                                 fmaxf(fmaxf(fabsf(x4), fabsf(x5)), fmaxf(fabsf(x6), fabsf(x7))));
-          bad |= !(m < 65504.0f);
+          bigm |= (m < 65504.0f ? 0u : 1u) << i;
           auto h2 = [](float lo, float hi) {
             const __half2 h = __floats2half2_rn(lo, hi);
             return *reinterpret_cast<const uint32_t*>(&h);
@@ -582,7 +653,13 @@ __device__ void tc_tile(const CUtensorMap* tm_w, const CUtensorMap* tm_x, const 
         mbar_arrive(smem_u32(&xr_empty[rs]));
       }
     }
-    if (bad) record_status(&g_dtc_status, DEV_ERR_INVALID);
+    // tokens whose fp16 copy overflowed somewhere in this CTA's K range
+    for (uint32_t b = bigm; b != 0u; b &= b - 1u) {
+      const int t = (tid + (kXWarps * 32) * (__ffs(b) - 1)) >> 3;
+      atomicOr(&s_big[t >> 5], 1u << (t & 31));
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_u32(&acc_full));      // the overflow flags are in place
 
     if (COMP) {
       // the published P: gate per token, then T = alpha g P (P read straight

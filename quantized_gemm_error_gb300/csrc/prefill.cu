@@ -86,6 +86,7 @@ struct GemmParams {
   int t_row_bytes;      // bytes per T2 row box (<= 128)
   int b_row_bytes;      // bytes per B row (2r)
   int ks;               // CTAs of a cluster splitting K (1, 2 or 4; 128-token tiles only)
+  const float* tscale;  // [M] 2^e_m: the fp16 token copy holds x_m 2^-e_m (power-of-two token scaling)
 };
 
 // K split: the partial accumulators of a cluster meet in shared memory,
@@ -313,7 +314,17 @@ w4_gemm_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
     }
 
     // epilogue: TMEM lanes 32*(warp%4) .. +31 are this warp's rows (tokens);
-    // warps 2-5 take output columns [0, 128), warps 6-9 columns [128, 256)
+    // warps 2-5 take output columns [0, 128), warps 6-9 columns [128, 256).
+    // The fp16 token copy held x 2^-e (power-of-two token scaling): the main
+    // term is multiplied by 2^e (loaded before the wait); a correction in its
+    // own accumulator is unscaled, one in the main accumulators was scaled
+    // with the tokens.
+    float tsc0 = 1.0f, tsc1 = 1.0f;
+    {
+      const int tk = m0 + 32 * (warp & 3) + lane;
+      if (tk < p.M) tsc0 = __ldg(p.tscale + tk);
+      if (kMH > 1 && tk + 128 < p.M) tsc1 = __ldg(p.tscale + tk + 128);
+    }
     ok = __all_sync(0xffffffffu, ok && mbar_wait(smem_u32(&bar_acc), 0, kWaitNs));
     if (!ok) give_up();
     tc_fence_after();
@@ -351,6 +362,9 @@ w4_gemm_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
 #pragma unroll
           for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
         }
+        const float tsc = mh ? tsc1 : tsc0;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] *= tsc;
         if (sep_comp) {
 #pragma unroll
           for (int i = 0; i < 32; ++i) v[i] += __uint_as_float(rc[i]);
@@ -446,17 +460,16 @@ struct CompDownParams {
   __nv_bfloat16* T2;    // [M][t2_cols]: T_hi in [0, r), T_lo in [r, 2r)
   int t2_cols;
   __half* x16;          // optional [M][K] fp16 copy of x for the GEMM (NULL: not written)
+  float* tscale;        // with x16: [M] the scale 2^e_m of each token's copy (written here)
+  int scale_T;          // T2 holds T_m 2^-e_m (the correction joins the GEMM's scaled accumulators)
 };
 
-// 8 consecutive bf16 (k0..k7) -> 8 fp16 in the GEMM's operand order within an
-// 8-k chunk: (k0,k4) (k1,k5) (k2,k6) (k3,k7).  Exact inside the fp16 range;
-// flags values beyond it.
-__device__ __forceinline__ uint4 bf16x8_to_f16x8(uint4 v, bool& out_of_range) {
-  const float x0 = bf16x2_lo(v.x), x1 = bf16x2_hi(v.x), x2 = bf16x2_lo(v.y), x3 = bf16x2_hi(v.y);
-  const float x4 = bf16x2_lo(v.z), x5 = bf16x2_hi(v.z), x6 = bf16x2_lo(v.w), x7 = bf16x2_hi(v.w);
-  const float m = fmaxf(fmaxf(fmaxf(fabsf(x0), fabsf(x1)), fmaxf(fabsf(x2), fabsf(x3))),
-                        fmaxf(fmaxf(fabsf(x4), fabsf(x5)), fmaxf(fabsf(x6), fabsf(x7))));
-  out_of_range |= !(m < 65504.0f);
+// 8 consecutive bf16 (k0..k7), times the token's scale 2^-e (a power of two,
+// so exact), -> 8 fp16 in the GEMM's operand order within an 8-k chunk:
+// (k0,k4) (k1,k5) (k2,k6) (k3,k7).
+__device__ __forceinline__ uint4 bf16x8_to_f16x8(uint4 v, float sc) {
+  const float x0 = bf16x2_lo(v.x) * sc, x1 = bf16x2_hi(v.x) * sc, x2 = bf16x2_lo(v.y) * sc, x3 = bf16x2_hi(v.y) * sc;
+  const float x4 = bf16x2_lo(v.z) * sc, x5 = bf16x2_hi(v.z) * sc, x6 = bf16x2_lo(v.w) * sc, x7 = bf16x2_hi(v.w) * sc;
   auto h2 = [](float lo, float hi) {
     const __half2 h = __floats2half2_rn(lo, hi);
     return *reinterpret_cast<const uint32_t*>(&h);
@@ -482,6 +495,19 @@ __global__ void __launch_bounds__(kCdThreads) comp_down_kernel(const CompDownPar
   const int tok0 = (int)(blockIdx.x / CK) * kCdTok;
   const int npieces = p.K / 32;
   const int pc0 = rank * npieces / CK, pc1 = (rank + 1) * npieces / CK;
+  // Power-of-two token scaling of the fp16 copy: the copy is written
+  // unscaled while each thread keeps the max |x| of its tokens (bits of a
+  // non-negative float order like the values; NaN above inf); the cluster's
+  // maxima meet in distributed shared memory with the partials, and only a
+  // token whose max reaches 2^15 (rare) is converted again, scaled.
+  __shared__ unsigned s_wmax[kCdWarps][kCdTok];            // per warp
+  __shared__ unsigned s_tmax[kCdTok];                      // this CTA's K range
+  __shared__ float s_tsc[kCdTok];                          // 2^-e of each token of the tile
+  __shared__ int s_tany;                                   // some token of the tile is scaled
+  if (threadIdx.x == 0) s_tany = 0;                        // read after two cluster barriers
+  unsigned tm[kCdMT];
+#pragma unroll
+  for (int t = 0; t < kCdMT; ++t) tm[t] = 0u;
   // the vector gate's weights (h <= 32, r <= 64), copied by rank 0 while its
   // K slice streams
   __shared__ __align__(16) float gate_s[gate_smem_floats(64, 32)];
@@ -494,7 +520,6 @@ __global__ void __launch_bounds__(kCdThreads) comp_down_kernel(const CompDownPar
     for (int t = 0; t < kCdMT; ++t)
 #pragma unroll
       for (int i = 0; i < 4; ++i) acc[rt][t][i] = 0.0f;
-  bool bad = false;
   for (int pb = pc0 + warp; pb < pc1; pb += U * kCdWarps) {
     uint4 xv[U][kCdMT], va[U][RT], vb[U][RT];
 #pragma unroll
@@ -527,7 +552,8 @@ __global__ void __launch_bounds__(kCdThreads) comp_down_kernel(const CompDownPar
 #pragma unroll
         for (int t = 0; t < kCdMT; ++t) {
           const int tok = tok0 + t * 8 + g;
-          if (tok < p.M) *reinterpret_cast<uint4*>(p.x16 + (size_t)tok * p.K + kb) = bf16x8_to_f16x8(xv[u][t], bad);
+          tm[t] = max(tm[t], __float_as_uint(bf16x8_absmax(xv[u][t])));   // zeros past M
+          if (tok < p.M) *reinterpret_cast<uint4*>(p.x16 + (size_t)tok * p.K + kb) = bf16x8_to_f16x8(xv[u][t], 1.0f);
         }
       }
 #pragma unroll
@@ -539,7 +565,15 @@ __global__ void __launch_bounds__(kCdThreads) comp_down_kernel(const CompDownPar
         }
     }
   }
-  if (bad) record_status(&g_prefill_status, DEV_ERR_INVALID);
+  if (p.x16) {
+    // lanes 4g .. 4g + 3 hold tokens g and 8 + g of the tile
+#pragma unroll
+    for (int t = 0; t < kCdMT; ++t) {
+      tm[t] = max(tm[t], __shfl_xor_sync(0xffffffffu, tm[t], 1));
+      tm[t] = max(tm[t], __shfl_xor_sync(0xffffffffu, tm[t], 2));
+      if (c == 0) s_wmax[warp][t * 8 + g] = tm[t];
+    }
+  }
   // fixed-order sum over the warps, one projection-row tile at a time
 #pragma unroll
   for (int rt = 0; rt < RT; ++rt) {
@@ -558,7 +592,26 @@ __global__ void __launch_bounds__(kCdThreads) comp_down_kernel(const CompDownPar
     }
     __syncthreads();
   }
-  cluster_sync();                                          // every CTA's partial is in place
+  if (p.x16 && threadIdx.x < kCdTok) {                     // (the warps' maxima are behind the barriers above)
+    unsigned m = 0u;
+#pragma unroll
+    for (int w = 0; w < kCdWarps; ++w) m = max(m, s_wmax[w][threadIdx.x]);
+    s_tmax[threadIdx.x] = m;
+  }
+  cluster_sync();                                          // every CTA's partial and maxima are in place
+  if (p.x16 && threadIdx.x < kCdTok) {
+    unsigned m = 0u;
+    for (int q = 0; q < CK; ++q)
+      m = max(m, __float_as_uint(dsmem_ld_f32(dsmem_addr(smem_u32(&s_tmax[threadIdx.x]), (uint32_t)q))));
+    const int ex = token_scale_exp(__uint_as_float(m));
+    s_tsc[threadIdx.x] = exp2_int(-ex);
+    if (ex > 0) s_tany = 1;
+    const int tok = tok0 + (int)threadIdx.x;
+    if (rank == 0 && tok < p.M) {
+      p.tscale[tok] = exp2_int(ex);
+      if (m > 0x7f7fffffu) record_status(&g_prefill_status, DEV_ERR_INVALID);   // inf or NaN
+    }
+  }
   if (rank == 0) {
     // the CK partials in rank order (all loads in flight), into this CTA's own
     // partial; then row r is the gate logit, rows 0..r-1 the down-projection
@@ -576,6 +629,17 @@ __global__ void __launch_bounds__(kCdThreads) comp_down_kernel(const CompDownPar
     }
   }
   cluster_sync();                                          // peers are done reading; rank 0's sums in place
+  if (p.x16 && s_tany) {
+    // rare: the tokens that take a scale, converted again over this CTA's K range
+    const int units = (pc1 - pc0) * 4;                     // 8-k units
+    for (int e = threadIdx.x; e < kCdTok * units; e += kCdThreads) {
+      const int t = e / units, tok = tok0 + t;
+      if (tok < p.M && s_tsc[t] != 1.0f) {
+        const size_t o = (size_t)tok * p.K + pc0 * 32 + (e % units) * 8;
+        *reinterpret_cast<uint4*>(p.x16 + o) = bf16x8_to_f16x8(ldg16(p.x + o), s_tsc[t]);
+      }
+    }
+  }
   __shared__ float hid[kCdTok * gate_hid_stride(32)];      // [16 tokens][h | 1]
   if (rank == 0 && p.gh > 0) {
     // vector gate on the summed partial (part[j][m]): t scaled in place by gamma(t)
@@ -592,7 +656,8 @@ __global__ void __launch_bounds__(kCdThreads) comp_down_kernel(const CompDownPar
       const int m = e / p.r, j = e % p.r;
       const int tok = tok0 + m;
       const float gate = p.gh > 0 ? 1.0f : 1.0f / (1.0f + expf(-(part[p.r][m] + p.b_g)));
-      const float tv = p.alpha * gate * part[j][m];
+      // T_m 2^-e_m when the correction joins the GEMM's scaled accumulators
+      const float tv = p.alpha * gate * part[j][m] * (p.scale_T ? s_tsc[m] : 1.0f);
       const __nv_bfloat16 hi = __float2bfloat16_rn(tv);
       const __nv_bfloat16 lo = __float2bfloat16_rn(tv - __bfloat162float(hi));
       if (tok < p.M) {
@@ -604,13 +669,57 @@ __global__ void __launch_bounds__(kCdThreads) comp_down_kernel(const CompDownPar
 }
 
 // --------------------------------------------------------------- to_fp16 --
-// fp16 copy of the activations for the GEMM when no compensator pass reads them.
+// fp16 copy of the activations for the GEMM when no compensator pass reads
+// them, one token row per block at a time: the row's 16-byte units are loaded
+// into registers (CPT per thread) while the row's max |x| is taken, then
+// written with the row's power-of-two scale 2^-e (e = 0 unless the max reaches
+// 2^15).  CPT = 0: rows longer than 4096 units, read twice.
+template <int CPT>
 __global__ void __launch_bounds__(256) to_fp16_kernel(const uint4* __restrict__ x, uint4* __restrict__ x16,
-                                                      size_t n8) {
-  bool bad = false;
-  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n8; i += (size_t)gridDim.x * blockDim.x)
-    x16[i] = bf16x8_to_f16x8(__ldg(x + i), bad);
-  if (bad) record_status(&g_prefill_status, DEV_ERR_INVALID);
+                                                      float* __restrict__ tscale, int M, int K) {
+  constexpr int kT = 256;
+  __shared__ unsigned s_max[2][kT / 32];                   // per warp, alternating rows
+  const int k8 = K / 8, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  int par = 0;
+  for (int m = blockIdx.x; m < M; m += gridDim.x, par ^= 1) {
+    const uint4* row = x + (size_t)m * k8;
+    uint4* out = x16 + (size_t)m * k8;
+    constexpr int kR = CPT > 0 ? CPT : 1;
+    uint4 v[kR];
+    unsigned am = 0u;                                      // bits of max |x| (NaN above inf)
+    if constexpr (CPT > 0) {
+#pragma unroll
+      for (int i = 0; i < CPT; ++i) {
+        const int j = (int)threadIdx.x + kT * i;
+        v[i] = j < k8 ? __ldg(row + j) : make_uint4(0, 0, 0, 0);
+        am = max(am, __float_as_uint(bf16x8_absmax(v[i])));
+      }
+    } else {
+      for (int j = threadIdx.x; j < k8; j += kT) am = max(am, __float_as_uint(bf16x8_absmax(__ldg(row + j))));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) am = max(am, __shfl_xor_sync(0xffffffffu, am, o));
+    if (lane == 0) s_max[par][warp] = am;
+    __syncthreads();                                       // (the other slot is still being read for the last row)
+    unsigned mx = 0u;
+#pragma unroll
+    for (int w = 0; w < kT / 32; ++w) mx = max(mx, s_max[par][w]);
+    const int ex = token_scale_exp(__uint_as_float(mx));
+    const float sc = exp2_int(-ex);
+    if constexpr (CPT > 0) {
+#pragma unroll
+      for (int i = 0; i < CPT; ++i) {
+        const int j = (int)threadIdx.x + kT * i;
+        if (j < k8) out[j] = bf16x8_to_f16x8(v[i], sc);
+      }
+    } else {
+      for (int j = threadIdx.x; j < k8; j += kT) out[j] = bf16x8_to_f16x8(__ldg(row + j), sc);
+    }
+    if (threadIdx.x == 0) {
+      tscale[m] = exp2_int(ex);
+      if (mx > 0x7f7fffffu) record_status(&g_prefill_status, DEV_ERR_INVALID);   // inf or NaN
+    }
+  }
 }
 
 // ----------------------------------------------------------- comp_up_add --
@@ -704,8 +813,8 @@ int pick_ks(int BM, int ctas, int k_steps, int num_sms) {
   return ks;
 }
 
-int launch_gemm(const spear_w4_layer& L, const __half* x16, int M, void* y, int out_f32, const __nv_bfloat16* T2,
-                int r_fused, cudaStream_t st) {
+int launch_gemm(const spear_w4_layer& L, const __half* x16, const float* tscale, int M, void* y, int out_f32,
+                const __nv_bfloat16* T2, int r_fused, cudaStream_t st) {
   DeviceInfo di;
   if (int rc = device_info(&di)) return rc;
   const bool perch = L.group_size == L.K;
@@ -724,6 +833,7 @@ int launch_gemm(const spear_w4_layer& L, const __half* x16, int M, void* y, int 
   p.scales = reinterpret_cast<const __half*>(L.scales);
   p.zeros = L.zeros;
   p.y = y; p.out_f32 = out_f32;
+  p.tscale = tscale;
   p.r = r_fused;
   if (r_fused > 0) {
     const int tcols = t2_cols_for(r_fused);
@@ -765,11 +875,13 @@ int launch_gemm(const spear_w4_layer& L, const __half* x16, int M, void* y, int 
 }
 
 int launch_comp_down(const spear_w4_layer& L, const uint16_t* x, int M, __nv_bfloat16* T2, __half* x16,
-                     cudaStream_t st) {
+                     float* tscale, int scale_T, cudaStream_t st) {
   DeviceInfo di;
   if (int rc = device_info(&di)) return rc;
   CompDownParams p{};
   p.x16 = x16;
+  p.tscale = tscale;
+  p.scale_T = scale_T;
   p.M = M; p.K = L.K; p.r = L.rank;
   p.x = reinterpret_cast<const __nv_bfloat16*>(x);
   p.A = reinterpret_cast<const __nv_bfloat16*>(L.A);
@@ -801,10 +913,15 @@ int launch_comp_down(const spear_w4_layer& L, const uint16_t* x, int M, __nv_bfl
   return cuda_check(e, "comp_down launch");
 }
 
-int launch_to_fp16(const uint16_t* x, __half* x16, size_t n, cudaStream_t st) {
-  const size_t n8 = n / 8;   // K % 128 == 0, so every row is a whole number of 16-byte groups
-  const unsigned blocks = (unsigned)std::min<size_t>((n8 + 255) / 256, 148 * 16);
-  to_fp16_kernel<<<blocks, 256, 0, st>>>(reinterpret_cast<const uint4*>(x), reinterpret_cast<uint4*>(x16), n8);
+int launch_to_fp16(const uint16_t* x, __half* x16, float* tscale, int M, int K, cudaStream_t st) {
+  DeviceInfo di;
+  if (int rc = device_info(&di)) return rc;
+  // K % 128 == 0, so every row is a whole number of 16-byte units
+  const int units = K / 8;
+  auto fn = units <= 256 ? to_fp16_kernel<1> : units <= 512 ? to_fp16_kernel<2> : units <= 1024 ? to_fp16_kernel<4>
+          : units <= 2048 ? to_fp16_kernel<8> : units <= 4096 ? to_fp16_kernel<16> : to_fp16_kernel<0>;
+  const unsigned blocks = (unsigned)std::min(M, di.num_sms * 8);
+  fn<<<blocks, 256, 0, st>>>(reinterpret_cast<const uint4*>(x), reinterpret_cast<uint4*>(x16), tscale, M, K);
   return cuda_check(cudaGetLastError(), "to_fp16 launch");
 }
 
@@ -842,9 +959,10 @@ int stream_events(StreamEvents* ev) {
   return SPEAR_OK;
 }
 
-// Workspace: [T2: M x 2r bf16][X16: M x K fp16][Y32: M x N fp32, stream mode with bf16 output only]
+// Workspace: [T2: M x 2r bf16][X16: M x K fp16][token scales: M fp32]
+// [Y32: M x N fp32, stream mode with bf16 output only]
 struct WsLayout {
-  size_t t2, x16, y32, total;
+  size_t t2, x16, ts, y32, total;
 };
 
 WsLayout ws_layout(const spear_w4_layer& L, int M, int mode, int out_f32) {
@@ -853,6 +971,7 @@ WsLayout ws_layout(const spear_w4_layer& L, int M, int mode, int out_f32) {
   size_t off = 0;
   w.t2 = off;  off = align256(off + (comp ? (size_t)M * t2_cols_for(L.rank) * 2 : 0));
   w.x16 = off; off = align256(off + (size_t)M * L.K * 2);
+  w.ts = off;  off = align256(off + (size_t)M * 4);
   w.y32 = off;
   if (comp && resolve_mode(mode) == SPEAR_PREFILL_STREAM && !out_f32) off = align256(off + (size_t)M * L.N * 4);
   w.total = off;
@@ -880,13 +999,17 @@ int launch_prefill(const spear_w4_layer& L, const uint16_t* x, int M, void* y, i
   char* base = reinterpret_cast<char*>(ws);
   __nv_bfloat16* T2 = reinterpret_cast<__nv_bfloat16*>(base + lay.t2);
   __half* x16 = reinterpret_cast<__half*>(base + lay.x16);
+  float* ts = reinterpret_cast<float*>(base + lay.ts);
   if (!comp) {
-    if (int rc = launch_to_fp16(x, x16, (size_t)M * L.K, st)) return rc;
-    return launch_gemm(L, x16, M, y, out_f32, nullptr, 0, st);
+    if (int rc = launch_to_fp16(x, x16, ts, M, L.K, st)) return rc;
+    return launch_gemm(L, x16, ts, M, y, out_f32, nullptr, 0, st);
   }
   if (resolve_mode(mode) == SPEAR_PREFILL_FUSED) {
-    if (int rc = launch_comp_down(L, x, M, T2, x16, st)) return rc;
-    return launch_gemm(L, x16, M, y, out_f32, T2, L.rank, st);
+    // 256-token tiles add the correction into the main (token-scaled) accumulators
+    const bool perch = L.group_size == L.K;
+    const int scale_T = pick_bm(M, L.N, perch, di.num_sms) == 256 ? 1 : 0;
+    if (int rc = launch_comp_down(L, x, M, T2, x16, ts, scale_T, st)) return rc;
+    return launch_gemm(L, x16, ts, M, y, out_f32, T2, L.rank, st);
   }
   // stream mode: the down-projection runs on st_aux beside the W4 GEMM on st;
   // the GEMM writes fp32 so the up-projection-and-add rounds only once
@@ -896,10 +1019,10 @@ int launch_prefill(const spear_w4_layer& L, const uint16_t* x, int M, void* y, i
   if (int rc = stream_events(&ev)) return rc;
   if (int rc = cuda_check(cudaEventRecord(ev.fork, st), "fork record")) return rc;
   if (int rc = cuda_check(cudaStreamWaitEvent(st_aux, ev.fork, 0), "fork wait")) return rc;
-  if (int rc = launch_comp_down(L, x, M, T2, nullptr, st_aux)) return rc;
+  if (int rc = launch_comp_down(L, x, M, T2, nullptr, nullptr, 0, st_aux)) return rc;
   if (int rc = cuda_check(cudaEventRecord(ev.join, st_aux), "join record")) return rc;
-  if (int rc = launch_to_fp16(x, x16, (size_t)M * L.K, st)) return rc;
-  if (int rc = launch_gemm(L, x16, M, y32, 1, nullptr, 0, st)) return rc;
+  if (int rc = launch_to_fp16(x, x16, ts, M, L.K, st)) return rc;
+  if (int rc = launch_gemm(L, x16, ts, M, y32, 1, nullptr, 0, st)) return rc;
   if (int rc = cuda_check(cudaStreamWaitEvent(st, ev.join, 0), "join wait")) return rc;
   return launch_comp_up(L, M, y, out_f32, y32, T2, st);
 }

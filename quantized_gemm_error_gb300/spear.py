@@ -33,7 +33,7 @@ EXPORTS = ["spear_pack_w4_sizes", "spear_pack_w4", "spear_decode_workspace_bytes
            "spear_linear_decode", "spear_linear_decode_noalloc", "spear_prefill_workspace_bytes", "spear_linear_prefill",
            "spear_workspace_init", "spear_set_launch_overlap", "spear_set_wait_limit_ns", "spear_layer_select_mask",
            "spear_chunk_select",
-           "spear_linear_cka",
+           "spear_linear_cka", "spear_cka_damage",
            "spear_get_device_status", "spear_status_string", "spear_last_error", "spear_version"]
 
 
@@ -81,6 +81,7 @@ def load(path: str = LIB_PATH):
             "spear_layer_select_mask": [P, P, I, ctypes.c_double, I, I, P, P],
             "spear_chunk_select": [P, P, I, I, P, I, ctypes.c_double, ctypes.POINTER(I), ctypes.POINTER(ctypes.c_double)],
             "spear_linear_cka": [P, P, I, I, I, ctypes.POINTER(ctypes.c_double)],
+            "spear_cka_damage": [P, P, I, I, I, ctypes.POINTER(ctypes.c_double)],
             "spear_get_device_status": [ctypes.POINTER(I), P],
             "spear_set_launch_overlap": [I],
             "spear_set_wait_limit_ns": [ctypes.c_uint64],
@@ -241,6 +242,35 @@ def new_workspace(nbytes: int, device, zero: bool = True) -> torch.Tensor:
     return ws
 
 
+# Workspaces of the calls made without one: one per (kind, device, stream),
+# grown when a call needs more and otherwise reused.  Calls on one stream run
+# in order, so they never use it at the same time; a decode workspace is left
+# ready for the next call by the kernel itself.
+_default_ws = {}
+
+
+def _default_workspace(kind: str, nbytes: int, device, stream, zero: bool) -> torch.Tensor:
+    dev = torch.device(device)
+    idx = dev.index if dev.index is not None else torch.cuda.current_device()
+    key = (kind, idx, _stream(stream).value or 0)
+    ws = _default_ws.get(key)
+    if ws is None or ws.numel() < nbytes:
+        ws = torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=torch.device("cuda", idx))
+        if isinstance(stream, torch.cuda.Stream):
+            ws.record_stream(stream)                  # freed (when replaced) only after that stream's work
+        if zero:
+            spear_workspace_init(ws, stream)          # on the stream the calls use
+        _default_ws[key] = ws
+    return ws
+
+
+def reset_default_workspaces() -> None:
+    """Drops the workspaces kept for calls made without one (the next call
+    makes a zeroed one): after spear_get_device_status reports
+    SPEAR_ERR_TIMEOUT, or to release the memory."""
+    _default_ws.clear()
+
+
 def spear_workspace_init(ws: torch.Tensor, stream=None):
     _check(load().spear_workspace_init(_ptr(ws), ws.numel() * ws.element_size(), _stream(stream)),
            "spear_workspace_init")
@@ -269,12 +299,14 @@ def _out(y, M, N, out_dtype, device):
 
 def spear_linear_decode(layer: W4Layer, x: torch.Tensor, *, y=None, out_dtype: int = OUT_BF16,
                         workspace: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
-    """y = dequant(Wq) x + alpha g(x) B (A x) for M <= 64 tokens, one kernel launch."""
+    """y = dequant(Wq) x + alpha g(x) B (A x) for M <= 64 tokens, one kernel launch.
+    Without `workspace` the call uses the binding's workspace for this device
+    and stream (made once, zeroed, then reused; see reset_default_workspaces)."""
     _check_io(layer, x, y, out_dtype)
     M = x.shape[0]
     y = _out(y, M, layer.N, out_dtype, x.device)
     if workspace is None:
-        workspace = new_workspace(spear_decode_workspace_bytes(layer, M), x.device)
+        workspace = _default_workspace("decode", spear_decode_workspace_bytes(layer, M), x.device, stream, True)
     L = layer.c_struct()
     _check(load().spear_linear_decode(ctypes.byref(L), _ptr(x), M, _ptr(y), out_dtype, _ptr(workspace),
                                       workspace.numel(), _stream(stream)), "spear_linear_decode")
@@ -301,7 +333,8 @@ def spear_linear_prefill(layer: W4Layer, x: torch.Tensor, *, y=None, out_dtype: 
     M = x.shape[0]
     y = _out(y, M, layer.N, out_dtype, x.device)
     if workspace is None:
-        workspace = new_workspace(spear_prefill_workspace_bytes(layer, M, mode), x.device, zero=False)
+        workspace = _default_workspace("prefill", spear_prefill_workspace_bytes(layer, M, mode), x.device, stream,
+                                       False)
     L = layer.c_struct()
     aux = None if stream_aux is None else _stream(stream_aux)
     _check(load().spear_linear_prefill(ctypes.byref(L), _ptr(x), M, _ptr(y), out_dtype, mode,
@@ -336,10 +369,24 @@ def spear_linear_cka(X, Y) -> float:
     return out.value
 
 
+def spear_cka_damage(X_ref, Y_quant) -> float:
+    """1 - CKA(X_ref, Y_quant) of two host matrices [n][dx], [n][dy] (fp32),
+    computed by the library: one module's damage score."""
+    x = np.ascontiguousarray(X_ref, dtype=np.float32)
+    y = np.ascontiguousarray(Y_quant, dtype=np.float32)
+    if x.ndim != 2 or y.ndim != 2 or x.shape[0] != y.shape[0]:
+        raise ValueError("X_ref and Y_quant must be [n][d] with the same n")
+    out = ctypes.c_double()
+    _check(load().spear_cka_damage(x.ctypes.data_as(ctypes.c_void_p), y.ctypes.data_as(ctypes.c_void_p),
+                                   x.shape[0], x.shape[1], y.shape[1], ctypes.byref(out)), "spear_cka_damage")
+    return out.value
+
+
 def cka_damage(reference_outputs, quantised_outputs):
-    """Per-module damage scores 1 - CKA(reference, quantised) for the
-    module-selection rule; each argument a list of host [n][d] matrices."""
-    return np.array([1.0 - spear_linear_cka(a, b) for a, b in zip(reference_outputs, quantised_outputs)],
+    """Per-module damage scores for the module-selection rule (one
+    spear_cka_damage call per module); each argument a list of host [n][d]
+    matrices."""
+    return np.array([spear_cka_damage(a, b) for a, b in zip(reference_outputs, quantised_outputs)],
                     dtype=np.float32)
 
 

@@ -64,6 +64,19 @@ def test_damage_scores_select_the_damaged_modules():
     assert mask.tolist() == [0, 0, 1, 1] and set(ranks[2:].tolist()) == {32}
 
 
+def test_damage_score_is_one_minus_cka_computed_by_the_library():
+    """spear_cka_damage (C ABI) equals 1 - spear_linear_cka on the same inputs,
+    and is checked the same way."""
+    sp = _spear()
+    rng = np.random.default_rng(9)
+    X = rng.standard_normal((96, 40)).astype(np.float32)
+    Y = (X[:, :24] + 0.3 * rng.standard_normal((96, 24))).astype(np.float32)
+    assert sp.spear_cka_damage(X, Y) == 1.0 - sp.spear_linear_cka(X, Y)
+    assert sp.spear_cka_damage(X, X) == pytest.approx(0.0, abs=1e-12)
+    with pytest.raises(sp.SpearError):
+        sp.spear_cka_damage(np.ones((10, 4), np.float32), X[:10])
+
+
 def test_rejects_degenerate_inputs():
     sp = _spear()
     X = np.ones((10, 4), np.float32)

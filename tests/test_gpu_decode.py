@@ -149,3 +149,50 @@ def test_empty_batch_is_a_no_op():
     assert spear.spear_get_device_status() == 0
     with pytest.raises(spear.SpearError):
         spear.spear_linear_decode(L, to_dev_u16(make_tokens(rng, 65, 1024), torch.bfloat16))
+
+
+def test_calls_without_a_workspace_reuse_one_per_stream():
+    """Calls made without a workspace share the binding's one per (device,
+    stream): made and zeroed once on the call's stream, reused after."""
+    from quantized_gemm_error_gb300 import spear
+    lay, rng = make_layer(512, 1024, 32, seed=77)
+    L = gpu_layer(lay, 128, False)
+    ref = oracle.linear(oracle_layer(lay, 128, False), make_tokens(np.random.default_rng(1), 3, 1024), nthreads=8)
+    x = to_dev_u16(make_tokens(np.random.default_rng(1), 3, 1024), torch.bfloat16)
+    spear.reset_default_workspaces()
+    side = torch.cuda.Stream()
+    outs = []
+    for _ in range(3):
+        with torch.cuda.stream(side):
+            outs.append(spear.spear_linear_decode(L, x, out_dtype=spear.OUT_F32, stream=side))
+    torch.cuda.synchronize()
+    assert spear.spear_get_device_status() == 0
+    assert len([k for k in spear._default_ws if k[0] == "decode"]) == 1
+    for y in outs:
+        check_close(y, ref)
+    spear.reset_default_workspaces()
+    assert not spear._default_ws
+
+
+@pytest.mark.parametrize("N,K,G,sym,r,M", [
+    (512, 2048, 128, False, 32, 3),          # tokens staged in fp16 (M <= 8)
+    (1024, 1024, 1024, True, 16, 8),         # staged, per-channel scales
+    (512, 2048, 128, False, 32, 12),         # bf16 tokens from L1
+    (512, 1024, 128, False, 32, 24),         # tensor-core kernel, fp16 token tiles
+    (256, 1024, 1024, False, 32, 64),
+])
+def test_decode_activations_of_any_magnitude(N, K, G, sym, r, M):
+    """Tokens with |x| up to ~1e6 (beyond fp16): the fp16 launches scale each
+    such token by a power of two and match the oracle."""
+    from quantized_gemm_error_gb300.inputs import f32_to_bf16_bits
+    from spear_testutil import bf16_bits_to_f32
+    lay, rng = make_layer(N, K, r, seed=300 + N + M)
+    x = bf16_bits_to_f32(make_tokens(rng, M, K, outlier_frac=0.01)).reshape(M, K)
+    row_scale = np.ones(M, np.float32)
+    row_scale[0::3] = 3.0e4                                  # max |x| ~ 1e6 with the x20 outliers
+    x = x * row_scale[:, None]
+    x[min(1, M - 1), 5] = 9.5e5                              # one huge value in an ordinary token
+    x = f32_to_bf16_bits(x)
+    L = gpu_layer(lay, G, sym)
+    ref = oracle.linear(oracle_layer(lay, G, sym), x, nthreads=8)
+    check_close(_run(L, x, out_dtype=1), ref)

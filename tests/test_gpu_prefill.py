@@ -9,7 +9,9 @@ import pytest
 import torch
 
 import oracle
-from spear_testutil import check_close, gpu_layer, make_layer, make_tokens, oracle_layer, sample_columns, to_dev_u16
+from quantized_gemm_error_gb300.inputs import f32_to_bf16_bits
+from spear_testutil import (bf16_bits_to_f32, check_close, gpu_layer, make_layer, make_tokens, oracle_layer,
+                            sample_columns, to_dev_u16)
 
 pytestmark = pytest.mark.gpu
 
@@ -117,11 +119,41 @@ def test_prefill_gate_zero_equals_plain(N, K, M):
     assert torch.equal(y_on, y_off)
 
 
-def test_prefill_reports_activations_beyond_fp16_range():
+def _huge_tokens(rng, M, K):
+    """x ~ N(0, 1) with 1 % outlier channels x20, then rows scaled so some
+    tokens reach |x| ~ 1e6 (beyond fp16), some stay ordinary, one mixes a huge
+    and tiny values."""
+    x = bf16_bits_to_f32(make_tokens(rng, M, K, outlier_frac=0.01)).reshape(M, K)
+    row_scale = np.ones(M, np.float32)
+    row_scale[0::3] = 3.0e4                                  # max |x| ~ 1e6 with the x20 outliers
+    row_scale[1::7] = 1.5e3                                  # max ~ 1e5
+    x = x * row_scale[:, None]
+    x[2, 5] = 9.5e5                                          # one huge value in an ordinary token
+    return f32_to_bf16_bits(x)
+
+
+@pytest.mark.parametrize("N,K,G,sym,r,M,mode", [
+    (256, 256, 128, False, 0, 200, FUSED),                   # no compensator: the row-wise fp16 copy
+    (768, 1024, 128, False, 32, 300, FUSED),                 # 128-token tiles, correction in its own accumulator
+    (768, 1024, 128, False, 32, 300, STREAM),                # concurrent stream: the up-projection adds unscaled
+    (2560, 512, 128, False, 32, 2000, FUSED),                # 256-token tiles: the correction joins scaled accumulators
+    (1024, 1024, 1024, True, 32, 512, FUSED),                # per-channel scales, K split
+])
+def test_prefill_activations_of_any_magnitude(N, K, G, sym, r, M, mode):
+    """Tokens with |x| up to ~1e6 (beyond fp16) run on the fp16 GEMM through
+    power-of-two token scaling and match the oracle."""
+    lay, rng = make_layer(N, K, r, seed=47 + N + M)
+    x = _huge_tokens(rng, M, K)
+    L = gpu_layer(lay, G, sym)
+    ref = oracle.linear(oracle_layer(lay, G, sym), x, nthreads=8)
+    check_close(_run(L, x, mode, 1), ref)
+
+
+def test_prefill_reports_non_finite_activations():
     from quantized_gemm_error_gb300 import spear
     lay, rng = make_layer(256, 256, 0, seed=47)
     x = make_tokens(rng, 128, 256)
-    x[3, 7] = 0x4780                                        # bf16 65536: beyond the fp16 range
+    x[3, 7] = 0x7F80                                        # bf16 +inf
     L = gpu_layer(lay, 128, False)
     spear.spear_linear_prefill(L, to_dev_u16(x, torch.bfloat16), out_dtype=1)
     torch.cuda.synchronize()
