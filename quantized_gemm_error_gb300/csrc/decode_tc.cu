@@ -411,32 +411,38 @@ __device__ void tc_tile(const CUtensorMap* tm_w, const CUtensorMap* tm_x, const 
 
   if (warp == kTmaWarp) {
     // ------------------------------------------------------------- TMA
+    // The whole warp runs the loop (lane 0 tests the slots and issues, the
+    // decisions are broadcast), like the MMA warp below.
     if (lane == 0) {
       prefetch_tmap(tm_w);
       prefetch_tmap(tm_x);
       SPEAR_CHECK(&g_dtc_status, n0 < p.N && (nunits == 0 || unit_of(nunits - 1) * kUnitK < p.K));
-      int ri = 0, xi = 0;
-      // the first weight units need no slot wait and read only the layer's
-      // weights: issue them before waiting for the kernel ahead (overlapped launches)
-      for (const int pre = nunits < kRawStages ? nunits : kRawStages; ri < pre; ++ri) {
-        const uint32_t full = smem_u32(&raw_full[ri]);
+    }
+    // the first weight units need no slot wait and read only the layer's
+    // weights: issue them before waiting for the kernel ahead (overlapped launches)
+    int ri = nunits < kRawStages ? nunits : kRawStages, xi = 0;
+    if (lane == 0) {
+      for (int i = 0; i < ri; ++i) {
+        const uint32_t full = smem_u32(&raw_full[i]);
         mbar_arrive_expect_tx(full, kRawBytes);
-        tma_load_2d(smem_u32(raw_ring + ri * kRawBytes), tm_w, unit_of(ri) * (kUnitK / 2), n0, full);
+        tma_load_2d(smem_u32(raw_ring + i * kRawBytes), tm_w, unit_of(i) * (kUnitK / 2), n0, full);
       }
-      pdl_wait();
-      bool ok = true;
-      uint64_t t0 = globaltimer_ns();
-      uint32_t idle = 0;
-      while (ok && (ri < nunits || xi < nsteps)) {
-        bool prog = false;
+    }
+    __syncwarp();
+    pdl_wait();
+    bool ok = true;
+    uint64_t t0 = globaltimer_ns();
+    uint32_t idle = 0;
+    while (ok && (ri < nunits || xi < nsteps)) {
+      uint32_t prog = 0;
+      if (lane == 0) {
         if (ri < nunits) {
           const int slot = ri % kRawStages;
           if (mbar_test_wait(smem_u32(&raw_empty[slot]), ((ri / kRawStages) & 1) ^ 1)) {
             const uint32_t full = smem_u32(&raw_full[slot]);
             mbar_arrive_expect_tx(full, kRawBytes);
             tma_load_2d(smem_u32(raw_ring + slot * kRawBytes), tm_w, unit_of(ri) * (kUnitK / 2), n0, full);
-            ++ri;
-            prog = true;
+            prog |= 1u;
           }
         }
         if (xi < nsteps) {
@@ -446,53 +452,58 @@ __device__ void tc_tile(const CUtensorMap* tm_w, const CUtensorMap* tm_x, const 
             mbar_arrive_expect_tx(full, NP * 128);
             tma_load_2d(smem_u32(xr_ring + slot * NP * 128), tm_x, unit_of(xi >> 2) * kUnitK + (xi & 3) * kStepK,
                         0, full);
-            ++xi;
-            prog = true;
-          }
-        }
-        if (prog) {
-          idle = 0;
-        } else {
-          __nanosleep(64);                                 // leave the issue slots to the converters
-          if ((++idle & 63) == 0) {
-            if (idle == 64) t0 = globaltimer_ns();
-            else if (globaltimer_ns() - t0 > kPipeWaitNs || s_abort) ok = false;
+            prog |= 2u;
           }
         }
       }
-      if (!ok) {
-        give_up(&s_abort);
-        // never leave with copies in flight: wait (bounded) for every issued fill
-        for (int i = std::max(0, ri - kRawStages); i < ri; ++i)
-          mbar_wait(smem_u32(&raw_full[i % kRawStages]), (i / kRawStages) & 1, kPipeWaitNs);
-        for (int i = std::max(0, xi - kXrStages); i < xi; ++i)
-          mbar_wait(smem_u32(&xr_full[i % kXrStages]), (i / kXrStages) & 1, kPipeWaitNs);
+      prog = __shfl_sync(0xffffffffu, prog, 0);
+      ri += (int)(prog & 1u);
+      xi += (int)(prog >> 1);
+      if (prog) {
+        idle = 0;
+      } else {
+        __nanosleep(64);                                   // leave the issue slots to the converters
+        if ((++idle & 63) == 0) {
+          if (idle == 64) t0 = globaltimer_ns();
+          else if (globaltimer_ns() - t0 > kPipeWaitNs || s_abort) ok = false;
+          ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        }
       }
+    }
+    if (!ok && lane == 0) {
+      give_up(&s_abort);
+      // never leave with copies in flight: wait (bounded) for every issued fill
+      for (int i = std::max(0, ri - kRawStages); i < ri; ++i)
+        mbar_wait(smem_u32(&raw_full[i % kRawStages]), (i / kRawStages) & 1, kPipeWaitNs);
+      for (int i = std::max(0, xi - kXrStages); i < xi; ++i)
+        mbar_wait(smem_u32(&xr_full[i % kXrStages]), (i / kXrStages) & 1, kPipeWaitNs);
     }
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------- MMA
-    if (lane == 0) {
-      const uint32_t idesc = idesc_f16_f32(64, kTileRows);
-      bool ok = true;
-      for (int s = 0; s < nsteps; ++s) {
-        ok = mbar_wait(smem_u32(&bf_full[s % BF]), (s / BF) & 1, kPipeWaitNs) &&
-             mbar_wait(smem_u32(&x16_full[s % kX16Stages]), (s / kX16Stages) & 1, kPipeWaitNs) && !s_abort;
-        if (!ok) {
-          give_up(&s_abort);
-          break;
-        }
-        tc_fence_after();
-        const uint32_t a0 = smem_u32(x16_ring + (s % kX16Stages) * kX16Bytes);
-        const uint32_t b0 = smem_u32(bf_ring + (s % BF) * kBfBytes);
-#pragma unroll
-        for (int kk = 0; kk < kStepK / 16; ++kk)
-          mma_bf16_ss(tmem, smem_desc(a0 + 32 * kk, 1024, LAYOUT_SW128), smem_desc(b0 + 32 * kk, 1024, LAYOUT_SW128),
-                      idesc, (s > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(smem_u32(&bf_empty[s % BF]));
-        mma_commit(smem_u32(&x16_empty[s % kX16Stages]));
+    // The whole warp runs the loop (every lane waits, one elected lane
+    // issues): a loop on one lane while the other 31 wait at a barrier issues
+    // at about a third of the rate.
+    const uint32_t idesc = idesc_f16_f32(64, kTileRows);
+    bool ok = true;
+    for (int s = 0; s < nsteps; ++s) {
+      ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bf_full[s % BF]), (s / BF) & 1, kPipeWaitNs) &&
+                                       mbar_wait(smem_u32(&x16_full[s % kX16Stages]), (s / kX16Stages) & 1,
+                                                 kPipeWaitNs) && !s_abort);
+      if (!ok) {
+        if (lane == 0) give_up(&s_abort);
+        break;
       }
-      if (ok) mma_commit(smem_u32(&acc_full));
+      tc_fence_after();
+      const uint32_t a0 = smem_u32(x16_ring + (s % kX16Stages) * kX16Bytes);
+      const uint32_t b0 = smem_u32(bf_ring + (s % BF) * kBfBytes);
+#pragma unroll
+      for (int kk = 0; kk < kStepK / 16; ++kk)
+        mma_bf16_ss_warp(tmem, smem_desc(a0 + 32 * kk, 1024, LAYOUT_SW128),
+                         smem_desc(b0 + 32 * kk, 1024, LAYOUT_SW128), idesc, (s > 0 || kk > 0) ? 1u : 0u);
+      mma_commit_warp(smem_u32(&bf_empty[s % BF]));
+      mma_commit_warp(smem_u32(&x16_empty[s % kX16Stages]));
     }
+    if (ok) mma_commit_warp(smem_u32(&acc_full));
   } else if (warp >= kConvWarp0) {
     // -------------------------------------- weight converters (16 warps)
     const int cw = warp - kConvWarp0;
@@ -935,7 +946,12 @@ int build_tc_plan(const spear_w4_layer& L, int NP, bool comp, const DeviceInfo& 
     TcPlan c = *pl;
     c.S = S;
     const int units_per = (pl->units + S - 1) / S;      // most units one CTA takes
-    c.Kp = has_rank ? std::max(1, std::min(kMaxKp, (int)std::ceil((double)L.K / (S * 512.0)))) : 1;
+    // one producer cluster per 16-row tile of [A; w_g] (its S CTAs split K):
+    // splitting K further over Kp clusters shortens the producers' loop but
+    // takes SMs from the tile clusters, and a larger S (fewer K steps per tile
+    // CTA) pays more -- measured at 64 tokens on 4096 x 11008 and 11008 x 4096:
+    // 34.1 -> 28.5 us and 45.0 -> 35.3 us per call
+    c.Kp = 1;
     const int nr_max = (kTileRows + S - 1) / S;
     // three fp16 weight steps in flight when they fit, else two
     c.BF = kMaxBfStages;

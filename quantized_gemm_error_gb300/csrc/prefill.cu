@@ -157,14 +157,18 @@ w4_gemm_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
-    if (lane == 0) {
-      int issued = 0;
-      for (int s = 0; s < total_stages; ++s) {
-        const int slot = s % kStages;
-        if (!mbar_wait(smem_u32(&bar_empty[slot]), ((s / kStages) & 1) ^ 1, kWaitNs) || s_abort) {
-          give_up();
-          break;
-        }
+    // The whole warp runs the loop (every lane waits, lane 0 issues): a loop
+    // on one lane while the other 31 wait at a barrier runs at about a third
+    // of the rate.  The same holds for the MMA issuer below.
+    int issued = 0;
+    for (int s = 0; s < total_stages; ++s) {
+      const int slot = s % kStages;
+      if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bar_empty[slot]), ((s / kStages) & 1) ^ 1, kWaitNs) &&
+                                       !s_abort)) {
+        if (lane == 0) give_up();
+        break;
+      }
+      if (lane == 0) {
         const uint32_t full = smem_u32(&bar_full[slot]);
         if (s < nmain) {
           const int sg = kb + s;        // K step
@@ -177,17 +181,18 @@ w4_gemm_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
           tma_load_2d(smem_u32(x_slot(slot)), &tm_t, j * 64, m0, full);
           tma_load_2d(smem_u32(w_slot(slot)), &tm_b, 0, n0, full);
         }
-        ++issued;
       }
-      // never leave with copies in flight: wait (bounded) for every issued stage
-      if (s_abort) {
-        for (int s = std::max(0, issued - kStages); s < issued; ++s)
-          mbar_wait(smem_u32(&bar_full[s % kStages]), (s / kStages) & 1, kWaitNs);
-      }
+      __syncwarp();
+      ++issued;
+    }
+    // never leave with copies in flight: wait (bounded) for every issued stage
+    if (s_abort && lane == 0) {
+      for (int s = std::max(0, issued - kStages); s < issued; ++s)
+        mbar_wait(smem_u32(&bar_full[s % kStages]), (s / kStages) & 1, kWaitNs);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------- MMA issuer
-    if (lane == 0) {
+    {
       const uint32_t idesc = idesc_f16_f32(128, kBN);            // fp16 X x fp16 W (M = 128 per MMA)
       const uint32_t idesc_comp = idesc_bf16_f32(128, kBN);      // bf16 T x bf16 B
       bool ok = true;
@@ -196,7 +201,8 @@ w4_gemm_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
         const uint32_t ph = (s / kStages) & 1;
         ok = mbar_wait(smem_u32(&bar_full[slot]), ph, kWaitNs) && !s_abort;
         if (ok && s < nmain) ok = mbar_wait(smem_u32(&bar_cvt[slot]), ph, kWaitNs) && !s_abort;
-        if (!ok) { give_up(); break; }
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) { if (lane == 0) give_up(); break; }
         tc_fence_after();
         const uint32_t xa = smem_u32(x_slot(slot)), wa = smem_u32(w_slot(slot));
         if (s < nmain) {
@@ -206,7 +212,7 @@ w4_gemm_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
 #pragma unroll
             for (int mh = 0; mh < kMH; ++mh) {                 // token rows 128 mh .. (16 KB apart)
               const uint64_t ad = smem_desc(xa + mh * 16384 + 32 * k, 1024, LAYOUT_SW128);
-              mma_bf16_ss(tmem + mh * kBN, ad, bd, idesc, (s > 0 || k > 0) ? 1u : 0u);
+              mma_bf16_ss_warp(tmem + mh * kBN, ad, bd, idesc, (s > 0 || k > 0) ? 1u : 0u);
             }
           }
         } else {
@@ -223,14 +229,14 @@ w4_gemm_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
 #pragma unroll
             for (int mh = 0; mh < kMH; ++mh) {
               const uint64_t ad = smem_desc(xa + mh * 128 * p.t_row_bytes + 32 * i, 8 * p.t_row_bytes, a_layout);
-              if (kMH == 1) mma_bf16_ss(tmem + kBN, ad, bd, idesc_comp, (j > 0 || i > 0) ? 1u : 0u);
-              else mma_bf16_ss(tmem + mh * kBN, ad, bd, idesc_comp, 1u);
+              if (kMH == 1) mma_bf16_ss_warp(tmem + kBN, ad, bd, idesc_comp, (j > 0 || i > 0) ? 1u : 0u);
+              else mma_bf16_ss_warp(tmem + mh * kBN, ad, bd, idesc_comp, 1u);
             }
           }
         }
-        mma_commit(smem_u32(&bar_empty[slot]));             // frees the stage when these MMAs finish
+        mma_commit_warp(smem_u32(&bar_empty[slot]));        // frees the stage when these MMAs finish
       }
-      mma_commit(smem_u32(&bar_acc));                        // accumulators complete
+      mma_commit_warp(smem_u32(&bar_acc));                   // accumulators complete
     }
   } else {
     // ------------------------------------------ converters, then the epilogue
