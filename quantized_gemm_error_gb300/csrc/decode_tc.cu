@@ -12,9 +12,10 @@
 // thread-block cluster of S CTAs (one per SM) that split its K range in
 // 256-k units (rank j takes units j, j + S, ...), so a tile's partial sums
 // meet in distributed shared memory and never touch HBM.  Before the tile
-// clusters come RT x Kp small "producer" clusters that compute
-// P = [A; w_g] x (rank r + 1 rows) over K slices with mma.sync and publish it
-// through the workspace; the tile CTAs read it only in their epilogue.
+// clusters come RT small "producer" clusters, one per 16-row tile of
+// [A; w_g], that compute P = [A; w_g] x (rank r + 1 rows) over K slices with
+// mma.sync and publish it through the workspace; the tile CTAs read it only in
+// their epilogue.
 //
 // Tile CTA (704 threads):
 //   warp 20   TMA: raw int4 units (256 rows x 128 bytes, 128-byte swizzle) and
@@ -73,7 +74,6 @@ constexpr int kConvWarp0 = 4, kConvWarps = 16;  // warps 4-19: weight conversion
 constexpr int kTmaWarp = 20, kMmaWarp = 21;
 constexpr int kThreads = 704;
 constexpr int kMaxS = 8;
-constexpr int kMaxKp = 8;                        // K ranges of the producer clusters
 constexpr uint64_t kPipeWaitNs = 2000ull * 1000 * 1000;   // 2 s: far beyond any legitimate wait
 constexpr uint64_t kTWaitNs = 200ull * 1000 * 1000;       // 200 ms for the published P
 
@@ -81,7 +81,7 @@ struct TcParams {
   int N, K, M, ng, sym;
   const uint8_t* qweight;
   int S;                    // CTAs per cluster
-  int RT, Kp;               // producer clusters: RT row tiles x Kp K ranges (RT = 0: none)
+  int RT;                   // producer clusters, one per 16-row tile of [A; w_g] (0: none)
   int units;                // 256-k units of K
   int bf_stages;             // fp16 weight steps in flight (2 or 3)
   int r;                    // rank (0 when the compensator is off)
@@ -97,9 +97,8 @@ struct TcParams {
   float b_g, alpha;
   int gh;                   // vector-gate hidden width (0: the scalar gate)
   const float *gw1, *gc1, *gw2, *gc2;
-  float* ws_part;           // [Kp][RT][16][NP] producer-cluster partials
   float* ws_P;              // [NP][r + 1]: (A x)[j] for j < r, w_g . x at j = r
-  unsigned* ws_sync;        // [0] producer row tiles published, [1] tile-CTA ticket, [2 + rt] Kp tickets
+  unsigned* ws_sync;        // [0] producer row tiles published, [1] tile-CTA ticket
   uint32_t off_bf, off_x16, off_xr, off_B, off_gate;   // dynamic shared memory layout
   uint64_t t_wait_ns;       // limit of the wait for the published P
 };
@@ -110,21 +109,19 @@ __device__ __forceinline__ void give_up(int* abort_flag) {
 }
 
 // ------------------------------------------------------------- producers --
-// Producer cluster pc = (row tile rt, K range kp): CTA `rank` of it covers K
-// slice kp * S + rank of Kp * S (128-k chunks).  Lane (g, c) of a warp loads
+// Producer cluster rt (a 16-row tile of [A; w_g]): CTA `rank` of it covers K
+// slice `rank` of S (128-k chunks).  Lane (g, c) of a warp loads
 // 8 consecutive k of a projection row and of a token; both operands use the
 // same k permutation, so the mma.sync sums are the plain dot products.
 template <int NP>
-__device__ void tc_producer(const TcParams& p, uint8_t* smem, int pc, int rank) {
+__device__ void tc_producer(const TcParams& p, uint8_t* smem, int rt, int rank) {
   constexpr int MT = NP / 8;
   constexpr int NW = kThreads / 32;
   constexpr int U = MT <= 2 ? 2 : 1;                       // 32-k pieces per pass
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, c = lane & 3;
-  const int rt = pc % p.RT, kp = pc / p.RT;
-  const int nsl = p.Kp * p.S, sl = kp * p.S + rank;
   const int nch = p.K / 128;
-  const int c0 = (int)((long long)sl * nch / nsl), c1 = (int)((long long)(sl + 1) * nch / nsl);
+  const int c0 = (int)((long long)rank * nch / p.S), c1 = (int)((long long)(rank + 1) * nch / p.S);
   const int npieces = (c1 - c0) * 4;
   float* red = reinterpret_cast<float*>(smem);             // [NW][MT][4][32]
   float* part = red + NW * MT * 128;                        // [16][NP]
@@ -194,55 +191,27 @@ __device__ void tc_producer(const TcParams& p, uint8_t* smem, int pc, int rank) 
   __syncthreads();
   cluster_sync();                                          // every CTA's partial is in its shared memory
 
-  __shared__ unsigned s_last;
   if (rank == 0) {
-    // sum the S partials in rank order
-    float* dst = p.Kp == 1 ? nullptr : p.ws_part + ((size_t)kp * p.RT + rt) * 16 * NP;
-    SPEAR_CHECK(&g_dtc_status, kp < p.Kp && rt < p.RT && p.S <= kMaxS && p.Kp <= kMaxKp);
+    // the S partials in rank order (every load in flight, then the sum), then
+    // row tile rt of P is published
+    SPEAR_CHECK(&g_dtc_status, rt < p.RT && p.S <= kMaxS);
     for (int e = threadIdx.x; e < 16 * NP; e += kThreads) {
       const uint32_t la = smem_u32(part + e);
       float pv[kMaxS];
 #pragma unroll
-      for (int q = 0; q < kMaxS; ++q)                        // every load in flight, then the sum
+      for (int q = 0; q < kMaxS; ++q)
         if (q < p.S) pv[q] = dsmem_ld_f32(dsmem_addr(la, (uint32_t)q));
       float v = 0.0f;
 #pragma unroll
       for (int q = 0; q < kMaxS; ++q)
         if (q < p.S) v += pv[q];
-      if (dst) {
-        dst[e] = v;
-      } else {
-        const int row = e / NP, tok = e % NP, i = rt * 16 + row;
-        if (i <= p.r) p.ws_P[(size_t)tok * (p.r + 1) + i] = v;
-      }
+      const int row = e / NP, tok = e % NP, i = rt * 16 + row;
+      if (i <= p.r) p.ws_P[(size_t)tok * (p.r + 1) + i] = v;
     }
     __syncthreads();
     if (threadIdx.x == 0) {
       __threadfence();
-      s_last = (p.Kp == 1) ? 1u : (atomicAdd(&p.ws_sync[2 + rt], 1u) == (unsigned)(p.Kp - 1));
-    }
-    __syncthreads();
-    if (s_last && p.Kp > 1) {
-      // the last of the Kp clusters of this row tile sums them in K order
-      __threadfence();
-      for (int e = threadIdx.x; e < 16 * NP; e += kThreads) {
-        float pv[kMaxKp];
-#pragma unroll
-        for (int q = 0; q < kMaxKp; ++q)
-          if (q < p.Kp) pv[q] = __ldcg(p.ws_part + ((size_t)q * p.RT + rt) * 16 * NP + e);
-        float v = 0.0f;
-#pragma unroll
-        for (int q = 0; q < kMaxKp; ++q)
-          if (q < p.Kp) v += pv[q];
-        const int row = e / NP, tok = e % NP, i = rt * 16 + row;
-        if (i <= p.r) p.ws_P[(size_t)tok * (p.r + 1) + i] = v;
-      }
-      __syncthreads();
-    }
-    if (s_last && threadIdx.x == 0) {
-      if (p.Kp > 1) p.ws_sync[2 + rt] = 0;                 // ticket ready for the next call
-      __threadfence();
-      atomicAdd(&p.ws_sync[0], 1u);                        // row tile rt of P is published
+      atomicAdd(&p.ws_sync[0], 1u);
     }
   }
   cluster_sync();                                          // peers keep their shared memory until read
@@ -866,7 +835,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
   pdl_launch_dependents();                                 // every CTA is resident: let the next kernel queue
   const int rank = (int)cluster_ctarank();
   const int cid = (int)blockIdx.x / p.S;
-  const int npc = p.RT * p.Kp;
+  const int npc = p.RT;
   if (cid < npc) {
     // producer clusters; with the compensator off they idle (the tile split
     // stays the one of the compensated layer, so a zero gate reproduces the
@@ -898,10 +867,10 @@ int np_for(int M) { return M <= 16 ? 16 : M <= 32 ? 32 : 64; }
 // ---------------------------------------------------------------- plan --
 struct TcPlan {
   int device, N, K, G, rank, comp, NP, gh;     // key
-  int S, RT, Kp, tiles, units, BF;
+  int S, RT, tiles, units, BF;
   size_t smem;
   uint32_t off_bf, off_x16, off_xr, off_B, off_gate;
-  size_t off_sync, off_part, off_P, total;
+  size_t off_sync, off_P, total;
   TcKernel fn;
 };
 
@@ -946,12 +915,11 @@ int build_tc_plan(const spear_w4_layer& L, int NP, bool comp, const DeviceInfo& 
     TcPlan c = *pl;
     c.S = S;
     const int units_per = (pl->units + S - 1) / S;      // most units one CTA takes
-    // one producer cluster per 16-row tile of [A; w_g] (its S CTAs split K):
-    // splitting K further over Kp clusters shortens the producers' loop but
-    // takes SMs from the tile clusters, and a larger S (fewer K steps per tile
-    // CTA) pays more -- measured at 64 tokens on 4096 x 11008 and 11008 x 4096:
-    // 34.1 -> 28.5 us and 45.0 -> 35.3 us per call
-    c.Kp = 1;
+    // one producer cluster per 16-row tile of [A; w_g], its S CTAs splitting
+    // K: splitting K further over more clusters shortens the producers' loop
+    // but takes SMs from the tile clusters, and a larger S (fewer K steps per
+    // tile CTA) pays more -- measured at 64 tokens on 4096 x 11008 and
+    // 11008 x 4096: 34.1 -> 28.5 us and 45.0 -> 35.3 us per call
     const int nr_max = (kTileRows + S - 1) / S;
     // three fp16 weight steps in flight when they fit, else two
     c.BF = kMaxBfStages;
@@ -968,7 +936,7 @@ int build_tc_plan(const spear_w4_layer& L, int NP, bool comp, const DeviceInfo& 
     if (cudaFuncSetAttribute(c.fn, cudaFuncAttributePreferredSharedMemoryCarveout,
                              (int)cudaSharedmemCarveoutMaxShared) != cudaSuccess)
       return fail(SPEAR_ERR_CUDA, "decode: cudaFuncSetAttribute failed");
-    const int clusters = pl->tiles + c.RT * c.Kp;
+    const int clusters = pl->tiles + c.RT;
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(clusters * S);
     cfg.blockDim = dim3(kThreads);
@@ -1009,8 +977,7 @@ int build_tc_plan(const spear_w4_layer& L, int NP, bool comp, const DeviceInfo& 
   *pl = best;
 
   size_t off = 0;
-  pl->off_sync = off; off = align_up(off + (2 + 8) * sizeof(unsigned), 256);
-  pl->off_part = off; off = align_up(off + (has_rank ? (size_t)pl->Kp * pl->RT * 16 * NP * 4 : 4), 256);
+  pl->off_sync = off; off = align_up(off + 2 * sizeof(unsigned), 256);
   pl->off_P = off;    off = align_up(off + (size_t)NP * (std::max(L.rank, 1) + 1) * 4, 256);
   pl->total = off;
   return SPEAR_OK;
@@ -1034,9 +1001,9 @@ int get_tc_plan(const spear_w4_layer& L, int M, TcPlan* out) {
   TcPlan p{};
   if (int rc = build_tc_plan(L, NP, comp != 0, di, &p)) return rc;
   if (log_plans())
-    fprintf(stderr, "[spear] decode tc plan N=%d K=%d G=%d rank=%d comp=%d NP=%d: S=%d RT=%d Kp=%d tiles=%d "
-            "units=%d BF=%d smem=%zu grid=%d\n", L.N, L.K, L.group_size, L.rank, comp, NP, p.S, p.RT, p.Kp,
-            p.tiles, p.units, p.BF, p.smem, (p.tiles + p.RT * p.Kp) * p.S);
+    fprintf(stderr, "[spear] decode tc plan N=%d K=%d G=%d rank=%d comp=%d NP=%d: S=%d RT=%d tiles=%d "
+            "units=%d BF=%d smem=%zu grid=%d\n", L.N, L.K, L.group_size, L.rank, comp, NP, p.S, p.RT,
+            p.tiles, p.units, p.BF, p.smem, (p.tiles + p.RT) * p.S);
   p.device = di.device; p.N = L.N; p.K = L.K; p.G = L.group_size; p.rank = L.rank; p.comp = comp; p.gh = gh;
   if (cache.size() > 4096) cache.clear();
   cache.push_back(p);
@@ -1071,7 +1038,7 @@ int launch_decode_tc(const spear_w4_layer& L, const uint16_t* x, int M, void* y,
   TcParams p{};
   p.N = L.N; p.K = L.K; p.M = M; p.ng = L.K / L.group_size; p.sym = L.symmetric;
   p.qweight = L.qweight;
-  p.S = pl.S; p.RT = pl.RT; p.Kp = pl.Kp; p.units = pl.units; p.bf_stages = pl.BF;
+  p.S = pl.S; p.RT = pl.RT; p.units = pl.units; p.bf_stages = pl.BF;
   p.r = pl.comp ? L.rank : 0;
   p.n_consumers = pl.tiles * pl.S;
   p.scales = reinterpret_cast<const __half*>(L.scales);
@@ -1085,14 +1052,13 @@ int launch_decode_tc(const spear_w4_layer& L, const uint16_t* x, int M, void* y,
   p.gh = L.gate_hidden; p.gw1 = L.gate_w1; p.gc1 = L.gate_c1; p.gw2 = L.gate_w2; p.gc2 = L.gate_c2;
   char* base = reinterpret_cast<char*>(ws);
   p.ws_sync = reinterpret_cast<unsigned*>(base + pl.off_sync);
-  p.ws_part = reinterpret_cast<float*>(base + pl.off_part);
   p.ws_P = reinterpret_cast<float*>(base + pl.off_P);
   p.t_wait_ns = wait_limit_ns(kTWaitNs);
   p.off_bf = pl.off_bf; p.off_x16 = pl.off_x16; p.off_xr = pl.off_xr; p.off_B = pl.off_B; p.off_gate = pl.off_gate;
 
   if (int rc = ensure_smem_limit(reinterpret_cast<const void*>(pl.fn), pl.smem)) return rc;
   cudaLaunchConfig_t cfg{};
-  cfg.gridDim = dim3((pl.tiles + pl.RT * pl.Kp) * pl.S);
+  cfg.gridDim = dim3((pl.tiles + pl.RT) * pl.S);
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = pl.smem;
   cfg.stream = st;
