@@ -669,15 +669,16 @@ __device__ void tc_tile(const CUtensorMap* tm_w, const CUtensorMap* tm_x, const 
         // vector gate: t = P [NP][r] into the token ring now; gamma(t) and T
         // (over the same bytes) are formed by warps 0-19 once the accumulator
         // is drained
-        for (int e0 = 0; e0 < NP * p.r; e0 += kPer * kXWarps * 32) {
-          float v[kPer];
+        constexpr int kPerV = 16;                          // (64 tokens x rank 32: one pass)
+        for (int e0 = 0; e0 < NP * p.r; e0 += kPerV * kXWarps * 32) {
+          float v[kPerV];
 #pragma unroll
-          for (int i = 0; i < kPer; ++i) {
+          for (int i = 0; i < kPerV; ++i) {
             const int e = e0 + tid + i * kXWarps * 32;
             v[i] = (pok && e < NP * p.r) ? __ldcg(p.ws_P + (size_t)(e / p.r) * rp + e % p.r) : 0.0f;
           }
 #pragma unroll
-          for (int i = 0; i < kPer; ++i) {
+          for (int i = 0; i < kPerV; ++i) {
             const int e = e0 + tid + i * kXWarps * 32;
             if (e < NP * p.r) ts[e] = v[i];
           }
