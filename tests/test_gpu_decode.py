@@ -180,6 +180,7 @@ def test_calls_without_a_workspace_reuse_one_per_stream():
     (512, 2048, 128, False, 32, 12),         # bf16 tokens from L1
     (512, 1024, 128, False, 32, 24),         # tensor-core kernel, fp16 token tiles
     (256, 1024, 1024, False, 32, 64),
+    (512, 2048, 2048, True, 32, 40),         # tensor-core kernel, per-channel scales (the scale after the sum)
 ])
 def test_decode_activations_of_any_magnitude(N, K, G, sym, r, M):
     """Tokens with |x| up to ~1e6 (beyond fp16): the fp16 launches scale each
@@ -196,3 +197,19 @@ def test_decode_activations_of_any_magnitude(N, K, G, sym, r, M):
     L = gpu_layer(lay, G, sym)
     ref = oracle.linear(oracle_layer(lay, G, sym), x, nthreads=8)
     check_close(_run(L, x, out_dtype=1), ref)
+
+
+@pytest.mark.parametrize("M", [3, 40])
+def test_decode_reports_non_finite_activations(M):
+    """A bf16 inf among the tokens is reported as SPEAR_ERR_INVALID_ARG on the
+    launches that carry the tokens in fp16 (staged tokens, the tensor-core
+    kernel); the output of that token is not defined."""
+    from quantized_gemm_error_gb300 import spear
+    lay, rng = make_layer(512, 2048, 32, seed=48 + M)
+    x = make_tokens(rng, M, 2048, outlier_frac=0.01)
+    x[min(1, M - 1), 300] = 0x7F80                          # bf16 +inf
+    L = gpu_layer(lay, 128, False)
+    spear.spear_linear_decode(L, to_dev_u16(x, torch.bfloat16), out_dtype=1)
+    torch.cuda.synchronize()
+    assert spear.STATUS_NAMES[spear.spear_get_device_status()] == "SPEAR_ERR_INVALID_ARG"
+    assert spear.spear_get_device_status() == 0

@@ -79,3 +79,29 @@ def test_vector_gate_hidden_width_is_checked():
     with pytest.raises(spear.SpearError):
         spear.spear_linear_decode(dataclasses.replace(L, **big), to_dev_u16(make_tokens(rng, 1, 512),
                                                                               torch.bfloat16))
+
+
+@pytest.mark.parametrize("M,path", [(5, "decode"), (40, "decode"), (300, "prefill")])
+def test_vector_gate_activations_of_any_magnitude(M, path):
+    """Tokens up to ~1e6 (beyond fp16) with the vector gate: the gate's
+    down-projection runs on the bf16 tokens, the main term through the fp16
+    launches' scaling (staged tokens, the tensor-core kernel's fp32 path for
+    overflowed tokens, prefill's power-of-two token scaling)."""
+    from quantized_gemm_error_gb300 import spear
+    from quantized_gemm_error_gb300.inputs import f32_to_bf16_bits
+    from spear_testutil import bf16_bits_to_f32
+    N, K = 512, 1024
+    L, OL, g, rng = _layers(N, K, 128, False, 32, 8, seed=500 + M)
+    x = bf16_bits_to_f32(make_tokens(rng, M, K, outlier_frac=0.01)).reshape(M, K)
+    row_scale = np.ones(M, np.float32)
+    row_scale[0::3] = 3.0e4
+    x = f32_to_bf16_bits(x * row_scale[:, None])
+    ref, _ = oracle.linear_vector_gate(OL, x, *g, nthreads=8)
+    xd = to_dev_u16(x, torch.bfloat16)
+    if path == "decode":
+        y = spear.spear_linear_decode(L, xd, out_dtype=1)
+    else:
+        y = spear.spear_linear_prefill(L, xd, out_dtype=1, mode=spear.PREFILL_FUSED)
+    torch.cuda.synchronize()
+    assert spear.spear_get_device_status() == 0
+    check_close(y, ref)
