@@ -254,6 +254,15 @@ def cpu_baseline(row_fraction: float = 1.0):
                       f"(seeded), fp64 accumulation, {secs:.1f} s"}
 
 
+def decode_workload_config() -> dict:
+    """The decode workload's keys both arms report: the layers, token counts,
+    quantisation format, rank and the algorithmic bytes of one step."""
+    return {"workload": "llama7b_decode_g128_r32", "shapes_KxN": [list(s) for s in DECODE_SHAPES],
+            "M": DECODE_M, "group_size": G, "symmetric": SYM, "rank": RANK,
+            "calls_per_step": len(DECODE_SHAPES) * len(DECODE_M),
+            "bytes_per_step": sum(decode_bytes(K, N, M) for (K, N) in DECODE_SHAPES for M in DECODE_M)}
+
+
 # ------------------------------------------------------------ reference arm
 
 def run_reference(args, world, rank):
@@ -291,7 +300,7 @@ def run_reference(args, world, rank):
         "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_s / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": {"workload": "llama7b_decode_g128_r32"},
+        "data": "synthetic", "config": dict(decode_workload_config(), parallelism="rank 0 on the host cores"),
         "cpu_baseline": {"value": value, "unit": "GB/s", "cores": nthreads, "host_cpus": os.cpu_count(),
                          "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -560,9 +569,7 @@ def run_ours(args, world, rank, local):
             "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": t_max / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic",
-            "config": {"workload": "llama7b_decode_g128_r32", "shapes_KxN": [list(s) for s in DECODE_SHAPES],
-                       "M": DECODE_M, "group_size": G, "symmetric": SYM, "rank": RANK,
-                       "calls_per_step": len(calls), "bytes_per_step": step_bytes,
+            "config": {**decode_workload_config(),
                        "l2": f"every call of a step reads its own weight copy; each layer rotates through "
                              f"{ncopy} copies ({ncopy * set_bytes / 1e6:.0f} MB of weights in all; the smallest "
                              f"layer's copies alone >= 4x L2 {l2_bytes / 1e6:.0f} MB), per-call timings likewise",
