@@ -97,7 +97,7 @@ struct TcParams {
   float b_g, alpha;
   int gh;                   // vector-gate hidden width (0: the scalar gate)
   const float *gw1, *gc1, *gw2, *gc2;
-  float* ws_P;              // [NP][r + 1]: (A x)[j] for j < r, w_g . x at j = r
+  float* ws_P;              // [NP][r + 4]: (A x)[j] for j < r, w_g . x at j = r (16-byte rows)
   unsigned* ws_sync;        // [0] producer row tiles published, [1] tile-CTA ticket
   uint32_t off_bf, off_x16, off_xr, off_B, off_gate;   // dynamic shared memory layout
   uint64_t t_wait_ns;       // limit of the wait for the published P
@@ -206,7 +206,7 @@ __device__ void tc_producer(const TcParams& p, uint8_t* smem, int rt, int rank) 
       for (int q = 0; q < kMaxS; ++q)
         if (q < p.S) v += pv[q];
       const int row = e / NP, tok = e % NP, i = rt * 16 + row;
-      if (i <= p.r) p.ws_P[(size_t)tok * (p.r + 1) + i] = v;
+      if (i <= p.r) p.ws_P[(size_t)tok * (p.r + 4) + i] = v;
     }
     __syncthreads();
     if (threadIdx.x == 0) {
@@ -659,59 +659,52 @@ __device__ void tc_tile(const CUtensorMap* tm_w, const CUtensorMap* tm_x, const 
         ticket = atomicAdd(&p.ws_sync[1], 1u);
       }
       named_sync(1, kXWarps * 32);
-      // one round trip: every thread loads its pairs of P and, for the token of
-      // each pair, the gate row, all in flight together; the gate is formed
-      // per pair (the same value for every pair of a token)
-      const int rp = p.r + 1, half_r = p.r / 2;
+      // one round trip: every thread loads its (token, 4-component) pieces of
+      // P as 16-byte loads (the rows are r + 4 floats), and for the scalar
+      // gate the token's gate logit, all in flight together; no load is
+      // conditional (indexes past the end re-read the last piece) and no
+      // index needs a division
       const bool pok = s_pok != 0;
-      constexpr int kPer = 8;                              // pairs per thread and pass (r <= 32: one pass)
-      if (p.gh > 0) {
-        // vector gate: t = P [NP][r] into the token ring now; gamma(t) and T
-        // (over the same bytes) are formed by warps 0-19 once the accumulator
-        // is drained
-        constexpr int kPerV = 16;                          // (64 tokens x rank 32: one pass)
-        for (int e0 = 0; e0 < NP * p.r; e0 += kPerV * kXWarps * 32) {
-          float v[kPerV];
+      const int ps = p.r + 4, r4 = p.r >> 2, lr4 = __ffs(r4) - 1;   // r4 = 4, 8 or 16
+      const int nq = NP << lr4;                             // (token, piece) items
+      constexpr int kPerQ = 4;                             // pieces per thread and pass
+      for (int e0 = 0; e0 < nq; e0 += kPerQ * kXWarps * 32) {
+        float4 v[kPerQ];
+        float gl[kPerQ];
 #pragma unroll
-          for (int i = 0; i < kPerV; ++i) {
-            const int e = e0 + tid + i * kXWarps * 32;
-            v[i] = (pok && e < NP * p.r) ? __ldcg(p.ws_P + (size_t)(e / p.r) * rp + e % p.r) : 0.0f;
-          }
-#pragma unroll
-          for (int i = 0; i < kPerV; ++i) {
-            const int e = e0 + tid + i * kXWarps * 32;
-            if (e < NP * p.r) ts[e] = v[i];
-          }
-        }
-        cp_async_wait<0>();                      // the staged gate weights (published by the epilogue's barrier)
-      }
-      for (int e0 = 0; p.gh == 0 && e0 < NP * half_r; e0 += kPer * kXWarps * 32) {
-        float pa[kPer], pb[kPer], pg[kPer];
-#pragma unroll
-        for (int i = 0; i < kPer; ++i) {
-          const int e = e0 + tid + i * kXWarps * 32;
-          pa[i] = pb[i] = pg[i] = 0.0f;
-          if (pok && e < NP * half_r) {
-            const int t = e / half_r, jj = 2 * (e % half_r);
-            const float* row = p.ws_P + (size_t)t * rp;
-            pa[i] = __ldcg(row + jj);
-            pb[i] = __ldcg(row + jj + 1);
-            pg[i] = __ldcg(row + p.r);
-          }
+        for (int i = 0; i < kPerQ; ++i) {
+          const int e = min(e0 + tid + i * kXWarps * 32, nq - 1);
+          const float* row = p.ws_P + (size_t)(e >> lr4) * ps;
+          v[i] = __ldcg(reinterpret_cast<const float4*>(row) + (e & (r4 - 1)));
+          gl[i] = p.gh == 0 ? __ldcg(row + p.r) : 0.0f;
         }
 #pragma unroll
-        for (int i = 0; i < kPer; ++i) {
+        for (int i = 0; i < kPerQ; ++i) {
           const int e = e0 + tid + i * kXWarps * 32;
-          if (e < NP * half_r) {
-            const int t = e / half_r;
-            const float gt = (pok && t < p.M) ? p.alpha / (1.0f + expf(-(pg[i] + p.b_g))) : 0.0f;
-            const float ta = gt * pa[i], tb = gt * pb[i];
-            const float ha = __bfloat162float(__float2bfloat16_rn(ta)), hb = __bfloat162float(__float2bfloat16_rn(tb));
-            thl_s[e] = make_uint2(pack_bf16x2(ha, hb), pack_bf16x2(ta - ha, tb - hb));
+          if (e >= nq) break;
+          if (!pok) v[i] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);      // P never arrived
+          if (p.gh > 0) {
+            // vector gate: t = P [NP][r] into the token ring now; gamma(t) and
+            // T (over the same bytes) are formed by warps 0-19 once the
+            // accumulator is drained
+            reinterpret_cast<float4*>(ts)[e] = v[i];
+          } else {
+            // T = alpha g P for four components, as two hi/lo pairs: the
+            // 16 bytes of elements (m, 2q) and (m, 2q + 1) of thl_s
+            const float gt = (pok && (e >> lr4) < p.M) ? p.alpha / (1.0f + expf(-(gl[i] + p.b_g))) : 0.0f;
+            const float t0 = gt * v[i].x, t1 = gt * v[i].y, t2 = gt * v[i].z, t3 = gt * v[i].w;
+            const float h0 = __bfloat162float(__float2bfloat16_rn(t0)), h1 = __bfloat162float(__float2bfloat16_rn(t1));
+            const float h2 = __bfloat162float(__float2bfloat16_rn(t2)), h3 = __bfloat162float(__float2bfloat16_rn(t3));
+            reinterpret_cast<uint4*>(thl_s)[e] = make_uint4(pack_bf16x2(h0, h1), pack_bf16x2(t0 - h0, t1 - h1),
+                                                            pack_bf16x2(h2, h3), pack_bf16x2(t2 - h2, t3 - h3));
           }
         }
       }
+      if (p.gh > 0) cp_async_wait<0>();                   // the staged gate weights (published by the barrier below)
       named_sync(1, kXWarps * 32);
+      // vector gate: its hidden units from t here, while the last MMAs and the
+      // drain run (gamma and T follow the drain on all warps)
+      if (p.gh > 0) vector_gate_hidden_rows(ts, NP, GateSmem(gate_s, p.r, p.gh), hs, tid, kXWarps * 32);
     }
   }
 
@@ -723,24 +716,40 @@ __device__ void tc_tile(const CUtensorMap* tm_w, const CUtensorMap* tm_x, const 
     // TMA and MMA warps never reach this barrier.
     named_sync(2, kTmaWarp * 32);                          // drained partial, T (or t) and B rows in place
     if (p.gh > 0) {
-      // vector gate over warps 0-19: T = alpha gamma(t) t, each pair of t
-      // turned into its hi/lo pair in place (uniform branch: every barrier
-      // below is reached by all 640 threads)
+      // vector gate over warps 0-19 (the token warps formed the hidden units):
+      // T = alpha gamma(t) t, each pair of t turned into its hi/lo pair in
+      // place (uniform branch: the barrier below is reached by all 640 threads)
       constexpr int kEpi = kTmaWarp * 32;
       const GateSmem gt(gate_s, p.r, p.gh);
-      vector_gate_hidden_rows(ts, NP, gt, hs, threadIdx.x, kEpi);
-      named_sync(2, kEpi);
-      vector_gate_apply_rows(ts, NP, gt, hs, threadIdx.x, kEpi);
-      named_sync(2, kEpi);
-      const int half_r = p.r / 2;
+      // gamma for four rank components of one token per thread, and T = alpha
+      // gamma t for them turned into two hi/lo pairs over the same 16 bytes
       const bool pok = s_pok != 0;
-      for (int e = threadIdx.x; e < NP * half_r; e += kEpi) {
-        const int m = e / half_r;
+      const int r4 = p.r / 4, hstr = gate_hid_stride(p.gh);
+      for (int e = threadIdx.x; e < NP * r4; e += kEpi) {
+        const int m = e / r4, q = e % r4;
+        float4 a = reinterpret_cast<const float4*>(gt.c2)[q];
+        const float* hh = hs + m * hstr;
+#pragma unroll 4
+        for (int i = 0; i < p.gh; ++i) {
+          const float4 wv = reinterpret_cast<const float4*>(gt.W2t + i * p.r)[q];
+          const float hv = hh[i];
+          a.x = fmaf(wv.x, hv, a.x);
+          a.y = fmaf(wv.y, hv, a.y);
+          a.z = fmaf(wv.z, hv, a.z);
+          a.w = fmaf(wv.w, hv, a.w);
+        }
         const bool on = pok && m < p.M;
-        const float2 tv = reinterpret_cast<const float2*>(ts)[e];     // t[m][2jj], t[m][2jj + 1]
-        const float ta = on ? p.alpha * tv.x : 0.0f, tb = on ? p.alpha * tv.y : 0.0f;
-        const float ha = __bfloat162float(__float2bfloat16_rn(ta)), hb = __bfloat162float(__float2bfloat16_rn(tb));
-        thl_s[e] = make_uint2(pack_bf16x2(ha, hb), pack_bf16x2(ta - ha, tb - hb));
+        float4* tp = reinterpret_cast<float4*>(ts + m * p.r) + q;
+        const float4 tv = *tp;
+        const float t0 = on ? p.alpha * tv.x / (1.0f + expf(-a.x)) : 0.0f;
+        const float t1 = on ? p.alpha * tv.y / (1.0f + expf(-a.y)) : 0.0f;
+        const float t2 = on ? p.alpha * tv.z / (1.0f + expf(-a.z)) : 0.0f;
+        const float t3 = on ? p.alpha * tv.w / (1.0f + expf(-a.w)) : 0.0f;
+        const float h0 = __bfloat162float(__float2bfloat16_rn(t0)), h1 = __bfloat162float(__float2bfloat16_rn(t1));
+        const float h2 = __bfloat162float(__float2bfloat16_rn(t2)), h3 = __bfloat162float(__float2bfloat16_rn(t3));
+        // pairs (m, 2q) and (m, 2q + 1) of T hi/lo: the 16 bytes read above
+        *reinterpret_cast<uint4*>(tp) = make_uint4(pack_bf16x2(h0, h1), pack_bf16x2(t0 - h0, t1 - h1),
+                                                   pack_bf16x2(h2, h3), pack_bf16x2(t2 - h2, t3 - h3));
       }
       named_sync(2, kEpi);
     }
@@ -979,7 +988,7 @@ int build_tc_plan(const spear_w4_layer& L, int NP, bool comp, const DeviceInfo& 
 
   size_t off = 0;
   pl->off_sync = off; off = align_up(off + 2 * sizeof(unsigned), 256);
-  pl->off_P = off;    off = align_up(off + (size_t)NP * (std::max(L.rank, 1) + 1) * 4, 256);
+  pl->off_P = off;    off = align_up(off + (size_t)NP * (std::max(L.rank, 1) + 4) * 4, 256);
   pl->total = off;
   return SPEAR_OK;
 }
