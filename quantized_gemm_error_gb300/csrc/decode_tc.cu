@@ -14,8 +14,9 @@
 // meet in distributed shared memory and never touch HBM.  Before the tile
 // clusters come RT small "producer" clusters, one per 16-row tile of
 // [A; w_g], that compute P = [A; w_g] x (rank r + 1 rows) over K slices with
-// mma.sync and publish it through the workspace; the tile CTAs read it only in
-// their epilogue.
+// mma.sync and publish it through the workspace; the last of them to publish
+// forms T from P (either gate) and publishes it too, and the tile CTAs read
+// T only in their epilogue.
 //
 // Tile CTA (704 threads):
 //   warp 20   TMA: raw int4 units (256 rows x 128 bytes, 128-byte swizzle) and
@@ -27,15 +28,15 @@
 //             drain the accumulator into this CTA's partial in shared memory;
 //   warps 0-3 convert the token tile to fp16 (exact for |x| < 65504) and
 //             flag the tokens holding a larger value, then read the published
-//             P and form T (scalar gate) or load t = A x (vector gate) in the
-//             spent ring; after the drain the converter warps recompute a
-//             flagged token's partial in fp32 (tc_exact_rows);
+//             T hi/lo that the last producer CTA formed (tc_form_T: either
+//             gate) into the spent ring; after the drain the converter warps
+//             recompute a flagged token's partial in fp32 (tc_exact_rows);
 //   warp 21   one thread issues tcgen05.mma with the tokens as the 64-row A
 //             operand and the weights as the 256-column B operand:
 //             D[64 x 256] (+)= X[64 x 16] W[256 x 16]^T, fp32 in tensor memory.
-// Epilogue: warps 0-19 run the vector gate's MLP (if any) and add B T into the
-// partial rows this CTA finishes; then the S partials of the cluster are
-// summed in a fixed order through DSMEM, each CTA finishing 256 / S rows of y.
+// Epilogue: warps 0-19 add B T into the partial rows this CTA finishes; then
+// the S partials of the cluster are summed in a fixed order through DSMEM,
+// each CTA finishing 256 / S rows of y.
 //
 // Shared memory carries every weight several times (int4 in, fp16 out, fp16
 // read by the tensor core: ~10 bytes per int4 byte), which bounds this kernel
@@ -98,8 +99,9 @@ struct TcParams {
   int gh;                   // vector-gate hidden width (0: the scalar gate)
   const float *gw1, *gc1, *gw2, *gc2;
   float* ws_P;              // [NP][r + 4]: (A x)[j] for j < r, w_g . x at j = r (16-byte rows)
-  unsigned* ws_sync;        // [0] producer row tiles published, [1] tile-CTA ticket
-  uint32_t off_bf, off_x16, off_xr, off_B, off_gate;   // dynamic shared memory layout
+  uint4* ws_T;              // [NP][r / 4]: T hi/lo, pairs (2q, 2q + 1) of token m at m r / 4 + q
+  unsigned* ws_sync;        // [0] producer row tiles published, [1] tile-CTA ticket, [2] T published
+  uint32_t off_bf, off_x16, off_xr, off_B;   // dynamic shared memory layout
   uint64_t t_wait_ns;       // limit of the wait for the published P
 };
 
@@ -109,6 +111,50 @@ __device__ __forceinline__ void give_up(int* abort_flag) {
 }
 
 // ------------------------------------------------------------- producers --
+// The producer CTA that publishes the last row tile of P forms T for every
+// token, with all of its threads and long before the tile CTAs need it:
+//   scalar gate  T[m] = alpha g_m t_m,        g_m = sigmoid(P[m][r] + b_g)
+//   vector gate  T[m] = alpha gamma(t_m) t_m  (the bottleneck MLP on t_m)
+// with t_m = P[m][0 .. r) and T = 0 for tokens m >= M, split into bf16 hi +
+// lo (T = hi + lo to ~2^-16 relative) in the pair order of the epilogue's
+// B operand, and published with ws_sync[2].
+template <int NP>
+__device__ __noinline__ void tc_form_T(const TcParams& p, uint8_t* smem) {
+  const int r = p.r, ps = r + 4, r4 = r / 4;
+  float* ts = reinterpret_cast<float*>(smem);               // [NP][r]
+  float* gl = ts + NP * r;                                   // [NP] gate logits (scalar gate)
+  float* gsm = gl + NP;                                      // gate weights (vector gate), 16-byte aligned
+  float* hid = gsm + (p.gh > 0 ? gate_smem_floats(r, p.gh) : 0);   // [NP][h | 1]
+  if (p.gh > 0) stage_gate_weights_async(p.gw1, p.gw2, p.gc1, p.gc2, r, p.gh, gsm, threadIdx.x, kThreads);
+  for (int e = threadIdx.x; e < NP * r4; e += kThreads)
+    reinterpret_cast<float4*>(ts)[e] = __ldcg(reinterpret_cast<const float4*>(p.ws_P + (size_t)(e / r4) * ps) + e % r4);
+  for (int m = threadIdx.x; m < NP; m += kThreads) gl[m] = __ldcg(p.ws_P + (size_t)m * ps + r);
+  if (p.gh > 0) cp_async_wait<0>();
+  __syncthreads();
+  if (p.gh > 0) {
+    const GateSmem g(gsm, r, p.gh);
+    vector_gate_hidden_rows(ts, NP, g, hid, threadIdx.x, kThreads);
+    __syncthreads();
+    vector_gate_apply_rows(ts, NP, g, hid, threadIdx.x, kThreads);     // t *= gamma(t)
+    __syncthreads();
+  }
+  for (int e = threadIdx.x; e < NP * r4; e += kThreads) {
+    const int m = e / r4;
+    const float gm = m >= p.M ? 0.0f : p.gh > 0 ? p.alpha : p.alpha / (1.0f + expf(-(gl[m] + p.b_g)));
+    const float4 tv = reinterpret_cast<const float4*>(ts)[e];
+    const float t0 = gm * tv.x, t1 = gm * tv.y, t2 = gm * tv.z, t3 = gm * tv.w;
+    const float h0 = __bfloat162float(__float2bfloat16_rn(t0)), h1 = __bfloat162float(__float2bfloat16_rn(t1));
+    const float h2 = __bfloat162float(__float2bfloat16_rn(t2)), h3 = __bfloat162float(__float2bfloat16_rn(t3));
+    __stcg(p.ws_T + e, make_uint4(pack_bf16x2(h0, h1), pack_bf16x2(t0 - h0, t1 - h1),
+                                  pack_bf16x2(h2, h3), pack_bf16x2(t2 - h2, t3 - h3)));
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    atomicExch(&p.ws_sync[2], 1u);
+  }
+}
+
 // Producer cluster rt (a 16-row tile of [A; w_g]): CTA `rank` of it covers K
 // slice `rank` of S (128-k chunks).  Lane (g, c) of a warp loads
 // 8 consecutive k of a projection row and of a token; both operands use the
@@ -209,10 +255,14 @@ __device__ void tc_producer(const TcParams& p, uint8_t* smem, int rt, int rank) 
       if (i <= p.r) p.ws_P[(size_t)tok * (p.r + 4) + i] = v;
     }
     __syncthreads();
+    __shared__ int s_last;
     if (threadIdx.x == 0) {
       __threadfence();
-      atomicAdd(&p.ws_sync[0], 1u);
+      s_last = atomicAdd(&p.ws_sync[0], 1u) == (unsigned)(p.RT - 1);
+      __threadfence();                                     // every row tile of P is visible from here
     }
+    __syncthreads();
+    if (s_last) tc_form_T<NP>(p, smem);                    // this CTA's shared memory is no longer read
   }
   cluster_sync();                                          // peers keep their shared memory until read
 }
@@ -317,7 +367,6 @@ __device__ void tc_tile(const CUtensorMap* tm_w, const CUtensorMap* tm_x, const 
   uint8_t* x16_ring = smem + p.off_x16;                    // [3][64 tokens][128 B] fp16 tokens
   uint8_t* xr_ring = smem + p.off_xr;                      // [2][NP tokens][128 B] bf16 tokens (TMA)
   uint8_t* B_s = smem + p.off_B;                           // [nr][2r + 16 bytes]
-  float* gate_s = reinterpret_cast<float*>(smem + p.off_gate);   // vector gate: W1, W2, c1, c2
   // after the main loop: the partial [64 tokens][260] over the raw ring and
   // the start of the weight ring
   float* red = reinterpret_cast<float*>(smem);
@@ -326,10 +375,6 @@ __device__ void tc_tile(const CUtensorMap* tm_w, const CUtensorMap* tm_x, const 
   // ring once the last token tile is converted (NP r 4 <= 2 NP 128 bytes);
   // element (m, jj) holds the hi and the lo bf16 pair of T[m][2jj .. 2jj+1]
   uint2* thl_s = reinterpret_cast<uint2*>(xr_ring);                 // [NP][r/2]
-  // vector gate: t [NP][r] fp32 over the same bytes, turned into T hi/lo in
-  // place; the hidden units in static memory
-  float* ts = reinterpret_cast<float*>(xr_ring);
-  __shared__ float hs[NP * gate_hid_stride(32)];                    // [NP][h | 1]
   const int b_stride = 2 * p.r + 16;
 
   if (threadIdx.x == 0) {
@@ -369,9 +414,6 @@ __device__ void tc_tile(const CUtensorMap* tm_w, const CUtensorMap* tm_x, const 
     }
     for (int r = threadIdx.x; r < kTileRows; r += kXWarps * 32)
       s_scale[r] = (PERCH && n0 + r < p.N) ? __half2float(__ldg(p.scales + (size_t)(n0 + r) * p.ng)) : 1.0f;
-    // the vector gate's weights, copied while the K loop runs
-    if (COMP && p.gh > 0)
-      stage_gate_weights_async(p.gw1, p.gw2, p.gc1, p.gc2, p.r, p.gh, gate_s, threadIdx.x, kXWarps * 32);
   }
   tc_fence_before();
   __syncthreads();
@@ -642,13 +684,13 @@ __device__ void tc_tile(const CUtensorMap* tm_w, const CUtensorMap* tm_x, const 
     if (lane == 0) mbar_arrive(smem_u32(&acc_full));      // the overflow flags are in place
 
     if (COMP) {
-      // the published P: gate per token, then T = alpha g P (P read straight
-      // from the workspace, every load of a thread in flight together)
+      // T hi/lo as the last producer published it, copied into the spent
+      // token ring (one round trip: every load of a thread in flight together)
       if (tid == 0) {
         const uint64_t tw = globaltimer_ns();
         int pok = 0;
         for (unsigned i = 0;; ++i) {
-          if (ld_acquire_gpu(&p.ws_sync[0]) >= (unsigned)p.RT) { pok = 1; break; }
+          if (ld_acquire_gpu(&p.ws_sync[2]) != 0u) { pok = 1; break; }
           if ((i & 63) == 63 && globaltimer_ns() - tw > p.t_wait_ns) break;
           __nanosleep(64);
         }
@@ -659,52 +701,19 @@ __device__ void tc_tile(const CUtensorMap* tm_w, const CUtensorMap* tm_x, const 
         ticket = atomicAdd(&p.ws_sync[1], 1u);
       }
       named_sync(1, kXWarps * 32);
-      // one round trip: every thread loads its (token, 4-component) pieces of
-      // P as 16-byte loads (the rows are r + 4 floats), and for the scalar
-      // gate the token's gate logit, all in flight together; no load is
-      // conditional (indexes past the end re-read the last piece) and no
-      // index needs a division
       const bool pok = s_pok != 0;
-      const int ps = p.r + 4, r4 = p.r >> 2, lr4 = __ffs(r4) - 1;   // r4 = 4, 8 or 16
-      const int nq = NP << lr4;                             // (token, piece) items
-      constexpr int kPerQ = 4;                             // pieces per thread and pass
-      for (int e0 = 0; e0 < nq; e0 += kPerQ * kXWarps * 32) {
-        float4 v[kPerQ];
-        float gl[kPerQ];
+      const int n4 = NP * p.r / 4;                         // 16-byte pieces of T hi/lo
+      constexpr int kPerQ = 4;
+      for (int e0 = 0; e0 < n4; e0 += kPerQ * kXWarps * 32) {
+        uint4 v[kPerQ];
 #pragma unroll
-        for (int i = 0; i < kPerQ; ++i) {
-          const int e = min(e0 + tid + i * kXWarps * 32, nq - 1);
-          const float* row = p.ws_P + (size_t)(e >> lr4) * ps;
-          v[i] = __ldcg(reinterpret_cast<const float4*>(row) + (e & (r4 - 1)));
-          gl[i] = p.gh == 0 ? __ldcg(row + p.r) : 0.0f;
-        }
+        for (int i = 0; i < kPerQ; ++i) v[i] = __ldcg(p.ws_T + min(e0 + tid + i * kXWarps * 32, n4 - 1));
 #pragma unroll
         for (int i = 0; i < kPerQ; ++i) {
           const int e = e0 + tid + i * kXWarps * 32;
-          if (e >= nq) break;
-          if (!pok) v[i] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);      // P never arrived
-          if (p.gh > 0) {
-            // vector gate: t = P [NP][r] into the token ring now; gamma(t) and
-            // T (over the same bytes) are formed by warps 0-19 once the
-            // accumulator is drained
-            reinterpret_cast<float4*>(ts)[e] = v[i];
-          } else {
-            // T = alpha g P for four components, as two hi/lo pairs: the
-            // 16 bytes of elements (m, 2q) and (m, 2q + 1) of thl_s
-            const float gt = (pok && (e >> lr4) < p.M) ? p.alpha / (1.0f + expf(-(gl[i] + p.b_g))) : 0.0f;
-            const float t0 = gt * v[i].x, t1 = gt * v[i].y, t2 = gt * v[i].z, t3 = gt * v[i].w;
-            const float h0 = __bfloat162float(__float2bfloat16_rn(t0)), h1 = __bfloat162float(__float2bfloat16_rn(t1));
-            const float h2 = __bfloat162float(__float2bfloat16_rn(t2)), h3 = __bfloat162float(__float2bfloat16_rn(t3));
-            reinterpret_cast<uint4*>(thl_s)[e] = make_uint4(pack_bf16x2(h0, h1), pack_bf16x2(t0 - h0, t1 - h1),
-                                                            pack_bf16x2(h2, h3), pack_bf16x2(t2 - h2, t3 - h3));
-          }
+          if (e < n4) reinterpret_cast<uint4*>(thl_s)[e] = pok ? v[i] : make_uint4(0u, 0u, 0u, 0u);
         }
       }
-      if (p.gh > 0) cp_async_wait<0>();                   // the staged gate weights (published by the barrier below)
-      named_sync(1, kXWarps * 32);
-      // vector gate: its hidden units from t here, while the last MMAs and the
-      // drain run (gamma and T follow the drain on all warps)
-      if (p.gh > 0) vector_gate_hidden_rows(ts, NP, GateSmem(gate_s, p.r, p.gh), hs, tid, kXWarps * 32);
     }
   }
 
@@ -714,45 +723,7 @@ __device__ void tc_tile(const CUtensorMap* tm_w, const CUtensorMap* tm_x, const 
     // before the cluster reads it: one (16-row, 8-token) tile per warp at a
     // time on mma.sync (B rows as A, T hi/lo as B).  Warps 0-19 only: the
     // TMA and MMA warps never reach this barrier.
-    named_sync(2, kTmaWarp * 32);                          // drained partial, T (or t) and B rows in place
-    if (p.gh > 0) {
-      // vector gate over warps 0-19 (the token warps formed the hidden units):
-      // T = alpha gamma(t) t, each pair of t turned into its hi/lo pair in
-      // place (uniform branch: the barrier below is reached by all 640 threads)
-      constexpr int kEpi = kTmaWarp * 32;
-      const GateSmem gt(gate_s, p.r, p.gh);
-      // gamma for four rank components of one token per thread, and T = alpha
-      // gamma t for them turned into two hi/lo pairs over the same 16 bytes
-      const bool pok = s_pok != 0;
-      const int r4 = p.r / 4, hstr = gate_hid_stride(p.gh);
-      for (int e = threadIdx.x; e < NP * r4; e += kEpi) {
-        const int m = e / r4, q = e % r4;
-        float4 a = reinterpret_cast<const float4*>(gt.c2)[q];
-        const float* hh = hs + m * hstr;
-#pragma unroll 4
-        for (int i = 0; i < p.gh; ++i) {
-          const float4 wv = reinterpret_cast<const float4*>(gt.W2t + i * p.r)[q];
-          const float hv = hh[i];
-          a.x = fmaf(wv.x, hv, a.x);
-          a.y = fmaf(wv.y, hv, a.y);
-          a.z = fmaf(wv.z, hv, a.z);
-          a.w = fmaf(wv.w, hv, a.w);
-        }
-        const bool on = pok && m < p.M;
-        float4* tp = reinterpret_cast<float4*>(ts + m * p.r) + q;
-        const float4 tv = *tp;
-        const float t0 = on ? p.alpha * tv.x / (1.0f + expf(-a.x)) : 0.0f;
-        const float t1 = on ? p.alpha * tv.y / (1.0f + expf(-a.y)) : 0.0f;
-        const float t2 = on ? p.alpha * tv.z / (1.0f + expf(-a.z)) : 0.0f;
-        const float t3 = on ? p.alpha * tv.w / (1.0f + expf(-a.w)) : 0.0f;
-        const float h0 = __bfloat162float(__float2bfloat16_rn(t0)), h1 = __bfloat162float(__float2bfloat16_rn(t1));
-        const float h2 = __bfloat162float(__float2bfloat16_rn(t2)), h3 = __bfloat162float(__float2bfloat16_rn(t3));
-        // pairs (m, 2q) and (m, 2q + 1) of T hi/lo: the 16 bytes read above
-        *reinterpret_cast<uint4*>(tp) = make_uint4(pack_bf16x2(h0, h1), pack_bf16x2(t0 - h0, t1 - h1),
-                                                   pack_bf16x2(h2, h3), pack_bf16x2(t2 - h2, t3 - h3));
-      }
-      named_sync(2, kEpi);
-    }
+    named_sync(2, kTmaWarp * 32);                          // drained partial, T and B rows in place
     if (!s_abort) {
       const int g = lane >> 2, c = lane & 3;
       const int rtiles = nr / 16, ttiles = (p.M + 7) / 8;
@@ -826,6 +797,7 @@ __device__ void tc_tile(const CUtensorMap* tm_w, const CUtensorMap* tm_x, const 
   }
   if (COMP && threadIdx.x == 0 && ticket == (unsigned)(p.n_consumers - 1)) {   // every tile CTA has seen P
     p.ws_sync[1] = 0;
+    p.ws_sync[2] = 0;
     atomicExch(&p.ws_sync[0], 0u);
   }
   tc_fence_before();
@@ -879,14 +851,14 @@ struct TcPlan {
   int device, N, K, G, rank, comp, NP, gh;     // key
   int S, RT, tiles, units, BF;
   size_t smem;
-  uint32_t off_bf, off_x16, off_xr, off_B, off_gate;
-  size_t off_sync, off_P, total;
+  uint32_t off_bf, off_x16, off_xr, off_B;
+  size_t off_sync, off_P, off_T, total;
   TcKernel fn;
 };
 
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
-size_t tile_smem(int NP, int BF, int nr_max, int rank, int gate_floats, TcPlan* c) {
+size_t tile_smem(int NP, int BF, int nr_max, int rank, TcPlan* c) {
   size_t off = (size_t)kRawStages * kRawBytes;
   c->off_bf = (uint32_t)off;
   off += (size_t)BF * kBfBytes;
@@ -896,15 +868,12 @@ size_t tile_smem(int NP, int BF, int nr_max, int rank, int gate_floats, TcPlan* 
   off += (size_t)kXrStages * NP * 128;
   c->off_B = (uint32_t)off;
   off += (size_t)align_up(nr_max, 16) * (2 * std::max(rank, 8) + 16);   // whole 16-row MMA tiles
-  c->off_gate = (uint32_t)off;
-  off += (size_t)gate_floats * 4;
   return align_up(off, 1024) + 1024;            // + alignment slack of the dynamic base
 }
 
 int build_tc_plan(const spear_w4_layer& L, int NP, bool comp, const DeviceInfo& di, TcPlan* pl) {
   const bool has_rank = L.rank > 0;             // the split depends on this, not on comp_enabled
   const bool perch = L.group_size == L.K;
-  const int gate_floats = (comp && L.gate_hidden > 0) ? gate_smem_floats(L.rank, L.gate_hidden) : 0;
   pl->NP = NP;
   pl->tiles = (L.N + kTileRows - 1) / kTileRows;
   pl->units = (L.K + kUnitK - 1) / kUnitK;
@@ -912,7 +881,11 @@ int build_tc_plan(const spear_w4_layer& L, int NP, bool comp, const DeviceInfo& 
   pl->fn = pick_tc(NP, perch, comp);
 
   // Producer smem: [NW][MT][4][32] + [16][NP] floats
-  const size_t prod_smem = ((size_t)(kThreads / 32) * (NP / 8) * 128 + 16 * NP) * 4 + 1024;
+  // (the last producer then forms T over the same bytes: t [NP][r], the gate
+  // logits, the vector gate's weights and hidden units)
+  const int gh = comp ? L.gate_hidden : 0;
+  const size_t form_T_floats = (size_t)NP * (L.rank + 1) + (gh > 0 ? gate_smem_floats(L.rank, gh) + NP * gate_hid_stride(gh) : 0);
+  const size_t prod_smem = std::max(((size_t)(kThreads / 32) * (NP / 8) * 128 + 16 * NP), form_T_floats) * 4 + 1024;
   // the dynamic shared memory a CTA may take next to the kernel's static arrays
   cudaFuncAttributes fa{};
   if (cudaFuncGetAttributes(&fa, pl->fn) != cudaSuccess) return fail(SPEAR_ERR_CUDA, "decode: cudaFuncGetAttributes failed");
@@ -933,10 +906,10 @@ int build_tc_plan(const spear_w4_layer& L, int NP, bool comp, const DeviceInfo& 
     const int nr_max = (kTileRows + S - 1) / S;
     // three fp16 weight steps in flight when they fit, else two
     c.BF = kMaxBfStages;
-    size_t sm = tile_smem(NP, c.BF, nr_max, L.rank, gate_floats, &c);
+    size_t sm = tile_smem(NP, c.BF, nr_max, L.rank, &c);
     if (sm > smem_limit) {
       c.BF = 2;
-      sm = tile_smem(NP, c.BF, nr_max, L.rank, gate_floats, &c);
+      sm = tile_smem(NP, c.BF, nr_max, L.rank, &c);
     }
     c.smem = std::max(sm, prod_smem);
     if (c.smem > smem_limit) continue;
@@ -987,8 +960,9 @@ int build_tc_plan(const spear_w4_layer& L, int NP, bool comp, const DeviceInfo& 
   *pl = best;
 
   size_t off = 0;
-  pl->off_sync = off; off = align_up(off + 2 * sizeof(unsigned), 256);
+  pl->off_sync = off; off = align_up(off + 3 * sizeof(unsigned), 256);
   pl->off_P = off;    off = align_up(off + (size_t)NP * (std::max(L.rank, 1) + 4) * 4, 256);
+  pl->off_T = off;    off = align_up(off + (size_t)NP * std::max(L.rank, 1) * 4, 256);
   pl->total = off;
   return SPEAR_OK;
 }
@@ -998,7 +972,7 @@ int get_tc_plan(const spear_w4_layer& L, int M, TcPlan* out) {
   if (int rc = device_info(&di)) return rc;
   const int NP = np_for(M);
   const int comp = (L.comp_enabled && L.rank > 0) ? 1 : 0;
-  const int gh = comp ? L.gate_hidden : 0;     // the vector gate's staged weights take shared memory
+  const int gh = comp ? L.gate_hidden : 0;     // the last producer's shared memory holds the vector gate
   static std::mutex mu;
   static std::vector<TcPlan> cache;
   std::lock_guard<std::mutex> lk(mu);
@@ -1063,8 +1037,9 @@ int launch_decode_tc(const spear_w4_layer& L, const uint16_t* x, int M, void* y,
   char* base = reinterpret_cast<char*>(ws);
   p.ws_sync = reinterpret_cast<unsigned*>(base + pl.off_sync);
   p.ws_P = reinterpret_cast<float*>(base + pl.off_P);
+  p.ws_T = reinterpret_cast<uint4*>(base + pl.off_T);
   p.t_wait_ns = wait_limit_ns(kTWaitNs);
-  p.off_bf = pl.off_bf; p.off_x16 = pl.off_x16; p.off_xr = pl.off_xr; p.off_B = pl.off_B; p.off_gate = pl.off_gate;
+  p.off_bf = pl.off_bf; p.off_x16 = pl.off_x16; p.off_xr = pl.off_xr; p.off_B = pl.off_B;
 
   if (int rc = ensure_smem_limit(reinterpret_cast<const void*>(pl.fn), pl.smem)) return rc;
   cudaLaunchConfig_t cfg{};

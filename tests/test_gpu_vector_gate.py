@@ -2,7 +2,7 @@
 weight W + alpha B diag(gamma(A x)) A, gamma a bottleneck MLP; read as
 gamma(t) = sigmoid(W2 relu(W1 t + c1) + c2)) against the oracle's
 linear_vector_gate: decode on the warp-level kernel (1, 5, 12 tokens) and the
-tensor-core kernel (24, 64 tokens), prefill on 128- and 256-token tiles in
+tensor-core kernel (20-64 tokens, ranks 16, 32 and 64), prefill on 128- and 256-token tiles in
 both modes; no w_g is given."""
 import dataclasses
 
@@ -39,6 +39,12 @@ def _layers(N, K, G, sym, r, h, seed):
     (256, 2048, 128, False, 16, 4, 12),      # two token tiles
     (320, 1152, 128, False, 64, 16, 24),     # tensor-core kernel, 32 token rows
     (256, 1024, 1024, True, 32, 32, 64),     # tensor-core kernel, per-channel scales
+    # tensor-core kernel: the gate's lanes per token and pieces per lane for
+    # each rank, hidden widths that are not multiples of 8
+    (512, 1024, 128, False, 16, 5, 40),      # 2 lanes per token, 2 pieces each
+    (384, 2048, 128, False, 64, 9, 64),      # 8 pieces per lane, two hidden chunks
+    (256, 1024, 128, False, 16, 3, 20),      # 4 lanes per token, 1 piece each
+    (320, 1536, 128, True, 32, 12, 33),      # 2 lanes per token, 4 pieces each
 ])
 def test_decode_vector_gate_matches_oracle(N, K, G, sym, r, h, M):
     from quantized_gemm_error_gb300 import spear
