@@ -137,7 +137,8 @@ spear_status spear_pack_w4(const float* W, int N, int K, int group_size, int sym
  *   x : device bf16 [M][K];  y : device [M][N], bf16 or fp32 (out_dtype).
  * M <= 16 runs on warp-level MMAs; M >= 17 on the tcgen05 tensor cores.
  * The thread blocks of the launch exchange the M x (rank+1) down-projection
- * through `workspace` (device, at least spear_decode_workspace_bytes()).
+ * and the gated term T derived from it through `workspace` (device, at least
+ * spear_decode_workspace_bytes()).
  * The workspace must be zeroed once before its first use
  * (spear_workspace_init) and is left ready for the next call; two calls that
  * run at the same time must not share one.  After a SPEAR_ERR_TIMEOUT device

@@ -76,7 +76,7 @@ constexpr int kTmaWarp = 20, kMmaWarp = 21;
 constexpr int kThreads = 704;
 constexpr int kMaxS = 8;
 constexpr uint64_t kPipeWaitNs = 2000ull * 1000 * 1000;   // 2 s: far beyond any legitimate wait
-constexpr uint64_t kTWaitNs = 200ull * 1000 * 1000;       // 200 ms for the published P
+constexpr uint64_t kTWaitNs = 200ull * 1000 * 1000;       // 200 ms for the published T
 
 struct TcParams {
   int N, K, M, ng, sym;
@@ -102,7 +102,7 @@ struct TcParams {
   uint4* ws_T;              // [NP][r / 4]: T hi/lo, pairs (2q, 2q + 1) of token m at m r / 4 + q
   unsigned* ws_sync;        // [0] producer row tiles published, [1] tile-CTA ticket, [2] T published
   uint32_t off_bf, off_x16, off_xr, off_B;   // dynamic shared memory layout
-  uint64_t t_wait_ns;       // limit of the wait for the published P
+  uint64_t t_wait_ns;       // limit of the wait for the published T
 };
 
 __device__ __forceinline__ void give_up(int* abort_flag) {
