@@ -269,12 +269,13 @@ def run_reference(args, world, rank):
     if rank != 0:
         return
     nthreads = host_threads()
-    # size each step's sample so the whole run stays within about two minutes
+    # size each step's sample so the whole run stays within --ref-budget-s
+    # (two minutes by default)
     probe_L, probe_x = oracle_case(4096, 4096, 1, seed=1)
     rows = np.arange(64, dtype=np.int32)
     dt, _ = time_oracle([(probe_L, probe_x, rows)], nthreads)
     per_row_m1 = dt / 64
-    budget = 120.0 / max(1, args.steps + args.warmup)
+    budget = args.ref_budget_s / max(1, args.steps + args.warmup)
     cases = []
     for (K, N) in DECODE_SHAPES:
         for M in DECODE_M:
@@ -286,16 +287,30 @@ def run_reference(args, world, rank):
     rng = np.random.default_rng(0)
     step_cases = [(L, x, np.sort(rng.choice(L["N"], rows_per_case, replace=False)).astype(np.int32))
                   for L, x in cases]
-    for _ in range(args.warmup):
-        time_oracle(step_cases, nthreads)
+    # every call also forms its tokens' rank-r code over all of K, whatever
+    # rows it covers: when even one row per call does not fit a step's share
+    # of the time, a step takes a rotating block of the 12 calls instead
+    per_call = len(step_cases)
+    if rows_per_case == 1:
+        t_full, _ = time_oracle(step_cases, nthreads)
+        if t_full > budget:
+            per_call = max(1, int(len(step_cases) * budget / t_full))
+    blocks = [[step_cases[(i + j) % len(step_cases)] for j in range(per_call)]
+              for i in range(0, len(step_cases), per_call)]
+    for i in range(args.warmup):
+        time_oracle(blocks[i % len(blocks)], nthreads)
     total_s, total_b = 0.0, 0.0
-    for _ in range(args.steps):
-        s, b = time_oracle(step_cases, nthreads)
+    for i in range(args.steps):
+        s, b = time_oracle(blocks[i % len(blocks)], nthreads)
         total_s += s
         total_b += b
     value = total_b / total_s / 1e9
-    sample = (f"each step: the 12 decode calls of the step on {rows_per_case} seeded output rows per "
-              f"call, fp64 accumulation")
+    if per_call == len(step_cases):
+        sample = (f"each step: the 12 decode calls of the step on {rows_per_case} seeded output rows per "
+                  f"call, fp64 accumulation")
+    else:
+        sample = (f"each step: {per_call} of the step's 12 decode calls in rotation, {rows_per_case} seeded "
+                  f"output row per call, fp64 accumulation")
     print(json.dumps({
         "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_s / args.steps * 1e3,
@@ -931,6 +946,8 @@ def main():
     ap.add_argument("--steps", type=int, default=20000)
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--ref-budget-s", type=float, default=120.0,
+                    help="host seconds the reference arm aims to spend over all its steps")
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extra", action="store_true",
