@@ -507,42 +507,87 @@ def run_ours(args, world, rank, local):
         y_off[(K, N, M)] = yo
         xo += M * K
         yo += M * N
+    # two slots of device buffers (and of host outputs), so that a step's
+    # inputs can travel in while the step before it computes and its outputs
+    # travel out while the step after it computes, as a serving loop would
+    # pipeline them: every step still copies its own inputs from pinned host
+    # memory and reads its own outputs back inside the timed region
     h_x = torch.empty(xo, dtype=torch.bfloat16).pin_memory()
-    h_y = torch.empty(yo, dtype=torch.bfloat16).pin_memory()
-    d_x = torch.empty(xo, dtype=torch.bfloat16, device=device)
-    d_y = torch.empty(yo, dtype=torch.bfloat16, device=device)
+    h_y = [torch.empty(yo, dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+    d_x = [torch.empty(xo, dtype=torch.bfloat16, device=device) for _ in range(2)]
+    d_y = [torch.empty(yo, dtype=torch.bfloat16, device=device) for _ in range(2)]
     for (K, N, M) in call_list:
         h_x[x_off[(K, N, M)]:x_off[(K, N, M)] + M * K].copy_(xs_dev[(K, M)].reshape(-1).cpu())
     h2d, d2h = xo * 2, yo * 2
     torch.cuda.synchronize()
-    e2e_graphs = []
+    # the 12 calls of a step, one graph per (weight-copy phase, slot)
+    e2e_graphs = {}
     for t in range(nphase):
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=stream):
-            d_x.copy_(h_x, non_blocking=True)
-            for (K, N, M) in call_list:
-                L = layer_of(step_copy(t, DECODE_M.index(M), ncopy), K, N)
-                xv = d_x[x_off[(K, N, M)]:x_off[(K, N, M)] + M * K].view(M, K)
-                yv = d_y[y_off[(K, N, M)]:y_off[(K, N, M)] + M * N].view(M, N)
-                spear.spear_linear_decode(L, xv, y=yv, workspace=ws, stream=stream)
-            h_y.copy_(d_y, non_blocking=True)
-        e2e_graphs.append(g)
+        for sl in range(2):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for (K, N, M) in call_list:
+                    L = layer_of(step_copy(t, DECODE_M.index(M), ncopy), K, N)
+                    xv = d_x[sl][x_off[(K, N, M)]:x_off[(K, N, M)] + M * K].view(M, K)
+                    yv = d_y[sl][y_off[(K, N, M)]:y_off[(K, N, M)] + M * N].view(M, N)
+                    spear.spear_linear_decode(L, xv, y=yv, workspace=ws, stream=stream)
+            e2e_graphs[(t, sl)] = g
+    s_in, s_out = torch.cuda.Stream(device=device), torch.cuda.Stream(device=device)
+    ev = lambda: torch.cuda.Event()
+    computed = [ev(), ev()]                # slot's last compute done
+    arrived = [ev(), ev()]                 # slot's inputs in place
+    returned = [ev(), ev()]                # slot's outputs read back
+
+    def e2e_run(nsteps):
+        for sl in range(2):                # every slot free
+            computed[sl].record(stream)
+            returned[sl].record(s_out)
+        for i in range(nsteps):
+            sl = i % 2
+            s_in.wait_event(computed[sl])                  # the step two back is done with this slot
+            with torch.cuda.stream(s_in):
+                d_x[sl].copy_(h_x, non_blocking=True)
+            arrived[sl].record(s_in)
+            stream.wait_event(arrived[sl])
+            stream.wait_event(returned[sl])                # its outputs two steps back are read
+            with torch.cuda.stream(stream):
+                e2e_graphs[(i % nphase, sl)].replay()
+            computed[sl].record(stream)
+            s_out.wait_event(computed[sl])
+            with torch.cuda.stream(s_out):
+                h_y[sl].copy_(d_y[sl], non_blocking=True)
+            returned[sl].record(s_out)
+        stream.wait_event(returned[(nsteps - 1) % 2])
+        stream.wait_event(returned[nsteps % 2])
+
     e2e_steps = max(3, min(args.steps, 2000))
-    with torch.cuda.stream(stream):
-        for g in e2e_graphs:
-            g.replay()
+    e2e_run(2 * nphase)
     torch.cuda.synchronize()
     barrier(world)
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):
-        a.record(stream)
-        for i in range(e2e_steps):
-            e2e_graphs[i % nphase].replay()
-        b.record(stream)
+    a.record(stream)
+    e2e_run(e2e_steps)
+    b.record(stream)
     torch.cuda.synchronize()
     e2e_ms = reduce_max(a.elapsed_time(b), world)
     e2e_value = world * e2e_steps * step_bytes / (e2e_ms / 1e3) / 1e9
-    assert torch.equal(h_y[:N_CHECK].to(torch.float32), d_y[:N_CHECK].cpu().to(torch.float32))
+    last = (e2e_steps - 1) % 2
+    assert torch.equal(h_y[last][:N_CHECK].to(torch.float32), d_y[last][:N_CHECK].cpu().to(torch.float32))
+    # the same steps with each step's copies and calls in series on one
+    # stream (no overlap between steps), reported beside it
+    torch.cuda.synchronize()
+    barrier(world)
+    a.record(stream)
+    with torch.cuda.stream(stream):
+        for i in range(e2e_steps):
+            d_x[0].copy_(h_x, non_blocking=True)
+            e2e_graphs[(i % nphase, 0)].replay()
+            h_y[0].copy_(d_y[0], non_blocking=True)
+    b.record(stream)
+    torch.cuda.synchronize()
+    e2e_serial_value = world * e2e_steps * step_bytes / (reduce_max(a.elapsed_time(b), world) / 1e3) / 1e9
+    last = 0
+    assert torch.equal(h_y[last][:N_CHECK].to(torch.float32), d_y[last][:N_CHECK].cpu().to(torch.float32))
 
     prefill = None
     if not args.no_prefill:
@@ -598,7 +643,10 @@ def run_ours(args, world, rank, local):
                          "time_share": shares},
             "cpu_baseline": cpu,
             "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
-                    "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+                    "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+                    "copies": "every step's H2D and D2H inside the timed region, on two copy streams, "
+                              "overlapping the neighbouring steps' kernels (two buffer slots)",
+                    "serial_value": round(e2e_serial_value, 2)},
             "gpu_launches": args.steps * len(calls),
             "clocks": clk.summary(),
             "comp_overhead_step": round(tot_on / tot_off - 1, 4),
