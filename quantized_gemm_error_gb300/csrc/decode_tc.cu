@@ -268,6 +268,30 @@ __device__ void tc_producer(const TcParams& p, uint8_t* smem, int rt, int rank) 
 }
 
 // ---------------------------------------------------------- tile CTAs --
+// The K units (256 k) of tile CTA `rank` of a cluster of S: rank, rank + S,
+// rank + 2 S, ... (the cluster walks each row's bytes together); the last
+// unit of K may hold only 128 k.  When U = b S + q units leave q CTAs one unit
+// longer than the rest and 2 q <= S (and K has no such tail), each of those q
+// units is split: its CTA keeps the first 128 k and CTA q + j takes the second
+// 128 k as one more unit, so no CTA carries more than b + 1/2 units.
+struct TcUnits {
+  int n;          // units of this CTA
+  bool half;      // its last unit holds 128 k
+  int k0_extra;   // k of a second-half unit taken from another CTA (its last), or -1
+  int kbase, kstride;
+  __device__ TcUnits(int units, int K, int rank, int S) : kbase(rank * kUnitK), kstride(S * kUnitK) {
+    const int b = units / S, q = units % S;
+    const bool ktail = (K % kUnitK) != 0;
+    const bool split = !ktail && q > 0 && 2 * q <= S;
+    const bool takes = split && rank >= q && rank < 2 * q;
+    n = (units - rank + S - 1) / S + (takes ? 1 : 0);
+    half = (ktail && (units - 1) % S == rank) || (split && rank < 2 * q);
+    k0_extra = takes ? (b * S + rank - q) * kUnitK + kUnitK / 2 : -1;
+  }
+  __device__ int k0(int i) const { return (k0_extra >= 0 && i == n - 1) ? k0_extra : kbase + i * kstride; }
+  __device__ int len(int i) const { return (half && i == n - 1) ? kUnitK / 2 : kUnitK; }
+};
+
 // Rows n and n + 32 of the tile's partial for token t, computed in fp32 over
 // the CTA's K units from the int4 codes and the bf16 token: the path for a
 // token with a value beyond the fp16 range (the tensor core would see inf).
@@ -276,14 +300,14 @@ __device__ void tc_producer(const TcParams& p, uint8_t* smem, int rt, int rank) 
 // to the sum), so only the summation order differs from the tensor-core path.
 template <bool PERCH>
 __device__ __forceinline__ void tc_exact_rows(const TcParams& p, float* red, const float* s_scale, int n, int t,
-                                           int rank, int nunits) {
+                                           const TcUnits& us) {
   const int zrow = (p.ng + 1) / 2;
   const int row0 = n % kTileRows;
   const __nv_bfloat16* xt = p.x + (size_t)t * p.K;
   float acc[2] = {0.0f, 0.0f};
   bool nonfinite = false;
-  for (int i = 0; i < nunits; ++i) {
-    const int k0 = (rank + i * p.S) * kUnitK, k1 = min(p.K, k0 + kUnitK);
+  for (int i = 0; i < us.n; ++i) {
+    const int k0 = us.k0(i), k1 = min(p.K, k0 + us.len(i));
     for (int k = k0; k < k1; k += 32) {
       float xf[32];
 #pragma unroll
@@ -350,13 +374,11 @@ __device__ void tc_tile(const CUtensorMap* tm_w, const CUtensorMap* tm_x, const 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int S = p.S, BF = p.bf_stages;
   const int n0 = tile * kTileRows;
-  // K units of this CTA: rank, rank + S, rank + 2S, ... (the cluster walks
-  // each row's bytes together); the last unit of K may hold only 128 k
-  const int nunits = (p.units - rank + S - 1) / S;
-  const bool half_tail = (p.K % kUnitK) != 0 && (p.units - 1) % S == rank;
-  const int nsteps = 4 * nunits - (half_tail ? 2 : 0);     // 64-k steps (even)
+  // K units of this CTA (TcUnits)
+  const TcUnits us(p.units, p.K, rank, S);
+  const int nunits = us.n;
+  const int nsteps = 4 * nunits - (us.half ? 2 : 0);       // 64-k steps (even)
   const int ngroups = nsteps / 2;                          // 128-k groups
-  auto unit_of = [&](int i) { return rank + i * S; };      // global unit of local unit i
   // rows finished here: whole 16-row tiles, so every owner range starts on a
   // 16-byte boundary of the partial and of y
   const int e_r0 = 16 * (rank * (kTileRows / 16) / S), e_r1 = 16 * ((rank + 1) * (kTileRows / 16) / S);
@@ -427,7 +449,7 @@ __device__ void tc_tile(const CUtensorMap* tm_w, const CUtensorMap* tm_x, const 
     if (lane == 0) {
       prefetch_tmap(tm_w);
       prefetch_tmap(tm_x);
-      SPEAR_CHECK(&g_dtc_status, n0 < p.N && (nunits == 0 || unit_of(nunits - 1) * kUnitK < p.K));
+      SPEAR_CHECK(&g_dtc_status, n0 < p.N && (nunits == 0 || us.k0(nunits - 1) < p.K));
     }
     // the first weight units need no slot wait and read only the layer's
     // weights: issue them before waiting for the kernel ahead (overlapped launches)
@@ -436,7 +458,7 @@ __device__ void tc_tile(const CUtensorMap* tm_w, const CUtensorMap* tm_x, const 
       for (int i = 0; i < ri; ++i) {
         const uint32_t full = smem_u32(&raw_full[i]);
         mbar_arrive_expect_tx(full, kRawBytes);
-        tma_load_2d(smem_u32(raw_ring + i * kRawBytes), tm_w, unit_of(i) * (kUnitK / 2), n0, full);
+        tma_load_2d(smem_u32(raw_ring + i * kRawBytes), tm_w, us.k0(i) >> 1, n0, full);
       }
     }
     __syncwarp();
@@ -452,7 +474,7 @@ __device__ void tc_tile(const CUtensorMap* tm_w, const CUtensorMap* tm_x, const 
           if (mbar_test_wait(smem_u32(&raw_empty[slot]), ((ri / kRawStages) & 1) ^ 1)) {
             const uint32_t full = smem_u32(&raw_full[slot]);
             mbar_arrive_expect_tx(full, kRawBytes);
-            tma_load_2d(smem_u32(raw_ring + slot * kRawBytes), tm_w, unit_of(ri) * (kUnitK / 2), n0, full);
+            tma_load_2d(smem_u32(raw_ring + slot * kRawBytes), tm_w, us.k0(ri) >> 1, n0, full);
             prog |= 1u;
           }
         }
@@ -461,7 +483,7 @@ __device__ void tc_tile(const CUtensorMap* tm_w, const CUtensorMap* tm_x, const 
           if (mbar_test_wait(smem_u32(&xr_empty[slot]), ((xi / kXrStages) & 1) ^ 1)) {
             const uint32_t full = smem_u32(&xr_full[slot]);
             mbar_arrive_expect_tx(full, NP * 128);
-            tma_load_2d(smem_u32(xr_ring + slot * NP * 128), tm_x, unit_of(xi >> 2) * kUnitK + (xi & 3) * kStepK,
+            tma_load_2d(smem_u32(xr_ring + slot * NP * 128), tm_x, us.k0(xi >> 2) + (xi & 3) * kStepK,
                         0, full);
             prog |= 2u;
           }
@@ -523,7 +545,7 @@ __device__ void tc_tile(const CUtensorMap* tm_w, const CUtensorMap* tm_x, const 
     const int n = n0 + row;
     const bool row_ok = n < p.N;
     const int zrow = (p.ng + 1) / 2;
-    auto gidx = [&](int gl) { return PERCH ? 0 : 2 * unit_of(gl >> 1) + (gl & 1); };
+    auto gidx = [&](int gl) { return PERCH ? 0 : (us.k0(gl >> 1) >> 7) + (gl & 1); };
     // The prefetched registers hold the loaded zero-point byte and scale bits
     // as they are; the nibble is picked and the scale doubled where they are
     // used, so no instruction waits for the load before then.
@@ -632,7 +654,7 @@ __device__ void tc_tile(const CUtensorMap* tm_w, const CUtensorMap* tm_x, const 
       if (big16 != 0u) {
         __syncwarp();
         for (uint32_t b = big16; b != 0u; b &= b - 1u)
-          tc_exact_rows<PERCH>(p, red, s_scale, n0 + cb + lane, 16 * q + (__ffs(b) - 1), rank, nunits);
+          tc_exact_rows<PERCH>(p, red, s_scale, n0 + cb + lane, 16 * q + (__ffs(b) - 1), us);
       }
     } else {
       give_up(&s_abort);
@@ -897,7 +919,9 @@ int build_tc_plan(const spear_w4_layer& L, int NP, bool comp, const DeviceInfo& 
   for (int S = 1; S <= std::min(kMaxS, pl->units); ++S) {
     TcPlan c = *pl;
     c.S = S;
-    const int units_per = (pl->units + S - 1) / S;      // most units one CTA takes
+    // most 128-k halves one CTA takes (a split unit, see TcUnits, counts one)
+    const int ub = pl->units / S, uq = pl->units % S;
+    const int halves_per = 2 * ub + (uq == 0 ? 0 : (2 * uq <= S && L.K % kUnitK == 0) ? 1 : 2);
     // one producer cluster per 16-row tile of [A; w_g], its S CTAs splitting
     // K: splitting K further over more clusters shortens the producers' loop
     // but takes SMs from the tile clusters, and a larger S (fewer K steps per
@@ -949,7 +973,7 @@ int build_tc_plan(const spear_w4_layer& L, int NP, bool comp, const DeviceInfo& 
               fa.preferredShmemCarveout, smem_sm, regs_sm);
     }
     if (clusters > max_clusters) continue;       // every CTA must be resident at once
-    const int cost = units_per;
+    const int cost = halves_per;
     if (cost < best_cost) {
       best_cost = cost;
       best = c;

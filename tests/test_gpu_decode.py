@@ -39,6 +39,11 @@ def _run(layer, x_bits, out_dtype=0, ws=None):
     (256, 2048, 2048, True, 64, 32),
     (320, 1152, 128, False, 64, 33),
     (256, 1024, 1024, False, 32, 64),
+    # tensor-core kernel, K units not a multiple of the cluster: units split
+    # into halves between CTAs (11 units over clusters of 8, 9 over clusters
+    # of 6: three split each), group and per-channel scales
+    (512, 2816, 128, False, 32, 40),
+    (512, 2304, 2304, True, 32, 64),
     (1024, 1024, 128, True, 0, 5),          # rank 0: plain W4
 ])
 def test_decode_matches_oracle(N, K, G, sym, r, M):
@@ -181,6 +186,7 @@ def test_calls_without_a_workspace_reuse_one_per_stream():
     (512, 1024, 128, False, 32, 24),         # tensor-core kernel, fp16 token tiles
     (256, 1024, 1024, False, 32, 64),
     (512, 2048, 2048, True, 32, 40),         # tensor-core kernel, per-channel scales (the scale after the sum)
+    (512, 2816, 128, False, 32, 40),         # tensor-core kernel with split K units (fp32 rows over half units)
 ])
 def test_decode_activations_of_any_magnitude(N, K, G, sym, r, M):
     """Tokens with |x| up to ~1e6 (beyond fp16): the fp16 launches scale each
